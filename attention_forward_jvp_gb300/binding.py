@@ -1,0 +1,265 @@
+"""ctypes binding of the C ABI in include/attn_jvp.h.
+
+Argument marshalling only: shapes, strides and raw pointers of torch
+tensors are handed to ``libattn_jvp.so``; every arithmetic step runs in its
+CUDA kernels.  Outputs are allocated with torch (device memory plumbing).
+CPU (host) inputs are staged through the device: the host->device copies,
+the kernel and the device->host copies all run on the current stream.
+
+There is no fallback: if the library is missing or the GPU is absent the
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+EXPORTS = (
+    "attn_fwd_jvp",
+    "attn_fwd",
+    "attn_sync_check",
+    "attn_status_string",
+    "attn_launch_count",
+    "attn_set_wait_timeout_ns",
+    "attn_debug_skip_first_load",
+)
+
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+          3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT"}
+
+
+class AttnShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("M", ctypes.c_int32),
+                ("N", ctypes.c_int32), ("Dqk", ctypes.c_int32), ("Dv", ctypes.c_int32),
+                ("T", ctypes.c_int64), ("max_seq_len", ctypes.c_int32)]
+
+
+class AttnBias(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p), ("bias_stride", ctypes.c_int64 * 4),
+                ("mask", ctypes.c_void_p), ("mask_stride", ctypes.c_int64 * 4)]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """Open the library (once).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with attention_forward_jvp_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.attn_fwd_jvp.restype = i32
+    L.attn_fwd_jvp.argtypes = [ctypes.POINTER(AttnShape), vp, vp, vp, vp, vp, vp, vp,
+                               ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp, vp]
+    L.attn_fwd.restype = i32
+    L.attn_fwd.argtypes = [ctypes.POINTER(AttnShape), vp, vp, vp, vp,
+                           ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp]
+    L.attn_sync_check.restype = i32
+    L.attn_sync_check.argtypes = [vp]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_status_string.argtypes = [i32]
+    L.attn_launch_count.restype = ctypes.c_uint64
+    L.attn_launch_count.argtypes = []
+    L.attn_set_wait_timeout_ns.restype = None
+    L.attn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    L.attn_debug_skip_first_load.restype = None
+    L.attn_debug_skip_first_load.argtypes = [i32]
+    _LIB = L
+    return L
+
+
+def _check(status: int):
+    if status != 0:
+        raise AttnError(status, lib().attn_status_string(status).decode())
+
+
+def status_string(status: int) -> str:
+    return lib().attn_status_string(status).decode()
+
+
+def launch_count() -> int:
+    return int(lib().attn_launch_count())
+
+
+def sync_check(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise and return the device error status (0 = ok)."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(lib().attn_sync_check(ctypes.c_void_p(s.cuda_stream)))
+
+
+def set_wait_timeout_ns(ns: int):
+    lib().attn_set_wait_timeout_ns(int(ns))
+
+
+def debug_skip_first_load(enable: bool):
+    lib().attn_debug_skip_first_load(1 if enable else 0)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, dev):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, expected {dev}")
+
+
+def _describe(q, k, v, offsets, max_seq_len, bias, mask):
+    """Shape struct + bias struct (with the tensors kept alive)."""
+    sh = AttnShape()
+    keep = []
+    if offsets is None:
+        if q.dim() != 4:
+            raise ValueError("dense q must be [B, H, M, Dqk]")
+        B, H, M, Dqk = q.shape
+        N, Dv = k.shape[2], v.shape[3]
+        if tuple(k.shape) != (B, H, N, Dqk) or tuple(v.shape) != (B, H, N, Dv):
+            raise ValueError("k must be [B, H, N, Dqk] and v [B, H, N, Dv]")
+        sh.B, sh.H, sh.M, sh.N, sh.Dqk, sh.Dv, sh.T, sh.max_seq_len = B, H, M, N, Dqk, Dv, 0, 0
+        out_shape = (B, H, M, Dv)
+    else:
+        if q.dim() != 3:
+            raise ValueError("jagged q must be [H, T, Dqk]")
+        if max_seq_len is None:
+            raise ValueError("jagged inputs need max_seq_len")
+        H, T, Dqk = q.shape
+        Dv = v.shape[2]
+        if tuple(k.shape) != (H, T, Dqk) or tuple(v.shape) != (H, T, Dv):
+            raise ValueError("k must be [H, T, Dqk] and v [H, T, Dv]")
+        sh.B, sh.H, sh.M, sh.N, sh.Dqk, sh.Dv = offsets.numel() - 1, H, 0, 0, Dqk, Dv
+        sh.T, sh.max_seq_len = T, int(max_seq_len)
+        out_shape = (H, T, Dv)
+    bs = None
+    if bias is not None or mask is not None:
+        if offsets is not None:
+            raise ValueError("bias / mask are supported for dense inputs only")
+        bs = AttnBias()
+        full = (sh.B, sh.H, sh.M, sh.N)
+        if bias is not None:
+            if bias.dtype != torch.float32 or bias.device != q.device:
+                raise TypeError("bias must be float32 on the inputs' device")
+            be = bias.expand(full)
+            bs.bias = be.data_ptr()
+            bs.bias_stride = (ctypes.c_int64 * 4)(*be.stride())
+            keep.append(be)
+        if mask is not None:
+            if mask.dtype == torch.bool:
+                mask = mask.view(torch.uint8)
+            if mask.dtype != torch.uint8 or mask.device != q.device:
+                raise TypeError("mask must be bool/uint8 on the inputs' device")
+            me = mask.expand(full)
+            bs.mask = me.data_ptr()
+            bs.mask_stride = (ctypes.c_int64 * 4)(*me.stride())
+            keep.append(me)
+    return sh, bs, out_shape, keep
+
+
+def _scale(sm_scale):
+    return float("nan") if sm_scale is None else float(sm_scale)
+
+
+def attn_fwd_jvp(q, k, v, tq, tk, tv, causal: bool = False, sm_scale: Optional[float] = None,
+                 offsets: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
+                 bias: Optional[torch.Tensor] = None, mask: Optional[torch.Tensor] = None,
+                 out=None):
+    """Attention forward + JVP in one pass.  Returns (o, to, lse).
+
+    Dense: q, tq [B, H, M, Dqk]; k, tk [B, H, N, Dqk]; v, tv [B, H, N, Dv].
+    Jagged: [H, T, D] with int32 ``offsets`` [B + 1] and ``max_seq_len``.
+    ``bias`` (fp32) and ``mask`` (bool/uint8, True = attend) broadcast to
+    [B, H, M, N].  CPU inputs are copied to the current CUDA device and the
+    outputs copied back (the end-to-end path); CUDA inputs stay on device.
+    """
+    if q.device.type == "cpu":
+        return _host_call(attn_fwd_jvp, (q, k, v, tq, tk, tv), dict(
+            causal=causal, sm_scale=sm_scale, offsets=offsets, max_seq_len=max_seq_len,
+            bias=bias, mask=mask), n_out=3)
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("tq", tq), ("tk", tk), ("tv", tv)):
+        _need(t, name, torch.bfloat16, dev)
+    if tq.shape != q.shape or tk.shape != k.shape or tv.shape != v.shape:
+        raise ValueError("tangents must have the primals' shapes")
+    if offsets is not None:
+        _need(offsets, "offsets", torch.int32, dev)
+    sh, bs, out_shape, keep = _describe(q, k, v, offsets, max_seq_len, bias, mask)
+    if out is None:
+        o = torch.empty(out_shape, dtype=torch.bfloat16, device=dev)
+        to = torch.empty(out_shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(out_shape[:-1], dtype=torch.float32, device=dev)
+    else:
+        o, to, lse = out
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    st = lib().attn_fwd_jvp(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(tq), _ptr(tk),
+                            _ptr(tv), _ptr(offsets), ctypes.byref(bs) if bs is not None else None,
+                            1 if causal else 0, _scale(sm_scale), _ptr(o), _ptr(to), _ptr(lse),
+                            ctypes.c_void_p(stream))
+    del keep
+    _check(st)
+    return o, to, lse
+
+
+def attn_fwd(q, k, v, causal: bool = False, sm_scale: Optional[float] = None,
+             offsets: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
+             bias: Optional[torch.Tensor] = None, mask: Optional[torch.Tensor] = None, out=None):
+    """Attention forward only.  Returns (o, lse)."""
+    if q.device.type == "cpu":
+        return _host_call(attn_fwd, (q, k, v), dict(
+            causal=causal, sm_scale=sm_scale, offsets=offsets, max_seq_len=max_seq_len,
+            bias=bias, mask=mask), n_out=2)
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, dev)
+    if offsets is not None:
+        _need(offsets, "offsets", torch.int32, dev)
+    sh, bs, out_shape, keep = _describe(q, k, v, offsets, max_seq_len, bias, mask)
+    if out is None:
+        o = torch.empty(out_shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(out_shape[:-1], dtype=torch.float32, device=dev)
+    else:
+        o, lse = out
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    st = lib().attn_fwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(offsets),
+                        ctypes.byref(bs) if bs is not None else None, 1 if causal else 0,
+                        _scale(sm_scale), _ptr(o), _ptr(lse), ctypes.c_void_p(stream))
+    del keep
+    _check(st)
+    return o, lse
+
+
+def _host_call(fn, tensors, kw, n_out):
+    """End-to-end path for host tensors: copy in, compute, copy out."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dt = [t.to(dev, non_blocking=True) for t in tensors]
+    for key in ("offsets", "bias", "mask"):
+        if kw.get(key) is not None:
+            kw[key] = kw[key].to(dev, non_blocking=True)
+    outs = fn(*dt, **kw)
+    host = tuple(torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs)
+    for h, o in zip(host, outs):
+        h.copy_(o, non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return host[:n_out]
+
+
+def default_scale(dqk: int) -> float:
+    return 1.0 / math.sqrt(dqk)

@@ -1,0 +1,273 @@
+// Host side of the C ABI declared in attn_jvp.h: argument validation,
+// bulk-tensor-copy descriptors, per-device scratch, kernel dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn_jvp.h"
+#include "attn_kernel.cuh"
+
+namespace attn {
+template <int DQK, int DV, bool JVP>
+cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream);
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  int* scratch = nullptr;  // [0] = error word
+  int num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_skip_first_load{0};
+
+attn_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (d.scratch == nullptr) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    int* p = nullptr;
+    if (cudaMalloc(&p, 256) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemset(p, 0, 256) != cudaSuccess) {
+      cudaFree(p);
+      return ATTN_ERR_CUDA;
+    }
+    d.scratch = p;
+    d.num_sms = sms;
+  }
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = &d;
+  return ATTN_OK;
+}
+
+// 3-D bf16 view [z][rows][d] (d innermost), box 64 x box_rows x 1,
+// 128-byte swizzle; rows past `rows` read as zeros.
+bool encode_map(CUtensorMap* m, const void* base, uint64_t d, uint64_t rows, uint64_t z,
+                uint32_t box_rows) {
+  cuuint64_t dims[3] = {d, rows, z};
+  cuuint64_t strides[2] = {d * 2, d * rows * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status run(const attn_shape* s, const void* q, const void* k, const void* v, const void* tq,
+                const void* tk, const void* tv, const int32_t* offsets, const attn_bias* bias,
+                int causal, float sm_scale, void* o, void* to, float* lse, void* stream,
+                bool jvp) {
+  if (s == nullptr) return ATTN_ERR_INVALID_ARG;
+  const bool jagged = offsets != nullptr;
+  if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0) return ATTN_ERR_INVALID_ARG;
+  if ((s->Dqk != 64 && s->Dqk != 128) || (s->Dv != 64 && s->Dv != 128))
+    return ATTN_ERR_UNSUPPORTED;
+  if (!std::isnan(sm_scale) && !(sm_scale > 0.f && std::isfinite(sm_scale)))
+    return ATTN_ERR_INVALID_ARG;
+  const bool has_bias = bias != nullptr && (bias->bias != nullptr || bias->mask != nullptr);
+  int64_t work_rows = 0;
+  if (jagged) {
+    if (s->T < 0 || s->T > 0x7fffffffLL || s->max_seq_len < 0) return ATTN_ERR_INVALID_ARG;
+    if (has_bias) return ATTN_ERR_UNSUPPORTED;  // bias / mask are dense-only
+    work_rows = (s->B > 0 && s->H > 0) ? s->T : 0;
+  } else {
+    if (s->M < 0 || s->N < 0) return ATTN_ERR_INVALID_ARG;
+    if (causal && s->M != s->N) return ATTN_ERR_INVALID_ARG;
+    work_rows = static_cast<int64_t>(s->B) * s->H * s->M;
+    if (static_cast<int64_t>(s->B) * s->H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  }
+  if (work_rows == 0) return ATTN_OK;  // nothing to compute or write
+  if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID_ARG;
+  const bool have_keys = jagged ? true : s->N > 0;
+  if (have_keys && (k == nullptr || v == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (jvp) {
+    if (tq == nullptr || to == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (have_keys && (tk == nullptr || tv == nullptr)) return ATTN_ERR_INVALID_ARG;
+  }
+  if (!aligned16(q) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+  if (have_keys && (!aligned16(k) || !aligned16(v))) return ATTN_ERR_MISALIGNED;
+  if (jvp && (!aligned16(tq) || !aligned16(to))) return ATTN_ERR_MISALIGNED;
+  if (jvp && have_keys && (!aligned16(tk) || !aligned16(tv))) return ATTN_ERR_MISALIGNED;
+  if (has_bias && bias->bias != nullptr && (reinterpret_cast<uintptr_t>(bias->bias) & 3u) != 0)
+    return ATTN_ERR_MISALIGNED;
+
+  DeviceState* ds = nullptr;
+  attn_status st = device_state(&ds);
+  if (st != ATTN_OK) return st;
+
+  attn::KernelParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  const float scale = std::isnan(sm_scale) ? 1.0f / std::sqrt(static_cast<float>(s->Dqk)) : sm_scale;
+  kp.B = s->B;
+  kp.H = s->H;
+  kp.jagged = jagged ? 1 : 0;
+  kp.causal = causal ? 1 : 0;
+  kp.sm_scale = scale;
+  kp.scale_log2 = scale * attn::kLog2e;
+  kp.offsets = offsets;
+  kp.o = static_cast<__nv_bfloat16*>(o);
+  kp.to = static_cast<__nv_bfloat16*>(to);
+  kp.lse = lse;
+  kp.err = ds->scratch;
+  kp.timeout_ns = g_timeout_ns.load();
+  kp.skip_first_load = g_skip_first_load.load();
+  if (has_bias) {
+    kp.bias = bias->bias;
+    kp.mask = bias->mask;
+    for (int i = 0; i < 4; ++i) {
+      kp.bias_stride[i] = bias->bias_stride[i];
+      kp.mask_stride[i] = bias->mask_stride[i];
+    }
+  }
+  const uint64_t dqk = s->Dqk, dvv = s->Dv;
+  bool ok = true;
+  if (jagged) {
+    kp.M = kp.N = s->max_seq_len;
+    kp.T = s->T;
+    kp.max_seq_len = s->max_seq_len;
+    kp.n_mt = (s->max_seq_len + attn::kBM - 1) / attn::kBM;
+    const uint64_t T = static_cast<uint64_t>(s->T), H = static_cast<uint64_t>(s->H);
+    ok = ok && encode_map(&kp.tm_q, q, dqk, T, H, attn::kBM);
+    ok = ok && encode_map(&kp.tm_k, k, dqk, T, H, attn::kBN);
+    ok = ok && encode_map(&kp.tm_v, v, dvv, T, H, attn::kBN);
+    if (jvp) {
+      ok = ok && encode_map(&kp.tm_tq, tq, dqk, T, H, attn::kBM);
+      ok = ok && encode_map(&kp.tm_tk, tk, dqk, T, H, attn::kBN);
+      ok = ok && encode_map(&kp.tm_tv, tv, dvv, T, H, attn::kBN);
+    }
+  } else {
+    kp.M = s->M;
+    kp.N = s->N;
+    kp.n_mt = (s->M + attn::kBM - 1) / attn::kBM;
+    const uint64_t BH = static_cast<uint64_t>(s->B) * s->H;
+    const uint64_t M = s->M;
+    // With no keys no key tile is ever loaded; the maps only need to be valid.
+    const uint64_t N = s->N > 0 ? static_cast<uint64_t>(s->N) : M;
+    const void* kb = s->N > 0 ? k : q;
+    const void* vb = s->N > 0 ? v : q;
+    const uint64_t dvk = s->N > 0 ? dvv : dqk;
+    ok = ok && encode_map(&kp.tm_q, q, dqk, M, BH, attn::kBM);
+    ok = ok && encode_map(&kp.tm_k, kb, dqk, N, BH, attn::kBN);
+    ok = ok && encode_map(&kp.tm_v, vb, dvk, N, BH, attn::kBN);
+    if (jvp) {
+      const void* tkb = s->N > 0 ? tk : tq;
+      const void* tvb = s->N > 0 ? tv : tq;
+      ok = ok && encode_map(&kp.tm_tq, tq, dqk, M, BH, attn::kBM);
+      ok = ok && encode_map(&kp.tm_tk, tkb, dqk, N, BH, attn::kBN);
+      ok = ok && encode_map(&kp.tm_tv, tvb, dvk, N, BH, attn::kBN);
+    }
+  }
+  if (!ok) return ATTN_ERR_CUDA;
+  const int64_t units = static_cast<int64_t>(s->B) * s->H * kp.n_mt;
+  if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  kp.num_units = static_cast<int>(units);
+  int grid = static_cast<int>(units < ds->num_sms ? units : ds->num_sms);
+  if (grid < 1) grid = 1;  // the jagged tail fill still runs
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaErrorInvalidValue;
+  const int key = (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
+  if (jvp) {
+    switch (key) {
+      case 0: e = attn::launch_attn<64, 64, true>(kp, grid, cs); break;
+      case 1: e = attn::launch_attn<64, 128, true>(kp, grid, cs); break;
+      case 2: e = attn::launch_attn<128, 64, true>(kp, grid, cs); break;
+      case 3: e = attn::launch_attn<128, 128, true>(kp, grid, cs); break;
+    }
+  } else {
+    switch (key) {
+      case 0: e = attn::launch_attn<64, 64, false>(kp, grid, cs); break;
+      case 1: e = attn::launch_attn<64, 128, false>(kp, grid, cs); break;
+      case 2: e = attn::launch_attn<128, 64, false>(kp, grid, cs); break;
+      case 3: e = attn::launch_attn<128, 128, false>(kp, grid, cs); break;
+    }
+  }
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd_jvp(const attn_shape* shape, const void* q, const void* k, const void* v,
+                         const void* tq, const void* tk, const void* tv, const int32_t* offsets,
+                         const attn_bias* bias, int causal, float sm_scale, void* o, void* to,
+                         float* lse, void* stream) {
+  return run(shape, q, k, v, tq, tk, tv, offsets, bias, causal, sm_scale, o, to, lse, stream,
+             true);
+}
+
+attn_status attn_fwd(const attn_shape* shape, const void* q, const void* k, const void* v,
+                     const int32_t* offsets, const attn_bias* bias, int causal, float sm_scale,
+                     void* o, float* lse, void* stream) {
+  return run(shape, q, k, v, nullptr, nullptr, nullptr, offsets, bias, causal, sm_scale, o,
+             nullptr, lse, stream, false);
+}
+
+attn_status attn_sync_check(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  DeviceState* ds = nullptr;
+  attn_status st = device_state(&ds);
+  if (st != ATTN_OK) return st;
+  int word = 0;
+  if (cudaMemcpy(&word, ds->scratch, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemset(ds->scratch, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration (head dims must be 64 or 128; bias/mask dense only)";
+    case ATTN_ERR_MISALIGNED: return "a device pointer is not 16-byte aligned";
+    case ATTN_ERR_CUDA: return "CUDA error (no device, launch failure or driver entry point missing)";
+    case ATTN_ERR_TIMEOUT: return "a device pipeline wait ran out of time; outputs are undefined";
+  }
+  return "unknown status";
+}
+
+uint64_t attn_launch_count(void) { return g_launches.load(); }
+
+void attn_set_wait_timeout_ns(uint64_t ns) {
+  g_timeout_ns.store(ns < 1000000ull ? 1000000ull : ns);
+}
+
+void attn_debug_skip_first_load(int enable) { g_skip_first_load.store(enable ? 1 : 0); }
+
+}  // extern "C"

@@ -1,0 +1,716 @@
+// Fused attention forward (+ JVP) for sm_103a: one persistent kernel
+// family, templated on the head dims and on whether tangents are carried.
+//
+// Method ("Flash Attention v2 with JVP", _attn_fwd_inner / _attn_fwd):
+// for a tile of 128 query rows, stream the keys in tiles of 64 and keep
+// per row a running max m, denominator l and tangent sum r, plus the
+// accumulators O_acc = sum p V and tO_acc = sum p tV + sum (p tS) V, where
+// p = exp2(x - m) and x = S * sm_scale * log2(e) (+ bias * log2(e)).
+// The epilogue writes O = O_acc / l, tO = (tO_acc - r O) / l and
+// LSE = (m + log2 l) ln 2.
+//
+// GB300 mapping (one CTA per SM, 6 warps):
+//   warp 0      bulk-tensor (TMA) producer: Q, tQ once per work unit; K, tK
+//               into a ring of NK stages; V, tV into a ring of NV stages.
+//   warp 1      tcgen05 issuer: S = Q K^T and tS = tQ K^T + Q tK^T into a
+//               double-buffered TMEM region, then O += P V and
+//               tO += P tV + H V with P, H (bf16) read back from TMEM --
+//               the K = 2*BN contraction [P | H] [tV ; V] issued as two
+//               accumulating runs into one tO accumulator.
+//   warps 2..5  softmax / rescale / epilogue, one query row per thread
+//               (TMEM lane = row).  Rescaling is lazy: m moves (and O, tO,
+//               l, r are multiplied by exp2(m_old - m_new)) only when the
+//               row maximum grows by more than kRescaleThreshold; the
+//               result is exact because l, r and both accumulators share
+//               the same stale reference.
+//   Work units (query tile, head, batch or sequence) are walked by every
+//   CTA with a static stride over a longest-first order.
+//
+// Every mbarrier wait is bounded: on expiry the thread records
+// ERR_TIMEOUT in the device error word, raises a CTA-wide abort flag and
+// all roles leave their loops; in-flight copies and MMAs are drained with
+// bounded waits before tensor memory is released.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kBM = 128;       // query rows per work unit (= TMEM lanes)
+constexpr int kBN = 64;        // keys per pipeline step
+constexpr int kThreads = 192;  // 6 warps
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
+constexpr int ERR_TIMEOUT = 1;
+
+struct KernelParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_tq, tm_tk, tm_tv;
+  int B, H, M, N;  // jagged: B = sequences, M = N = max_seq_len
+  int jagged, causal;
+  int n_mt;        // query tiles per (b, h) or per (sequence, h)
+  int num_units;
+  float scale_log2;  // sm_scale * log2(e)
+  float sm_scale;
+  const int* offsets;
+  const float* bias;
+  long long bias_stride[4];
+  const unsigned char* mask;
+  long long mask_stride[4];
+  __nv_bfloat16* o;
+  __nv_bfloat16* to;
+  float* lse;
+  long long T;
+  int max_seq_len;
+  int* err;
+  unsigned long long timeout_ns;
+  int skip_first_load;
+};
+
+// Shared-memory and tensor-memory plan for one instantiation.
+template <int DQK, int DV, bool JVP>
+struct Plan {
+  static constexpr int NQ = JVP ? 2 : 1;  // primal (+ tangent) operands
+  static constexpr int Q_TILE = kBM * DQK * 2;
+  static constexpr int K_TILE = kBN * DQK * 2;
+  static constexpr int V_TILE = kBN * DV * 2;
+  static constexpr int Q_SUB = kBM * 128;  // one 64-column swizzled sub-tile
+  static constexpr int K_SUB = kBN * 128;
+  static constexpr int V_SUB = kBN * 128;
+  static constexpr int K_STAGE = NQ * K_TILE;
+  static constexpr int V_STAGE = NQ * V_TILE;
+  static constexpr int FIXED = NQ * Q_TILE;
+  static constexpr int BUDGET = 227 * 1024 - 2048;
+  static constexpr int NK = (FIXED + 4 * K_STAGE + 4 * V_STAGE <= BUDGET) ? 4 : 3;
+  static constexpr int NV = (FIXED + NK * K_STAGE + 4 * V_STAGE <= BUDGET)   ? 4
+                            : (FIXED + NK * K_STAGE + 3 * V_STAGE <= BUDGET) ? 3
+                                                                             : 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_TQ = Q_TILE;
+  static constexpr int OFF_K = FIXED;
+  static constexpr int OFF_V = OFF_K + NK * K_STAGE;
+  static constexpr int OFF_BAR = OFF_V + NV * V_STAGE;
+  // barriers: q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
+  //           s_full[2], p_full[2], o_done, mma_drain
+  static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + NK, B_VF = B_KE + NK,
+                       B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2, B_OD = B_PF + 2,
+                       B_DRAIN = B_OD + 1, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  // TMEM columns: buffer b holds S at [b*SBUF, b*SBUF+BN) and tS after it;
+  // then O_acc and tO_acc.
+  static constexpr int SBUF = JVP ? 2 * kBN : kBN;
+  static constexpr int COL_O = 2 * SBUF;
+  static constexpr int COL_TO = COL_O + DV;
+  static constexpr int COLS_USED = COL_O + (JVP ? 2 : 1) * DV;
+  static constexpr int TMEM_COLS = COLS_USED <= 256 ? 256 : 512;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
+  static_assert(COLS_USED <= 512, "tensor memory plan exceeds 512 columns");
+  static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims are multiples of 64");
+};
+
+struct Unit {
+  int z;            // third tensor-map coordinate: b*H + h (dense) or h (jagged)
+  int row0;         // first row of this (b, h) / sequence in the tensor map
+  int mt;           // query tile index
+  int q_len;        // query rows of this (b, h) / sequence
+  int kv_len;       // keys of this (b, h) / sequence
+  int nt;           // key tiles visited
+  int b, h;
+  long long out0;   // row index of query 0 in the [.., rows] output view
+  bool active;
+};
+
+// Work unit u.  Causal dense units and jagged units are ordered by
+// descending query tile, so the costliest units start first.
+__device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
+  Unit w;
+  const int BH = p.B * p.H;
+  if (!p.jagged) {
+    int bh, mt;
+    if (p.causal) {
+      mt = p.n_mt - 1 - u / BH;
+      bh = u % BH;
+    } else {
+      bh = u / p.n_mt;
+      mt = u % p.n_mt;
+    }
+    w.b = bh / p.H;
+    w.h = bh % p.H;
+    w.z = bh;
+    w.row0 = 0;
+    w.mt = mt;
+    w.q_len = p.M;
+    w.kv_len = p.N;
+    w.out0 = static_cast<long long>(bh) * p.M;
+  } else {
+    const int mt = p.n_mt - 1 - u / BH;
+    const int r = u % BH;
+    const int b = r / p.H, h = r % p.H;
+    const int begin = __ldg(p.offsets + b), end = __ldg(p.offsets + b + 1);
+    const int len = min(end - begin, p.max_seq_len);
+    w.b = b;
+    w.h = h;
+    w.z = h;
+    w.row0 = begin;
+    w.mt = mt;
+    w.q_len = len;
+    w.kv_len = len;
+    w.out0 = static_cast<long long>(h) * p.T + begin;
+  }
+  w.active = w.mt * kBM < w.q_len;
+  int hi = w.kv_len;
+  if (p.causal) hi = min(hi, (w.mt + 1) * kBM);
+  w.nt = w.active ? (hi + kBN - 1) / kBN : 0;
+  return w;
+}
+
+struct Waiter {
+  volatile int* abort_flag;
+  int* err;
+  unsigned long long timeout_ns;
+};
+
+// Bounded wait for the phase of `bar` with parity `parity`.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Waiter& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        *w.abort_flag = 1;
+        atomicCAS(w.err, 0, ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (teardown drains).
+__device__ __forceinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigned long long ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* packed, int n32) {
+  // n32 packed bf16x2 words, 16-byte stores
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < n32 / 4; ++i)
+    d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+}
+
+template <int DQK, int DV, bool JVP>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KernelParams p) {
+  using P = Plan<DQK, DV, JVP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + P::OFF_BAR;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(P::B_QF), 1);
+    mbar_init(bar(P::B_QE), 1);
+    for (int i = 0; i < P::NK; ++i) {
+      mbar_init(bar(P::B_KF + i), 1);
+      mbar_init(bar(P::B_KE + i), 1);
+    }
+    for (int i = 0; i < P::NV; ++i) {
+      mbar_init(bar(P::B_VF + i), 1);
+      mbar_init(bar(P::B_VE + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(P::B_SF + i), 1);
+      mbar_init(bar(P::B_PF + i), 4);  // one arrival per softmax warp
+    }
+    mbar_init(bar(P::B_OD), 1);
+    mbar_init(bar(P::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+    if (JVP) {
+      prefetch_tmap(&p.tm_tq);
+      prefetch_tmap(&p.tm_tk);
+      prefetch_tmap(&p.tm_tv);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), P::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter W{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t qfill = 0, kfill = 0, vfill = 0;
+      bool last_q_loaded = false;
+      bool skip = p.skip_first_load != 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        if (w.nt == 0) continue;
+        ok = wait_bar(bar(P::B_QE), (qfill & 1u) ^ 1u, W);
+        if (!ok) break;
+        if (!skip) {
+          mbar_arrive_expect_tx(bar(P::B_QF), P::NQ * P::Q_TILE);
+          const int r = w.row0 + w.mt * kBM;
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c) {
+            tma_load_3d(sbase + P::OFF_Q + c * P::Q_SUB, &p.tm_q, bar(P::B_QF), c * 64, r, w.z);
+            if (JVP)
+              tma_load_3d(sbase + P::OFF_TQ + c * P::Q_SUB, &p.tm_tq, bar(P::B_QF), c * 64, r, w.z);
+          }
+          last_q_loaded = true;
+        } else {
+          last_q_loaded = false;
+        }
+        skip = false;
+        ++qfill;
+        for (int j = 0; j < w.nt; ++j) {
+          const int r = w.row0 + j * kBN;
+          const uint32_t ks = kfill % P::NK;
+          ok = wait_bar(bar(P::B_KE + ks), ((kfill / P::NK) & 1u) ^ 1u, W);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(P::B_KF + ks), P::K_STAGE);
+          const uint32_t kdst = sbase + P::OFF_K + ks * P::K_STAGE;
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c) {
+            tma_load_3d(kdst + c * P::K_SUB, &p.tm_k, bar(P::B_KF + ks), c * 64, r, w.z);
+            if (JVP)
+              tma_load_3d(kdst + P::K_TILE + c * P::K_SUB, &p.tm_tk, bar(P::B_KF + ks), c * 64, r,
+                          w.z);
+          }
+          ++kfill;
+          const uint32_t vs = vfill % P::NV;
+          ok = wait_bar(bar(P::B_VE + vs), ((vfill / P::NV) & 1u) ^ 1u, W);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(P::B_VF + vs), P::V_STAGE);
+          const uint32_t vdst = sbase + P::OFF_V + vs * P::V_STAGE;
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c) {
+            tma_load_3d(vdst + c * P::V_SUB, &p.tm_v, bar(P::B_VF + vs), c * 64, r, w.z);
+            if (JVP)
+              tma_load_3d(vdst + P::V_TILE + c * P::V_SUB, &p.tm_tv, bar(P::B_VF + vs), c * 64, r,
+                          w.z);
+          }
+          ++vfill;
+        }
+      }
+      // Teardown: every issued copy must have landed before the CTA exits.
+      for (uint32_t s = 0; s < P::NK && s < kfill; ++s) {
+        const uint32_t nf = (kfill - s + P::NK - 1) / P::NK;
+        drain_bar(bar(P::B_KF + s), (nf - 1) & 1u, p.timeout_ns);
+      }
+      for (uint32_t s = 0; s < P::NV && s < vfill; ++s) {
+        const uint32_t nf = (vfill - s + P::NV - 1) / P::NV;
+        drain_bar(bar(P::B_VF + s), (nf - 1) & 1u, p.timeout_ns);
+      }
+      if (qfill > 0 && last_q_loaded) drain_bar(bar(P::B_QF), (qfill - 1) & 1u, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false);
+      constexpr uint32_t idesc_o = idesc_bf16(kBM, DV, true);
+      uint32_t quse = 0, kuse = 0, vuse = 0, g = 0;
+      bool ok = true;
+      const uint32_t sQ = sbase + P::OFF_Q, sTQ = sbase + P::OFF_TQ;
+
+      // O += P V ; tO += P tV + H V   for global tile index gi
+      auto issue_pv = [&](uint32_t gi, bool first) -> bool {
+        const uint32_t sb = gi & 1u;
+        if (!wait_bar(bar(P::B_PF + sb), (gi >> 1) & 1u, W)) return false;
+        const uint32_t vs = vuse % P::NV;
+        if (!wait_bar(bar(P::B_VF + vs), (vuse / P::NV) & 1u, W)) return false;
+        tc_fence_after();
+        const uint32_t sV = sbase + P::OFF_V + vs * P::V_STAGE;
+        const uint32_t aP = tmem + sb * P::SBUF;  // P packed bf16 over BN/2 columns
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
+          mma_ts(tmem + P::COL_O, aP + kk * 8, dv, idesc_o, (first && kk == 0) ? 0u : 1u);
+        }
+        if (JVP) {
+          const uint32_t aH = aP + kBN;  // H = P o tS, packed in the tS columns
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t dtv = sdesc_sw128(sV + P::V_TILE + kk * 2048, P::V_SUB, 1024);
+            mma_ts(tmem + P::COL_TO, aP + kk * 8, dtv, idesc_o, (first && kk == 0) ? 0u : 1u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
+            mma_ts(tmem + P::COL_TO, aH + kk * 8, dv, idesc_o, 1u);
+          }
+        }
+        tc_commit(bar(P::B_VE + vs));
+        tc_commit(bar(P::B_OD));
+        ++vuse;
+        return true;
+      };
+
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        if (w.nt == 0) continue;
+        ok = wait_bar(bar(P::B_QF), quse & 1u, W);
+        if (!ok) break;
+        tc_fence_after();
+        for (int j = 0; j < w.nt; ++j) {
+          const uint32_t ks = kuse % P::NK;
+          ok = wait_bar(bar(P::B_KF + ks), (kuse / P::NK) & 1u, W);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sb = g & 1u;
+          const uint32_t dS = tmem + sb * P::SBUF;
+          const uint32_t sK = sbase + P::OFF_K + ks * P::K_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < DQK / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            const uint64_t dq = sdesc_sw128(sQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
+            const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_SUB + off, 16, 1024);
+            mma_ss(dS, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          if (JVP) {
+            const uint32_t dT = dS + kBN;
+#pragma unroll
+            for (int kk = 0; kk < DQK / 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;
+              const uint64_t dtq = sdesc_sw128(sTQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
+              const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_SUB + off, 16, 1024);
+              mma_ss(dT, dtq, dk, idesc_s, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < DQK / 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;
+              const uint64_t dq = sdesc_sw128(sQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
+              const uint64_t dtk =
+                  sdesc_sw128(sK + P::K_TILE + (kk >> 2) * P::K_SUB + off, 16, 1024);
+              mma_ss(dT, dq, dtk, idesc_s, 1u);
+            }
+          }
+          tc_commit(bar(P::B_SF + sb));
+          tc_commit(bar(P::B_KE + ks));
+          ++kuse;
+          if (j == w.nt - 1) tc_commit(bar(P::B_QE));
+          if (j > 0) {
+            ok = issue_pv(g - 1, j == 1);
+            if (!ok) break;
+          }
+          ++g;
+        }
+        if (!ok) break;
+        ok = issue_pv(g - 1, w.nt == 1);
+        ++quse;
+      }
+      // Teardown: all MMAs issued by this thread complete before TMEM is freed.
+      tc_commit(bar(P::B_DRAIN));
+      drain_bar(bar(P::B_DRAIN), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------- softmax / rescale / epilogue
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const bool has_bias = p.bias != nullptr;
+    const bool has_mask = p.mask != nullptr;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      if (!w.active) continue;
+      const int qi = w.mt * kBM + row;
+      const bool row_ok = qi < w.q_len;
+      __nv_bfloat16* orow = p.o + (w.out0 + qi) * DV;
+      __nv_bfloat16* torow = JVP ? p.to + (w.out0 + qi) * DV : nullptr;
+      if (w.nt == 0) {  // no keys at all: empty rows
+        if (row_ok) {
+          uint32_t z[DV / 2];
+#pragma unroll
+          for (int i = 0; i < DV / 2; ++i) z[i] = 0u;
+          store_row_bf16(orow, z, DV / 2);
+          if (JVP) store_row_bf16(torow, z, DV / 2);
+          p.lse[w.out0 + qi] = -INFINITY;
+        }
+        continue;
+      }
+      const float* brow = nullptr;
+      const unsigned char* mrow = nullptr;
+      if (has_bias)
+        brow = p.bias + w.b * p.bias_stride[0] + w.h * p.bias_stride[1] +
+               static_cast<long long>(qi) * p.bias_stride[2];
+      if (has_mask)
+        mrow = p.mask + w.b * p.mask_stride[0] + w.h * p.mask_stride[1] +
+               static_cast<long long>(qi) * p.mask_stride[2];
+
+      float m_run = -INFINITY, l_run = 0.f, r_run = 0.f;
+      for (int j = 0; j < w.nt; ++j, ++g) {
+        const uint32_t sb = g & 1u;
+        const int key0 = j * kBN;
+        // Prefetch this tile's bias / mask entries before waiting on S.
+        float bv[kBN];
+        uint32_t mv[kBN / 4];
+        if (has_bias) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) bv[c] = 0.f;
+          if (row_ok) {
+            const float* bp = brow + static_cast<long long>(key0) * p.bias_stride[3];
+            if (p.bias_stride[3] == 1 && (reinterpret_cast<uintptr_t>(bp) & 15u) == 0 &&
+                key0 + kBN <= w.kv_len) {
+#pragma unroll
+              for (int c = 0; c < kBN / 4; ++c) {
+                const float4 t4 = __ldg(reinterpret_cast<const float4*>(bp) + c);
+                bv[4 * c] = t4.x;
+                bv[4 * c + 1] = t4.y;
+                bv[4 * c + 2] = t4.z;
+                bv[4 * c + 3] = t4.w;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < kBN; ++c)
+                if (key0 + c < w.kv_len) bv[c] = __ldg(bp + c * p.bias_stride[3]);
+            }
+          }
+        }
+        if (has_mask) {
+#pragma unroll
+          for (int c = 0; c < kBN / 4; ++c) mv[c] = 0u;
+          if (row_ok) {
+            const unsigned char* mp = mrow + static_cast<long long>(key0) * p.mask_stride[3];
+            if (p.mask_stride[3] == 1 && (reinterpret_cast<uintptr_t>(mp) & 15u) == 0 &&
+                key0 + kBN <= w.kv_len) {
+#pragma unroll
+              for (int c = 0; c < kBN / 16; ++c) {
+                const uint4 t4 = __ldg(reinterpret_cast<const uint4*>(mp) + c);
+                mv[4 * c] = t4.x;
+                mv[4 * c + 1] = t4.y;
+                mv[4 * c + 2] = t4.z;
+                mv[4 * c + 3] = t4.w;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < kBN; ++c)
+                if (key0 + c < w.kv_len && __ldg(mp + c * p.mask_stride[3]) != 0)
+                  mv[c >> 2] |= 1u << ((c & 3) * 8);
+            }
+          }
+        }
+
+        ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[kBN];
+        uint32_t tr[kBN];
+        tmem_ld_32x32b_x64(tl + sb * P::SBUF, sr);
+        if constexpr (JVP) tmem_ld_32x32b_x64(tl + sb * P::SBUF + kBN, tr);
+        tmem_wait_ld();
+        float x[kBN], t[JVP ? kBN : 1];
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
+        if constexpr (JVP) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) t[c] = __uint_as_float(tr[c]);
+        }
+
+        const bool diag = p.causal && (key0 + kBN - 1 > w.mt * kBM);
+        const bool fast = !has_bias && !has_mask && !diag && (key0 + kBN <= w.kv_len);
+        float sc;  // factor taking x to log2 units inside the exponent
+        float mx = -INFINITY;
+        if (fast) {
+          sc = p.scale_log2;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, x[c]);
+          mx *= p.scale_log2;
+        } else {
+          sc = 1.f;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            const int kj = key0 + c;
+            bool keep = kj < w.kv_len;
+            if (p.causal) keep = keep && (kj <= qi);
+            if (has_mask) keep = keep && (((mv[c >> 2] >> ((c & 3) * 8)) & 0xffu) != 0u);
+            float v = x[c] * p.scale_log2;
+            if (has_bias) v = fmaf(bv[c], kLog2e, v);
+            x[c] = keep ? v : -INFINITY;
+            if constexpr (JVP) t[c] = keep ? t[c] : 0.f;
+            mx = fmaxf(mx, x[c]);
+          }
+        }
+        // lazy online-softmax update
+        const float m_new = fmaxf(m_run, mx);
+        float alpha = 1.f;
+        bool resc = false;
+        if (m_new > m_run + kRescaleThreshold) {
+          if (m_run != -INFINITY) {
+            alpha = ex2(m_run - m_new);
+            resc = true;
+          }
+          m_run = m_new;
+        }
+        const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+        float ls0 = 0.f, ls1 = 0.f, rs0 = 0.f, rs1 = 0.f;
+        uint32_t pk[kBN / 2];
+        uint32_t hk[kBN / 2];
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          const float p0 = ex2(fmaf(x[c], sc, neg_m));
+          const float p1 = ex2(fmaf(x[c + 1], sc, neg_m));
+          ls0 += p0;
+          ls1 += p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+          if constexpr (JVP) {
+            const float h0 = p0 * (t[c] * p.sm_scale);
+            const float h1 = p1 * (t[c + 1] * p.sm_scale);
+            rs0 += h0;
+            rs1 += h1;
+            hk[c / 2] = pack_bf16x2(h0, h1);
+          }
+        }
+        l_run = fmaf(l_run, alpha, ls0 + ls1);
+        if constexpr (JVP) r_run = fmaf(r_run, alpha, rs0 + rs1);
+        tmem_st_32x32b_x32(tl + sb * P::SBUF, pk);
+        if constexpr (JVP) tmem_st_32x32b_x32(tl + sb * P::SBUF + kBN, hk);
+
+        if (j > 0) {
+          // The previous tile's O/tO MMAs must be complete before O is
+          // touched here, and before this tile's P is released.
+          ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_OD), (g - 1) & 1u, W));
+          if (!ok) break;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, resc)) {
+            const float a = resc ? alpha : 1.f;
+#pragma unroll
+            for (int c0 = 0; c0 < DV; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tl + P::COL_O + c0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+              tmem_st_32x32b_x32(tl + P::COL_O + c0, v);
+              if constexpr (JVP) {
+                tmem_ld_32x32b_x32(tl + P::COL_TO + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+                tmem_st_32x32b_x32(tl + P::COL_TO + c0, v);
+              }
+            }
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(P::B_PF + sb));
+      }
+      if (!ok) break;
+
+      // ------------------------------------------------------------ epilogue
+      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_OD), (g - 1) & 1u, W));
+      if (!ok) break;
+      tc_fence_after();
+      const bool empty = !(l_run > 0.f);
+      const float inv_l = empty ? 0.f : 1.f / l_run;
+#pragma unroll
+      for (int c0 = 0; c0 < DV; c0 += 32) {
+        uint32_t ov[32];
+        uint32_t tv[32];
+        tmem_ld_32x32b_x32(tl + P::COL_O + c0, ov);
+        if constexpr (JVP) tmem_ld_32x32b_x32(tl + P::COL_TO + c0, tv);
+        tmem_wait_ld();
+        uint32_t po[16], pt[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float o0 = __uint_as_float(ov[i]) * inv_l;
+          const float o1 = __uint_as_float(ov[i + 1]) * inv_l;
+          po[i / 2] = pack_bf16x2(o0, o1);
+          if constexpr (JVP) {
+            const float t0 = (__uint_as_float(tv[i]) - r_run * o0) * inv_l;
+            const float t1 = (__uint_as_float(tv[i + 1]) - r_run * o1) * inv_l;
+            pt[i / 2] = pack_bf16x2(t0, t1);
+          }
+        }
+        if (row_ok) {
+          store_row_bf16(orow + c0, po, 16);
+          if constexpr (JVP) store_row_bf16(torow + c0, pt, 16);
+        }
+      }
+      if (row_ok) p.lse[w.out0 + qi] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
+    }
+
+    // Jagged rows past max_seq_len inside their sequence: empty rows.
+    if (ok && p.jagged) {
+      const int t128 = threadIdx.x - 64;
+      for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        const int begin = __ldg(p.offsets + b), end = __ldg(p.offsets + b + 1);
+        const int kept = min(end - begin, p.max_seq_len);
+        for (int h = 0; h < p.H; ++h) {
+          for (int rr = begin + kept + t128; rr < end; rr += 128) {
+            const long long o_row = static_cast<long long>(h) * p.T + rr;
+            uint32_t z[DV / 2];
+#pragma unroll
+            for (int i = 0; i < DV / 2; ++i) z[i] = 0u;
+            store_row_bf16(p.o + o_row * DV, z, DV / 2);
+            if (JVP) store_row_bf16(p.to + o_row * DV, z, DV / 2);
+            p.lse[o_row] = -INFINITY;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, P::TMEM_COLS);
+}
+
+template <int DQK, int DV, bool JVP>
+cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
+  using P = Plan<DQK, DV, JVP>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_done[dev]) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  attn_fwd_kernel<DQK, DV, JVP><<<grid, kThreads, P::SMEM_BYTES, stream>>>(kp);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

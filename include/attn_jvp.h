@@ -1,0 +1,148 @@
+/*
+ * attn_jvp.h -- C ABI of the fused attention forward + JVP library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * One pass over the keys computes, for every query row i:
+ *
+ *   S   = sm_scale * Q K^T + bias          (keys outside the valid set: -inf)
+ *   P   = softmax(S)                       (row-wise)
+ *   O   = P V
+ *   LSE = log sum_j exp(S_ij)              (natural log, fp32)
+ *   tS  = sm_scale * (tQ K^T + Q tK^T)     (0 outside the valid set)
+ *   tO  = P tV + (P o tS) V - rowsum(P o tS) o O
+ *
+ * which is the forward pass of softmax attention together with its
+ * Jacobian-vector product along the tangents (tQ, tK, tV).  Sources:
+ *   - "Flash Attention v2 with JVP" (flm/utils/jvp.py): _attn_fwd_inner
+ *     (score tangent, running max m, denominator l and tangent sum r) and
+ *     the _attn_fwd epilogue (O = acc / l, tO = (acc_A + acc_B - r O) / l,
+ *     LSE as a natural log, empty-row guard);
+ *   - "_06_fused_attention_blockptr_jvp.py" (Triton fused attention with
+ *     JVP): the same epilogue written as g_acc/l - (mu/l) O + p_tv_acc/l;
+ *   - "flash_attention.py" (triton_flashattn): _attn_fwd_inner additive
+ *     bias after the sm_scale product, boolean mask (nonzero = attend),
+ *     unequal head dims Dqk != Dv;
+ *   - "triton_multi_head_jagged_flash_attention.py" (FBGEMM): jagged
+ *     [H, T, D] layout with offsets[B + 1], lengths capped at max_seq_len.
+ *
+ * Valid set of row i: key j < key length; j <= i when causal (in-sequence
+ * indices for jagged); mask[b,h,i,j] != 0 when a mask is given.  A row
+ * whose valid set is empty gets O = tO = 0 and LSE = -inf.
+ *
+ * Conventions for every entry point:
+ *   - Pointers q..lse are DEVICE pointers owned by the caller; the library
+ *     keeps none of them after the call returns.  Every one of them must be
+ *     16-byte aligned (bulk tensor copies), else ATTN_ERR_MISALIGNED.
+ *   - q, k, v, tq, tk, tv, o, to are bf16 (raw 16-bit storage), lse fp32.
+ *   - Dense layouts (offsets == NULL), all contiguous, row-major:
+ *       q, tq [B, H, M, Dqk]   k, tk [B, H, N, Dqk]   v, tv [B, H, N, Dv]
+ *       o, to [B, H, M, Dv]    lse   [B, H, M]
+ *   - Jagged layouts (offsets != NULL), packed total-token layout:
+ *       q, k, tq, tk [H, T, Dqk]   v, tv, o, to [H, T, Dv]   lse [H, T]
+ *     offsets is a device int32 array [B + 1], offsets[0] = 0,
+ *     non-decreasing, offsets[B] <= T.  Sequence b owns tokens
+ *     [offsets[b], offsets[b+1]) and attends within its first
+ *     L_b = min(offsets[b+1] - offsets[b], max_seq_len) tokens; its rows
+ *     past L_b are written as empty rows; rows >= offsets[B] are not
+ *     written.  The device offsets are not checked by the host; keys of
+ *     neighbouring sequences may be read by a tile and are masked, so the
+ *     whole of v and tv must hold finite values.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream).  Argument errors are returned synchronously and
+ *     launch nothing.  A device-side failure (a pipeline wait that ran out
+ *     of time) is recorded in a per-device error word and reported by the
+ *     next attn_sync_check on that device.
+ *   - Supported head dims: Dqk, Dv in {64, 128}; otherwise
+ *     ATTN_ERR_UNSUPPORTED.
+ *   - The library allocates one small per-device scratch buffer (error
+ *     word) on first use and keeps it until the process exits.
+ */
+#ifndef ATTN_JVP_H
+#define ATTN_JVP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, causal with M != N (dense) */
+  ATTN_ERR_UNSUPPORTED = 2,   /* head dim outside {64, 128} */
+  ATTN_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+  ATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (no GPU, launch error) */
+  ATTN_ERR_TIMEOUT = 5        /* a device pipeline wait ran out of time; outputs undefined */
+} attn_status;
+
+/* Problem shape.  Dense: B, H, M (query length), N (key length), Dqk, Dv;
+ * T and max_seq_len ignored.  Jagged: B = number of sequences, H, Dqk, Dv,
+ * T = total tokens, max_seq_len = cap on a sequence's length; M and N are
+ * ignored. */
+typedef struct {
+  int32_t B, H, M, N, Dqk, Dv;
+  int64_t T;
+  int32_t max_seq_len;
+} attn_shape;
+
+/* Optional additive bias and boolean mask over [B, H, M, N] (dense only).
+ * Strides are in elements; a stride of 0 broadcasts that dimension (a key
+ * padding mask is {N, 0, 0, 1}).  A NULL pointer means "absent".  The
+ * bias is fp32 and added after the sm_scale product (it is not scaled and
+ * has no tangent); the mask is uint8, nonzero = attend.  Both may be given
+ * together ("flash_attention.py", _attn_fwd_inner). */
+typedef struct {
+  const float* bias;
+  int64_t bias_stride[4];
+  const uint8_t* mask;
+  int64_t mask_stride[4];
+} attn_bias;
+
+/* Forward + JVP in one pass ("Flash Attention v2 with JVP", _attn_fwd).
+ * sm_scale: NaN selects the default Dqk^-1/2 (_attention.forward).
+ * causal: nonzero = row i attends to keys j <= i; dense causal requires
+ * M == N (ATTN_ERR_INVALID_ARG otherwise).  bias may be NULL.
+ * Writes o, to (bf16) and lse (fp32). */
+attn_status attn_fwd_jvp(const attn_shape* shape,
+                         const void* q, const void* k, const void* v,
+                         const void* tq, const void* tk, const void* tv,
+                         const int32_t* offsets, const attn_bias* bias,
+                         int causal, float sm_scale,
+                         void* o, void* to, float* lse, void* stream);
+
+/* Forward only: the same operation without tangents (the FA2 forward of
+ * "flash_attention.py", _attn_fwd, and of the FBGEMM jagged forward with
+ * sm_scale and without its 1/max_seq_len factor).  Writes o and lse. */
+attn_status attn_fwd(const attn_shape* shape,
+                     const void* q, const void* k, const void* v,
+                     const int32_t* offsets, const attn_bias* bias,
+                     int causal, float sm_scale,
+                     void* o, float* lse, void* stream);
+
+/* Synchronises `stream`, then reads and clears the error word of the
+ * current device.  Returns ATTN_ERR_TIMEOUT if a launch since the last
+ * check reported a timed-out wait, ATTN_ERR_CUDA on a CUDA error, else
+ * ATTN_OK. */
+attn_status attn_sync_check(void* stream);
+
+/* Static description of a status code; never NULL. */
+const char* attn_status_string(attn_status s);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t attn_launch_count(void);
+
+/* Upper bound, in nanoseconds, on any single pipeline wait inside the
+ * kernels (default 2e9).  Values below 1e6 are raised to 1e6. */
+void attn_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook for failure detection: when nonzero, the next launches skip
+ * the first query-tile load, so the consumer's bounded wait runs out and
+ * the call reports ATTN_ERR_TIMEOUT through attn_sync_check.  0 restores
+ * normal operation. */
+void attn_debug_skip_first_load(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_JVP_H */

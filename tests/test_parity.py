@@ -1,0 +1,268 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerances (the target's, written here): O max abs error <= 1e-2,
+tO max abs error <= 2e-2 * max(1, ||tO_oracle||_inf), LSE max abs error
+<= 1e-3; -inf LSE (empty rows) must match exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_forward_jvp_gb300 import binding, build
+from attention_forward_jvp_gb300.workloads import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+T_TOL = 2e-2
+L_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    binding.lib()
+
+
+def dev(x):
+    return None if x is None else x.cuda()
+
+
+def run_gpu(inp, jvp=True):
+    q, k, v, tq, tk, tv = (dev(inp[n]) for n in ("q", "k", "v", "tq", "tk", "tv"))
+    kw = dict(causal=inp["causal"], sm_scale=inp["sm_scale"], offsets=dev(inp["offsets"]),
+              max_seq_len=inp["max_seq_len"], bias=dev(inp["bias"]), mask=dev(inp["mask"]))
+    if jvp:
+        out = binding.attn_fwd_jvp(q, k, v, tq, tk, tv, **kw)
+    else:
+        out = binding.attn_fwd(q, k, v, **kw)
+    assert binding.sync_check() == 0
+    return tuple(o.float().cpu().numpy() for o in out)
+
+
+def assert_close(O, tO, L, Or, tOr, Lr, what=""):
+    assert np.isfinite(O).all() and np.isfinite(tO).all(), f"{what}: non-finite output"
+    eo = np.abs(O - Or).max() if O.size else 0.0
+    tscale = max(1.0, np.abs(tOr).max() if tOr.size else 0.0)
+    et = np.abs(tO - tOr).max() if tO.size else 0.0
+    inf_r = np.isneginf(Lr)
+    assert np.array_equal(np.isneginf(L), inf_r), f"{what}: empty-row LSE pattern differs"
+    el = np.abs(L[~inf_r] - Lr[~inf_r]).max() if (~inf_r).any() else 0.0
+    assert eo <= O_TOL, f"{what}: O err {eo:.3e}"
+    assert et <= T_TOL * tscale, f"{what}: tO err {et:.3e} (scale {tscale:.2f})"
+    assert el <= L_TOL, f"{what}: LSE err {el:.3e}"
+    return eo, et, el
+
+
+def oracle_dense(inp):
+    return oracle.attention_fwd_jvp(inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"],
+                                    causal=inp["causal"], sm_scale=inp["sm_scale"],
+                                    bias=inp["bias"], mask=inp["mask"])
+
+
+# ------------------------------------------------------------ full configs
+def test_tiny_full():
+    inp = make_inputs(WORKLOADS["tiny"])
+    assert_close(*run_gpu(inp), *oracle_dense(inp), what="tiny")
+
+
+def test_noncausal_full():
+    inp = make_inputs(WORKLOADS["noncausal"])
+    assert_close(*run_gpu(inp), *oracle_dense(inp), what="noncausal")
+
+
+def _sampled_rows_check(inp, bh_list, rows, what):
+    O, tO, L = run_gpu(inp)
+    for b, h in bh_list:
+        o, to, l = oracle.attention_fwd_jvp_rows(
+            inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"], b, h, rows,
+            causal=inp["causal"], sm_scale=inp["sm_scale"], bias=inp["bias"], mask=inp["mask"])
+        assert_close(O[b, h, rows], tO[b, h, rows], L[b, h, rows], o, to, l, what=f"{what} b{b} h{h}")
+    return O, tO, L
+
+
+def test_causal_full_size_sampled_rows():
+    w = WORKLOADS["causal"]
+    inp = make_inputs(w)
+    rows = [0, 1, 63, 64, 65, 127, 128, 129, 1000, 2047, 2048, 3071, 4032, 4094, 4095]
+    _sampled_rows_check(inp, [(0, 0), (1, 15), (0, 9), (1, 3)], rows, "causal")
+
+
+def test_bias_mask_full_size_sampled_rows():
+    inp = make_inputs(WORKLOADS["bias_mask"])
+    rows = [0, 1, 127, 128, 1000, 1535, 1536, 2046, 2047]
+    _sampled_rows_check(inp, [(0, 0), (1, 7), (0, 5)], rows, "bias_mask")
+
+
+def test_jagged_full_size_subset_of_sequences():
+    w = WORKLOADS["jagged"]
+    inp = make_inputs(w)
+    O, tO, L = run_gpu(inp)
+    seqs = list(range(0, w.B, 7))
+    Or, tOr, Lr = oracle.attention_fwd_jvp_jagged(
+        inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"], inp["offsets"],
+        w.max_seq_len, sm_scale=inp["sm_scale"], only_seqs=set(seqs))
+    off = inp["offsets"].numpy()
+    for i in seqs:
+        sl = slice(off[i], off[i + 1])
+        assert_close(O[:, sl], tO[:, sl], L[:, sl], Or[:, sl], tOr[:, sl], Lr[:, sl], what=f"seq {i}")
+
+
+# ------------------------------------------------------------- edge shapes
+EDGE = [
+    # B, H, M, N, Dqk, Dv, causal
+    (1, 2, 999, 999, 64, 64, True),
+    (1, 2, 999, 999, 64, 64, False),
+    (1, 2, 1024, 1024, 64, 64, True),
+    (1, 2, 256, 1024, 64, 128, False),
+    (1, 2, 1000, 15, 128, 64, False),
+    (1, 2, 515, 999, 64, 64, False),
+    (1, 2, 515, 999, 128, 128, False),
+    (2, 3, 130, 70, 128, 64, False),
+    (1, 1, 1, 1, 64, 64, True),
+    (1, 2, 200, 1, 128, 128, False),
+    (1, 1, 300, 300, 128, 128, True),
+    (3, 2, 64, 200, 64, 128, False),
+]
+
+
+@pytest.mark.parametrize("B,H,M,N,Dqk,Dv,causal", EDGE)
+def test_edge_shapes(B, H, M, N, Dqk, Dv, causal):
+    w = Workload("edge", B=B, H=H, M=M, N=N, Dqk=Dqk, Dv=Dv, causal=causal,
+                 input_std=0.5, tangent_std=0.5, sm_scale=0.5)
+    inp = make_inputs(w, seed=20)
+    assert_close(*run_gpu(inp), *oracle_dense(inp), what=str((B, H, M, N, Dqk, Dv, causal)))
+
+
+def test_no_keys_gives_empty_rows():
+    w = Workload("nokeys", B=1, H=2, M=130, N=0, Dqk=64, Dv=64)
+    inp = make_inputs(w)
+    O, tO, L = run_gpu(inp)
+    assert np.all(O == 0) and np.all(tO == 0) and np.all(np.isneginf(L))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_jagged_edge_lengths(causal):
+    lens = [1, 63, 64, 65, 127, 128, 129, 300, 0, 2, 255, 256, 257]
+    w = Workload("jag", B=len(lens), H=3, Dqk=128, Dv=64, jagged=True, max_seq_len=200,
+                 max_len_draw=1, causal=causal, sm_scale=0.125)
+    inp = make_inputs(w, seed=3, lengths=lens)
+    O, tO, L = run_gpu(inp)
+    Or, tOr, Lr = oracle.attention_fwd_jvp_jagged(
+        inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"], inp["offsets"], 200,
+        causal=causal, sm_scale=0.125)
+    assert_close(O, tO, L, Or, tOr, Lr, what=f"jagged causal={causal}")
+
+
+def test_bias_and_mask_with_fully_masked_row():
+    w = Workload("bm", B=2, H=3, M=150, N=333, Dqk=128, Dv=128, bias=True)
+    inp = make_inputs(w, seed=4)
+    g = torch.Generator().manual_seed(5)
+    mask = (torch.rand((2, 3, 150, 333), generator=g) < 0.6).to(torch.uint8)
+    mask[0, 1, 7, :] = 0      # a fully masked row
+    mask[1, 2, 149, :] = 0
+    inp["mask"] = mask
+    O, tO, L = run_gpu(inp)
+    Or, tOr, Lr = oracle_dense(inp)
+    assert_close(O, tO, L, Or, tOr, Lr, what="bias+mask")
+    assert np.isneginf(L[0, 1, 7]) and np.all(O[0, 1, 7] == 0) and np.all(tO[0, 1, 7] == 0)
+
+
+def test_broadcast_bias_strides():
+    w = Workload("bb", B=2, H=2, M=140, N=190, Dqk=64, Dv=64)
+    inp = make_inputs(w, seed=6)
+    g = torch.Generator().manual_seed(7)
+    inp["bias"] = torch.randn((1, 2, 1, 190), generator=g)   # per-head key bias, broadcast
+    inp["mask"] = (torch.arange(190) < 170).to(torch.uint8).view(1, 1, 1, 190)
+    assert_close(*run_gpu(inp), *oracle_dense(inp), what="broadcast bias")
+
+
+# -------------------------------------------------------- kernel invariants
+@pytest.mark.parametrize("name", ["tiny", "edge_causal", "edge_bias"])
+def test_forward_only_matches_jvp_primal_bitwise(name):
+    if name == "tiny":
+        inp = make_inputs(WORKLOADS["tiny"])
+    elif name == "edge_causal":
+        inp = make_inputs(Workload("e", B=1, H=2, M=777, N=777, Dqk=128, Dv=128, causal=True), seed=8)
+    else:
+        inp = make_inputs(Workload("e", B=1, H=2, M=300, N=500, Dqk=128, Dv=64, bias=True,
+                                   mask_keep=420), seed=9)
+    O, _, L = run_gpu(inp, jvp=True)
+    O2, L2 = run_gpu(inp, jvp=False)
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)
+
+
+def test_causal_rows_ignore_future_keys_bitwise():
+    inp = make_inputs(Workload("c", B=1, H=2, M=640, N=640, Dqk=64, Dv=64, causal=True), seed=10)
+    O, tO, L = run_gpu(inp)
+    for nm in ("k", "v", "tk", "tv"):
+        inp[nm] = inp[nm].clone()
+        inp[nm][:, :, 400:] = 7.0
+    O2, tO2, L2 = run_gpu(inp)
+    assert np.array_equal(O[:, :, :400], O2[:, :, :400])
+    assert np.array_equal(tO[:, :, :400], tO2[:, :, :400])
+    assert np.array_equal(L[:, :, :400], L2[:, :, :400])
+
+
+def test_guard_bands_and_nan_prefill():
+    inp = make_inputs(Workload("g", B=1, H=2, M=333, N=200, Dqk=64, Dv=128), seed=11)
+    guard = 4096
+    n_o = 1 * 2 * 333 * 128
+    n_l = 1 * 2 * 333
+    ob = torch.full((n_o + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tb = torch.full((n_o + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lb = torch.full((n_l + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
+    o = ob[guard:guard + n_o].view(1, 2, 333, 128)
+    to = tb[guard:guard + n_o].view(1, 2, 333, 128)
+    lse = lb[guard:guard + n_l].view(1, 2, 333)
+    q, k, v, tq, tk, tv = (dev(inp[n]) for n in ("q", "k", "v", "tq", "tk", "tv"))
+    binding.attn_fwd_jvp(q, k, v, tq, tk, tv, sm_scale=inp["sm_scale"], out=(o, to, lse))
+    assert binding.sync_check() == 0
+    for buf, n in ((ob, n_o), (tb, n_o), (lb, n_l)):
+        assert torch.isnan(buf[:guard].float()).all() and torch.isnan(buf[guard + n:].float()).all()
+        assert torch.isfinite(buf[guard:guard + n].float()).all()
+    Or, tOr, Lr = oracle_dense(inp)
+    assert_close(o.float().cpu().numpy(), to.float().cpu().numpy(), lse.cpu().numpy(), Or, tOr, Lr)
+
+
+def test_host_buffers_end_to_end_match_device_path():
+    inp = make_inputs(WORKLOADS["tiny"])
+    O, tO, L = run_gpu(inp)
+    ho, hto, hl = binding.attn_fwd_jvp(inp["q"].pin_memory(), inp["k"].pin_memory(),
+                                       inp["v"].pin_memory(), inp["tq"].pin_memory(),
+                                       inp["tk"].pin_memory(), inp["tv"].pin_memory(),
+                                       sm_scale=inp["sm_scale"])
+    assert ho.device.type == "cpu"
+    assert np.array_equal(ho.float().numpy(), O) and np.array_equal(hto.float().numpy(), tO)
+    assert np.array_equal(hl.numpy(), L)
+
+
+def test_default_scale_is_inverse_sqrt_dqk():
+    inp = make_inputs(Workload("s", B=1, H=1, M=128, N=128, Dqk=128, Dv=64), seed=12)
+    inp["sm_scale"] = None
+    O, tO, L = run_gpu(inp)
+    inp2 = dict(inp, sm_scale=1.0 / math.sqrt(128))
+    assert_close(O, tO, L, *oracle_dense(inp2), what="default scale")
+
+
+# ----------------------------------------------------- failure detection
+def test_timed_out_wait_is_reported_and_context_survives():
+    inp = make_inputs(WORKLOADS["tiny"])
+    q, k, v, tq, tk, tv = (dev(inp[n]) for n in ("q", "k", "v", "tq", "tk", "tv"))
+    binding.set_wait_timeout_ns(100_000_000)
+    binding.debug_skip_first_load(True)
+    try:
+        binding.attn_fwd_jvp(q, k, v, tq, tk, tv, sm_scale=inp["sm_scale"])
+        st = binding.sync_check()
+    finally:
+        binding.debug_skip_first_load(False)
+        binding.set_wait_timeout_ns(2_000_000_000)
+    assert st == 5  # ATTN_ERR_TIMEOUT
+    assert binding.sync_check() == 0  # cleared
+    O, tO, L = run_gpu(inp)
+    assert_close(O, tO, L, *oracle_dense(inp), what="after timeout")
