@@ -475,7 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         mrow = p.mask + w.b * p.mask_stride[0] + w.h * p.mask_stride[1] +
                static_cast<long long>(qi) * p.mask_stride[2];
 
-      float m_run = -INFINITY, l_run = 0.f, r_run = 0.f;
+      // m_run: reference max (log2 units); l_run: exact sum of p (for LSE);
+      // lt_run / r_run: sums of the bf16 values of p and p*tS that the MMAs
+      // consume, so O and tO are normalised by the weights actually used.
+      float m_run = -INFINITY, l_run = 0.f, lt_run = 0.f, r_run = 0.f;
       for (int j = 0; j < w.nt; ++j, ++g) {
         const uint32_t sb = g & 1u;
         const int key0 = j * kBN;
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           m_run = m_new;
         }
         const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-        float ls0 = 0.f, ls1 = 0.f, rs0 = 0.f, rs1 = 0.f;
+        float ls0 = 0.f, ls1 = 0.f, lt0 = 0.f, lt1 = 0.f, rs0 = 0.f, rs1 = 0.f;
         uint32_t pk[kBN / 2];
         uint32_t hk[kBN / 2];
 #pragma unroll
@@ -589,16 +592,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const float p1 = ex2(fmaf(x[c + 1], sc, neg_m));
           ls0 += p0;
           ls1 += p1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
+          const uint32_t pw = pack_bf16x2(p0, p1);
+          pk[c / 2] = pw;
+          lt0 += bf16_lo(pw);
+          lt1 += bf16_hi(pw);
           if constexpr (JVP) {
             const float h0 = p0 * (t[c] * p.sm_scale);
             const float h1 = p1 * (t[c + 1] * p.sm_scale);
-            rs0 += h0;
-            rs1 += h1;
-            hk[c / 2] = pack_bf16x2(h0, h1);
+            const uint32_t hw = pack_bf16x2(h0, h1);
+            hk[c / 2] = hw;
+            rs0 += bf16_lo(hw);
+            rs1 += bf16_hi(hw);
           }
         }
         l_run = fmaf(l_run, alpha, ls0 + ls1);
+        lt_run = fmaf(lt_run, alpha, lt0 + lt1);
         if constexpr (JVP) r_run = fmaf(r_run, alpha, rs0 + rs1);
         tmem_st_32x32b_x32(tl + sb * P::SBUF, pk);
         if constexpr (JVP) tmem_st_32x32b_x32(tl + sb * P::SBUF + kBN, hk);
@@ -641,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!ok) break;
       tc_fence_after();
       const bool empty = !(l_run > 0.f);
-      const float inv_l = empty ? 0.f : 1.f / l_run;
+      const float inv_l = empty ? 0.f : 1.f / lt_run;
 #pragma unroll
       for (int c0 = 0; c0 < DV; c0 += 32) {
         uint32_t ov[32];

@@ -1,0 +1,375 @@
+#!/usr/bin/env python
+"""Benchmark: attention forward + JVP TFLOP/s on one GB300 (per rank).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload causal|noncausal|jagged|bias_mask|tiny]
+
+A step is one fused forward + JVP pass (one launch of the library's kernel)
+over the workload's synthetic inputs, already resident in HBM.  FLOPs are
+algorithmic: 6 * (Dqk + Dv) per score element (three QK-shaped and three
+PV-shaped matmuls), halved for causal attention.  Prints ONE JSON line on
+rank 0.  Under torchrun every rank runs an independent replica of the
+workload on its own GPU (no collective on the data path); the timed region
+is bracketed by barriers and the slowest rank's time is used.
+
+--impl reference times the float64 CPU oracle on the host cores (rank 0
+only) on a bounded sample of the same workload: each step is one head.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from attention_forward_jvp_gb300.workloads import WORKLOADS, flops_fwd_jvp, make_inputs, min_hbm_bytes  # noqa: E402
+
+METRIC = "attn fwd+JVP TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 tensor peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "attention_forward_jvp_gb300", "csrc", "*")))
+    files += sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def describe(w) -> str:
+    if w.jagged:
+        return (f"{w.name}: {w.B} sequences, lengths U{{1..{w.max_len_draw}}}, H{w.H} "
+                f"Dqk{w.Dqk} Dv{w.Dv}, packed [H,T,D], fwd+JVP")
+    return (f"{w.name}: B{w.B} H{w.H} M{w.M} N{w.N} Dqk{w.Dqk} Dv{w.Dv} "
+            f"{'causal' if w.causal else 'non-causal'}{' +bias+mask' if w.bias else ''} fwd+JVP")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        sel = []
+        try:
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id  # type: ignore[attr-defined]
+            sel = ["-i", bus]
+        except Exception:
+            sel = ["-i", str(device_index)]
+        self.cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                    "-lms", "100"] + sel
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        self.lines = [ln for ln in (out or "").splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        # samples under load: the upper half of the observed clocks
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "window": "warm-up + timed region"}
+
+
+def dist_setup(impl):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and impl == "ours":
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------ CPU baseline
+def oracle_sample(w, inp, n_units: int, start: int = 0):
+    """Run the oracle on a bounded sample of the workload: ``n_units``
+    heads (dense: whole (b, h) heads; jagged: (sequence, all heads)).
+    Returns (seconds, algorithmic flops of the sample, description)."""
+    import oracle
+    if w.jagged:
+        off = inp["offsets"].numpy()
+        seqs = [(start + i) % w.B for i in range(n_units)]
+        t0 = time.perf_counter()
+        oracle.attention_fwd_jvp_jagged(inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"],
+                                        inp["offsets"], w.max_seq_len, causal=w.causal,
+                                        sm_scale=inp["sm_scale"], only_seqs=set(seqs))
+        dt = time.perf_counter() - t0
+        lens = np.minimum(off[1:] - off[:-1], w.max_seq_len)[seqs].astype(np.float64)
+        fl = 6.0 * (w.Dqk + w.Dv) * float((lens ** 2).sum()) * w.H * (0.5 if w.causal else 1.0)
+        return dt, fl, f"{n_units} sequences x {w.H} heads of the {w.name} workload"
+    BH = w.B * w.H
+    units = [(start + i) % BH for i in range(n_units)]
+    q64 = {n: None for n in ("q", "k", "v", "tq", "tk", "tv")}
+    t0 = time.perf_counter()
+    for u in units:
+        b, h = divmod(u, w.H)
+        for n in q64:
+            q64[n] = oracle.to_f64(inp[n][b, h])
+        bias = None if inp["bias"] is None else oracle.to_f64(inp["bias"][b, h])
+        mask = None
+        if inp["mask"] is not None:
+            mk = inp["mask"]
+            mask = np.broadcast_to(oracle.to_f64(mk[b if mk.shape[0] > 1 else 0, h if mk.shape[1] > 1 else 0]) != 0,
+                                   (w.M, w.N))
+        oracle.head_fwd_jvp(q64["q"], q64["k"], q64["v"], q64["tq"], q64["tk"], q64["tv"],
+                            inp["sm_scale"], w.causal, bias, mask)
+    dt = time.perf_counter() - t0
+    fl = 6.0 * (w.Dqk + w.Dv) * w.M * w.N * n_units * (0.5 if w.causal else 1.0)
+    return dt, fl, (f"{n_units} of {BH} (batch, head) pairs of the {w.name} workload, all rows, "
+                    "float64 NumPy (the oracle computes the full score matrix even when causal)")
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    inp = make_inputs(w, seed=0)
+    for i in range(args.warmup):
+        oracle_sample(w, inp, 1, start=i)
+    times, flops = [], 0.0
+    desc = ""
+    for i in range(args.steps):
+        dt, fl, desc = oracle_sample(w, inp, 1, start=args.warmup + i)
+        times.append(dt)
+        flops = fl
+    tot = sum(times)
+    value = flops * args.steps / tot / 1e12
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": describe(w), "sample_per_step": "one head"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- ours
+def run_ours(args, w, world, rank, local):
+    from attention_forward_jvp_gb300 import binding
+    from attention_forward_jvp_gb300 import build as _b
+
+    if not os.path.exists(_b.LIB_PATH):
+        _b.build()
+    binding.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = make_inputs(w, seed=0)
+    d = {n: inp[n].to(dev) for n in ("q", "k", "v", "tq", "tk", "tv")}
+    kw = dict(causal=w.causal, sm_scale=inp["sm_scale"],
+              offsets=None if inp["offsets"] is None else inp["offsets"].to(dev),
+              max_seq_len=inp["max_seq_len"],
+              bias=None if inp["bias"] is None else inp["bias"].to(dev),
+              mask=None if inp["mask"] is None else inp["mask"].to(dev))
+    flops = flops_fwd_jvp(w, inp["offsets"])
+    out = binding.attn_fwd_jvp(d["q"], d["k"], d["v"], d["tq"], d["tk"], d["tv"], **kw)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.attn_fwd_jvp(d["q"], d["k"], d["v"], d["tq"], d["tk"], d["tv"], out=out, **kw)
+
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            step()
+        st = binding.sync_check(stream)
+        if st != 0:
+            raise RuntimeError(f"device error during warm-up: {binding.status_string(st)}")
+        barrier(world)
+        torch.cuda.synchronize()
+        n0 = binding.launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        launches = binding.launch_count() - n0
+    st = binding.sync_check(stream)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {binding.status_string(st)}")
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    # the step is exactly one launch of the fused kernel, so its average
+    # launch duration is the per-step device time measured on its stream
+    achieved = flops / (ms * 1e-3) / 1e12
+
+    # end to end through the public API with pinned host buffers
+    host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "tq", "tk", "tv")}
+    hkw = dict(kw)
+    for key in ("offsets", "bias", "mask"):
+        if inp[key] is not None:
+            hkw[key] = inp[key].pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d += sum(hkw[k].numel() * hkw[k].element_size() for k in ("offsets", "bias", "mask") if hkw[k] is not None)
+    e2e_steps = max(1, min(args.steps, 10))
+    hout = binding.attn_fwd_jvp(*[host[n] for n in ("q", "k", "v", "tq", "tk", "tv")], **hkw)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        hout = binding.attn_fwd_jvp(*[host[n] for n in ("q", "k", "v", "tq", "tk", "tv")], **hkw)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = max_over_ranks(e2e_s, world)
+    e2e_val = world * flops / e2e_s / 1e12
+
+    if rank != 0:
+        return 0
+    pk, pk_kind = peaks()
+    peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tf):
+        with open(tf) as fh:
+            rec = json.load(fh).get(w.name)
+        if rec and rec.get("kernel_hash") == kernel_source_hash():
+            traffic = rec.get("dram_bytes_per_launch")
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_kind": f"{pk_kind} bf16 burst (kernel timed alone)",
+            "algorithmic_bytes": min_hbm_bytes(w, inp),
+            "hbm_gbs": min_hbm_bytes(w, inp) / (ms * 1e-3) / 1e9}
+    cpu = None
+    if world == 1 and not args.skip_cpu_baseline:
+        n_units = args.cpu_sample
+        dt, fl, desc = oracle_sample(w, inp, n_units)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": desc, "seconds": dt}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": describe(w), "flops_per_step": flops,
+                   "l2": ("inputs larger than L2, no flush" if min_hbm_bytes(w, inp) > 129e6
+                          else "inputs smaller than L2 (re-read from L2 across steps)"),
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": value / world / peak,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "kernel_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="causal", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-sample", type=int, default=4, help="heads in the CPU-baseline sample")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = WORKLOADS[args.workload]
+    world, rank, local = dist_setup(args.impl)
+    if args.impl == "reference":
+        rc = run_reference(args, w, world, rank)
+    else:
+        rc = run_ours(args, w, world, rank, local)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())
