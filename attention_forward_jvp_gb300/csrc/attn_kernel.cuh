@@ -9,20 +9,27 @@
 // The epilogue writes O = O_acc / l, tO = (tO_acc - r O) / l and
 // LSE = (m + log2 l) ln 2.
 //
-// GB300 mapping (one CTA per SM, 6 warps):
+// GB300 mapping (one CTA per SM, 10 warps):
 //   warp 0      bulk-tensor (TMA) producer: Q, tQ once per work unit; K, tK
 //               into a ring of NK stages; V, tV into a ring of NV stages.
-//   warp 1      tcgen05 issuer: S = Q K^T and tS = tQ K^T + Q tK^T into a
-//               double-buffered TMEM region, then O += P V and
-//               tO += P tV + H V with P, H (bf16) read back from TMEM --
-//               the K = 2*BN contraction [P | H] [tV ; V] issued as two
-//               accumulating runs into one tO accumulator.
-//   warps 2..5  softmax / rescale / epilogue, one query row per thread
-//               (TMEM lane = row).  Rescaling is lazy: m moves (and O, tO,
-//               l, r are multiplied by exp2(m_old - m_new)) only when the
-//               row maximum grows by more than kRescaleThreshold; the
-//               result is exact because l, r and both accumulators share
-//               the same stale reference.
+//   warp 1      tcgen05 issuer, per key tile:
+//                 [S | Q tK^T] = Q [K ; tK]^T      one N = 128 MMA chain
+//                 tS += tQ K^T                     N = 64
+//                 [O | tO] += P [V | tV]           one N = 2 Dv MMA chain
+//                 tO += H V                        N = Dv
+//               so P tV + H V is the K = 2*BN contraction [P | H] [tV ; V]
+//               accumulated into one tO.  S / tS are double buffered in
+//               TMEM; P and H (bf16) are written back over the S / tS
+//               columns they came from and read by the MMA from TMEM.
+//   warps 2..9  softmax / rescale / epilogue: two warps per TMEM lane
+//               quadrant, each taking 32 of the 64 key columns of a row
+//               (row = TMEM lane).  The pair exchanges its partial row
+//               maximum through shared memory once per tile.  Rescaling
+//               is lazy: the reference max m moves (and O, tO, l, r are
+//               multiplied by exp2(m_old - m_new)) only when the row
+//               maximum grows by more than kRescaleThreshold; the result
+//               is exact because l, r and both accumulators share the
+//               same stale reference.
 //   Work units (query tile, head, batch or sequence) are walked by every
 //   CTA with a static stride over a longest-first order.
 //
@@ -42,11 +49,13 @@ namespace attn {
 
 constexpr int kBM = 128;       // query rows per work unit (= TMEM lanes)
 constexpr int kBN = 64;        // keys per pipeline step
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kHalf = kBN / 2; // key columns per softmax thread
+constexpr int kThreads = 320;  // 10 warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 constexpr int ERR_TIMEOUT = 1;
+constexpr int ERR_SMEM_ALIGN = 2;
 
 struct KernelParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_tq, tm_tk, tm_tv;
@@ -74,17 +83,22 @@ struct KernelParams {
 // Shared-memory and tensor-memory plan for one instantiation.
 template <int DQK, int DV, bool JVP>
 struct Plan {
-  static constexpr int NQ = JVP ? 2 : 1;  // primal (+ tangent) operands
-  static constexpr int Q_TILE = kBM * DQK * 2;
-  static constexpr int K_TILE = kBN * DQK * 2;
-  static constexpr int V_TILE = kBN * DV * 2;
+  static constexpr int NQ = JVP ? 2 : 1;   // primal (+ tangent) operands
   static constexpr int Q_SUB = kBM * 128;  // one 64-column swizzled sub-tile
   static constexpr int K_SUB = kBN * 128;
   static constexpr int V_SUB = kBN * 128;
-  static constexpr int K_STAGE = NQ * K_TILE;
+  static constexpr int Q_TILE = (DQK / 64) * Q_SUB;
+  static constexpr int V_TILE = (DV / 64) * V_SUB;
+  // K stage: for each 64-column chunk c, [K rows | tK rows] side by side so
+  // that Q [K ; tK]^T is one N = 128 operand.
+  static constexpr int K_GROUP = NQ * K_SUB;
+  static constexpr int K_STAGE = (DQK / 64) * K_GROUP;
+  // V stage: [V chunks | tV chunks], uniform 64-column stride, so that
+  // [V | tV] is one N = 2 Dv operand.
   static constexpr int V_STAGE = NQ * V_TILE;
   static constexpr int FIXED = NQ * Q_TILE;
-  static constexpr int BUDGET = 227 * 1024 - 2048;
+  static constexpr int XCHG_FLOATS = 2 * 2 * kBM;  // [parity][half][row]
+  static constexpr int BUDGET = 227 * 1024 - 512 - XCHG_FLOATS * 4;
   static constexpr int NK = (FIXED + 4 * K_STAGE + 4 * V_STAGE <= BUDGET) ? 4 : 3;
   static constexpr int NV = (FIXED + NK * K_STAGE + 4 * V_STAGE <= BUDGET)   ? 4
                             : (FIXED + NK * K_STAGE + 3 * V_STAGE <= BUDGET) ? 3
@@ -95,14 +109,16 @@ struct Plan {
   static constexpr int OFF_V = OFF_K + NK * K_STAGE;
   static constexpr int OFF_BAR = OFF_V + NV * V_STAGE;
   // barriers: q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-  //           s_full[2], p_full[2], o_done, mma_drain
+  //           s_full[2], p_full[2], o_done, mma_drain, pair[4] (the two
+  //           softmax warps of a TMEM quadrant)
   static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + NK, B_VF = B_KE + NK,
                        B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2, B_OD = B_PF + 2,
-                       B_DRAIN = B_OD + 1, NBAR = B_DRAIN + 1;
+                       B_DRAIN = B_OD + 1, B_PAIR = B_DRAIN + 1, NBAR = B_PAIR + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
-  // TMEM columns: buffer b holds S at [b*SBUF, b*SBUF+BN) and tS after it;
-  // then O_acc and tO_acc.
+  static constexpr int OFF_XCHG = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = OFF_XCHG + XCHG_FLOATS * 4;
+  // TMEM columns: buffer b holds S at [b*SBUF, b*SBUF + BN) and tS after it;
+  // then O_acc and tO_acc side by side.
   static constexpr int SBUF = JVP ? 2 * kBN : kBN;
   static constexpr int COL_O = 2 * SBUF;
   static constexpr int COL_TO = COL_O + DV;
@@ -111,6 +127,7 @@ struct Plan {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
   static_assert(COLS_USED <= 512, "tensor memory plan exceeds 512 columns");
   static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims are multiples of 64");
+  static_assert(NQ * DV <= 256, "[O | tO] MMA needs N <= 256");
 };
 
 struct Unit {
@@ -207,28 +224,44 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// n32 packed bf16x2 words to global memory with 16-byte stores.
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* packed, int n32) {
-  // n32 packed bf16x2 words, 16-byte stores
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < n32 / 4; ++i)
     d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
 }
 
+// Row maximum of 32 values, 3-input max tree.
+__device__ __forceinline__ float rowmax32(const float* x) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) a[i] = max3f(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  a[10] = fmaxf(x[30], x[31]);
+  const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]);
+  const float b2 = max3f(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+  return fmaxf(max3f(b0, b1, b2), b3);
+}
+
 template <int DQK, int DV, bool JVP>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KernelParams p) {
   using P = Plan<DQK, DV, JVP>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // 128-byte swizzled operands need 1024-byte aligned tiles; the dynamic
+  // shared window starts aligned, and a launch where it does not reports
+  // an error instead of computing.
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, ERR_SMEM_ALIGN);
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + P::OFF_BAR;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::OFF_MISC + 4);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  float* xchg = reinterpret_cast<float*>(smem + P::OFF_XCHG);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(P::B_QF), 1);
@@ -243,10 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(P::B_SF + i), 1);
-      mbar_init(bar(P::B_PF + i), 4);  // one arrival per softmax warp
+      mbar_init(bar(P::B_PF + i), 8);  // one arrival per softmax warp
     }
     mbar_init(bar(P::B_OD), 1);
     mbar_init(bar(P::B_DRAIN), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(P::B_PAIR + i), 64);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -306,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const uint32_t kdst = sbase + P::OFF_K + ks * P::K_STAGE;
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c) {
-            tma_load_3d(kdst + c * P::K_SUB, &p.tm_k, bar(P::B_KF + ks), c * 64, r, w.z);
+            tma_load_3d(kdst + c * P::K_GROUP, &p.tm_k, bar(P::B_KF + ks), c * 64, r, w.z);
             if (JVP)
-              tma_load_3d(kdst + P::K_TILE + c * P::K_SUB, &p.tm_tk, bar(P::B_KF + ks), c * 64, r,
+              tma_load_3d(kdst + c * P::K_GROUP + P::K_SUB, &p.tm_tk, bar(P::B_KF + ks), c * 64, r,
                           w.z);
           }
           ++kfill;
@@ -342,13 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false);
-      constexpr uint32_t idesc_o = idesc_bf16(kBM, DV, true);
+      constexpr uint32_t idesc_s = idesc_bf16(kBM, JVP ? 2 * kBN : kBN, false);  // [S | Q tK^T]
+      constexpr uint32_t idesc_t = idesc_bf16(kBM, kBN, false);                   // tQ K^T
+      constexpr uint32_t idesc_o = idesc_bf16(kBM, P::NQ * DV, true);             // [O | tO]
+      constexpr uint32_t idesc_h = idesc_bf16(kBM, DV, true);                     // H V
       uint32_t quse = 0, kuse = 0, vuse = 0, g = 0;
       bool ok = true;
       const uint32_t sQ = sbase + P::OFF_Q, sTQ = sbase + P::OFF_TQ;
 
-      // O += P V ; tO += P tV + H V   for global tile index gi
+      // [O | tO] += P [V | tV] ; tO += H V   for global tile index gi
       auto issue_pv = [&](uint32_t gi, bool first) -> bool {
         const uint32_t sb = gi & 1u;
         if (!wait_bar(bar(P::B_PF + sb), (gi >> 1) & 1u, W)) return false;
@@ -366,13 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const uint32_t aH = aP + kBN;  // H = P o tS, packed in the tS columns
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t dtv = sdesc_sw128(sV + P::V_TILE + kk * 2048, P::V_SUB, 1024);
-            mma_ts(tmem + P::COL_TO, aP + kk * 8, dtv, idesc_o, (first && kk == 0) ? 0u : 1u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
             const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
-            mma_ts(tmem + P::COL_TO, aH + kk * 8, dv, idesc_o, 1u);
+            mma_ts(tmem + P::COL_TO, aH + kk * 8, dv, idesc_h, 1u);
           }
         }
         tc_commit(bar(P::B_VE + vs));
@@ -399,25 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = (kk & 3) * 32;
             const uint64_t dq = sdesc_sw128(sQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
-            const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_SUB + off, 16, 1024);
+            const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
             mma_ss(dS, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
           }
           if (JVP) {
-            const uint32_t dT = dS + kBN;
 #pragma unroll
             for (int kk = 0; kk < DQK / 16; ++kk) {
               const uint32_t off = (kk & 3) * 32;
               const uint64_t dtq = sdesc_sw128(sTQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
-              const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_SUB + off, 16, 1024);
-              mma_ss(dT, dtq, dk, idesc_s, kk > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint32_t off = (kk & 3) * 32;
-              const uint64_t dq = sdesc_sw128(sQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
-              const uint64_t dtk =
-                  sdesc_sw128(sK + P::K_TILE + (kk >> 2) * P::K_SUB + off, 16, 1024);
-              mma_ss(dT, dq, dtk, idesc_s, 1u);
+              const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
+              mma_ss(dS + kBN, dtq, dk, idesc_t, 1u);
             }
           }
           tc_commit(bar(P::B_SF + sb));
@@ -441,11 +463,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     __syncwarp();
   } else {
     // -------------------------------------------- softmax / rescale / epilogue
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int quad = warp & 3;         // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;  // which 32 of the 64 key columns
     const int row = quad * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    // Bounded rendezvous of the two warps of this quadrant (64 arrivals per
+    // phase); shared-memory writes before it are visible after it.
+    uint32_t pair_phase = 0;
+    auto pair_sync = [&]() -> bool {
+      tc_fence_before();
+      mbar_arrive(bar(P::B_PAIR + quad));
+      const bool r = __all_sync(0xffffffffu, wait_bar(bar(P::B_PAIR + quad), pair_phase & 1u, W));
+      ++pair_phase;
+      tc_fence_after();
+      return r;
+    };
     const bool has_bias = p.bias != nullptr;
     const bool has_mask = p.mask != nullptr;
+    float* my_x0 = xchg + (0 * 2 + half) * kBM + row;
+    float* my_x1 = xchg + (1 * 2 + half) * kBM + row;
+    const float* other_x0 = xchg + (0 * 2 + (half ^ 1)) * kBM + row;
+    const float* other_x1 = xchg + (1 * 2 + (half ^ 1)) * kBM + row;
+    constexpr int DVH = DV / 2;  // output columns per softmax thread
+    const uint64_t scale2 = f2_make(p.sm_scale, p.sm_scale);
     uint32_t g = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
@@ -453,16 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!w.active) continue;
       const int qi = w.mt * kBM + row;
       const bool row_ok = qi < w.q_len;
-      __nv_bfloat16* orow = p.o + (w.out0 + qi) * DV;
-      __nv_bfloat16* torow = JVP ? p.to + (w.out0 + qi) * DV : nullptr;
+      __nv_bfloat16* orow = p.o + (w.out0 + qi) * DV + half * DVH;
+      __nv_bfloat16* torow = JVP ? p.to + (w.out0 + qi) * DV + half * DVH : nullptr;
       if (w.nt == 0) {  // no keys at all: empty rows
         if (row_ok) {
-          uint32_t z[DV / 2];
+          uint32_t z[DVH / 2];
 #pragma unroll
-          for (int i = 0; i < DV / 2; ++i) z[i] = 0u;
-          store_row_bf16(orow, z, DV / 2);
-          if (JVP) store_row_bf16(torow, z, DV / 2);
-          p.lse[w.out0 + qi] = -INFINITY;
+          for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
+          store_row_bf16(orow, z, DVH / 2);
+          if (JVP) store_row_bf16(torow, z, DVH / 2);
+          if (half == 0) p.lse[w.out0 + qi] = -INFINITY;
         }
         continue;
       }
@@ -475,25 +515,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         mrow = p.mask + w.b * p.mask_stride[0] + w.h * p.mask_stride[1] +
                static_cast<long long>(qi) * p.mask_stride[2];
 
-      // m_run: reference max (log2 units); l_run: exact sum of p (for LSE);
-      // lt_run / r_run: sums of the bf16 values of p and p*tS that the MMAs
-      // consume, so O and tO are normalised by the weights actually used.
-      float m_run = -INFINITY, l_run = 0.f, lt_run = 0.f, r_run = 0.f;
+      // m_run: reference max (log2 units), shared by both halves of a row.
+      // l2: exact partial sum of p (for LSE); lt2 / r2: partial sums of the
+      // bf16 values of p and p*tS that the MMAs consume, so O and tO are
+      // normalised by the weights actually used.  Pairs of fp32 lanes.
+      float m_run = -INFINITY;
+      uint64_t l2 = 0, lt2 = 0, r2 = 0;
       for (int j = 0; j < w.nt; ++j, ++g) {
         const uint32_t sb = g & 1u;
-        const int key0 = j * kBN;
+        const int key0 = j * kBN + half * kHalf;  // first key of this thread's columns
         // Prefetch this tile's bias / mask entries before waiting on S.
-        float bv[kBN];
-        uint32_t mv[kBN / 4];
+        float bv[kHalf];
+        uint32_t mv[kHalf / 4];
         if (has_bias) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) bv[c] = 0.f;
+          for (int c = 0; c < kHalf; ++c) bv[c] = 0.f;
           if (row_ok) {
             const float* bp = brow + static_cast<long long>(key0) * p.bias_stride[3];
             if (p.bias_stride[3] == 1 && (reinterpret_cast<uintptr_t>(bp) & 15u) == 0 &&
-                key0 + kBN <= w.kv_len) {
+                key0 + kHalf <= w.kv_len) {
 #pragma unroll
-              for (int c = 0; c < kBN / 4; ++c) {
+              for (int c = 0; c < kHalf / 4; ++c) {
                 const float4 t4 = __ldg(reinterpret_cast<const float4*>(bp) + c);
                 bv[4 * c] = t4.x;
                 bv[4 * c + 1] = t4.y;
@@ -501,21 +543,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 bv[4 * c + 3] = t4.w;
               }
             } else {
-#pragma unroll
-              for (int c = 0; c < kBN; ++c)
+              for (int c = 0; c < kHalf; ++c)
                 if (key0 + c < w.kv_len) bv[c] = __ldg(bp + c * p.bias_stride[3]);
             }
           }
         }
         if (has_mask) {
 #pragma unroll
-          for (int c = 0; c < kBN / 4; ++c) mv[c] = 0u;
+          for (int c = 0; c < kHalf / 4; ++c) mv[c] = 0u;
           if (row_ok) {
             const unsigned char* mp = mrow + static_cast<long long>(key0) * p.mask_stride[3];
             if (p.mask_stride[3] == 1 && (reinterpret_cast<uintptr_t>(mp) & 15u) == 0 &&
-                key0 + kBN <= w.kv_len) {
+                key0 + kHalf <= w.kv_len) {
 #pragma unroll
-              for (int c = 0; c < kBN / 16; ++c) {
+              for (int c = 0; c < kHalf / 16; ++c) {
                 const uint4 t4 = __ldg(reinterpret_cast<const uint4*>(mp) + c);
                 mv[4 * c] = t4.x;
                 mv[4 * c + 1] = t4.y;
@@ -523,8 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 mv[4 * c + 3] = t4.w;
               }
             } else {
-#pragma unroll
-              for (int c = 0; c < kBN; ++c)
+              for (int c = 0; c < kHalf; ++c)
                 if (key0 + c < w.kv_len && __ldg(mp + c * p.mask_stride[3]) != 0)
                   mv[c >> 2] |= 1u << ((c & 3) * 8);
             }
@@ -534,32 +574,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[kBN];
-        uint32_t tr[kBN];
-        tmem_ld_32x32b_x64(tl + sb * P::SBUF, sr);
-        if constexpr (JVP) tmem_ld_32x32b_x64(tl + sb * P::SBUF + kBN, tr);
+        uint32_t sr[kHalf];
+        uint32_t tr[kHalf];
+        tmem_ld_32x32b_x32(tl + sb * P::SBUF + half * kHalf, sr);
+        if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
         tmem_wait_ld();
-        float x[kBN], t[JVP ? kBN : 1];
+        float x[kHalf];
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(sr[c]);
-        if constexpr (JVP) {
-#pragma unroll
-          for (int c = 0; c < kBN; ++c) t[c] = __uint_as_float(tr[c]);
-        }
+        for (int c = 0; c < kHalf; ++c) x[c] = __uint_as_float(sr[c]);
 
-        const bool diag = p.causal && (key0 + kBN - 1 > w.mt * kBM);
-        const bool fast = !has_bias && !has_mask && !diag && (key0 + kBN <= w.kv_len);
+        const bool diag = p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
+        const bool fast = !has_bias && !has_mask && !diag && (j * kBN + kBN <= w.kv_len);
         float sc;  // factor taking x to log2 units inside the exponent
-        float mx = -INFINITY;
+        float mx;
         if (fast) {
           sc = p.scale_log2;
-#pragma unroll
-          for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, x[c]);
-          mx *= p.scale_log2;
+          mx = rowmax32(x) * p.scale_log2;
         } else {
           sc = 1.f;
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) {
+          for (int c = 0; c < kHalf; ++c) {
             const int kj = key0 + c;
             bool keep = kj < w.kv_len;
             if (p.causal) keep = keep && (kj <= qi);
@@ -567,11 +601,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             float v = x[c] * p.scale_log2;
             if (has_bias) v = fmaf(bv[c], kLog2e, v);
             x[c] = keep ? v : -INFINITY;
-            if constexpr (JVP) t[c] = keep ? t[c] : 0.f;
-            mx = fmaxf(mx, x[c]);
+            if constexpr (JVP) tr[c] = keep ? tr[c] : 0u;
           }
+          mx = rowmax32(x);
         }
-        // lazy online-softmax update
+        // the pair's row maximum over all 64 columns of the tile
+        float* mine = (g & 1u) ? my_x1 : my_x0;
+        const float* theirs = (g & 1u) ? other_x1 : other_x0;
+        *mine = mx;
+        ok = pair_sync();
+        if (!ok) break;
+        mx = fmaxf(mx, *theirs);
+
+        // lazy online-softmax update (identical in both halves)
         const float m_new = fmaxf(m_run, mx);
         float alpha = 1.f;
         bool resc = false;
@@ -583,33 +625,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           m_run = m_new;
         }
         const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-        float ls0 = 0.f, ls1 = 0.f, lt0 = 0.f, lt1 = 0.f, rs0 = 0.f, rs1 = 0.f;
-        uint32_t pk[kBN / 2];
-        uint32_t hk[kBN / 2];
+        const uint64_t sc2 = f2_make(sc, sc), nm2 = f2_make(neg_m, neg_m);
+        uint64_t ls = 0, lts = 0, rs = 0;
+        uint32_t pk[kHalf / 2];
+        uint32_t hk[kHalf / 2];
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          const float p0 = ex2(fmaf(x[c], sc, neg_m));
-          const float p1 = ex2(fmaf(x[c + 1], sc, neg_m));
-          ls0 += p0;
-          ls1 += p1;
+        for (int c = 0; c < kHalf; c += 2) {
+          float a0, a1;
+          f2_split(f2_fma(f2_make(x[c], x[c + 1]), sc2, nm2), a0, a1);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          const uint64_t pp = f2_make(p0, p1);
+          ls = f2_add(ls, pp);
           const uint32_t pw = pack_bf16x2(p0, p1);
           pk[c / 2] = pw;
-          lt0 += bf16_lo(pw);
-          lt1 += bf16_hi(pw);
+          lts = f2_add(lts, f2_make(bf16_lo(pw), bf16_hi(pw)));
           if constexpr (JVP) {
-            const float h0 = p0 * (t[c] * p.sm_scale);
-            const float h1 = p1 * (t[c + 1] * p.sm_scale);
+            const uint64_t ts = f2_mul(f2_make(__uint_as_float(tr[c]), __uint_as_float(tr[c + 1])), scale2);
+            float h0, h1;
+            f2_split(f2_mul(pp, ts), h0, h1);
             const uint32_t hw = pack_bf16x2(h0, h1);
             hk[c / 2] = hw;
-            rs0 += bf16_lo(hw);
-            rs1 += bf16_hi(hw);
+            rs = f2_add(rs, f2_make(bf16_lo(hw), bf16_hi(hw)));
           }
         }
-        l_run = fmaf(l_run, alpha, ls0 + ls1);
-        lt_run = fmaf(lt_run, alpha, lt0 + lt1);
-        if constexpr (JVP) r_run = fmaf(r_run, alpha, rs0 + rs1);
-        tmem_st_32x32b_x32(tl + sb * P::SBUF, pk);
-        if constexpr (JVP) tmem_st_32x32b_x32(tl + sb * P::SBUF + kBN, hk);
+        const uint64_t a2 = f2_make(alpha, alpha);
+        l2 = f2_fma(l2, a2, ls);
+        lt2 = f2_fma(lt2, a2, lts);
+        if constexpr (JVP) r2 = f2_fma(r2, a2, rs);
+        tmem_st_32x32b_x16(tl + sb * P::SBUF + half * (kHalf / 2), pk);
+        if constexpr (JVP) tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * (kHalf / 2), hk);
 
         if (j > 0) {
           // The previous tile's O/tO MMAs must be complete before O is
@@ -620,19 +664,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           if (__any_sync(0xffffffffu, resc)) {
             const float a = resc ? alpha : 1.f;
 #pragma unroll
-            for (int c0 = 0; c0 < DV; c0 += 32) {
+            for (int c0 = 0; c0 < DVH; c0 += 32) {
               uint32_t v[32];
-              tmem_ld_32x32b_x32(tl + P::COL_O + c0, v);
+              tmem_ld_32x32b_x32(tl + P::COL_O + half * DVH + c0, v);
               tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-              tmem_st_32x32b_x32(tl + P::COL_O + c0, v);
+              tmem_st_32x32b_x32(tl + P::COL_O + half * DVH + c0, v);
               if constexpr (JVP) {
-                tmem_ld_32x32b_x32(tl + P::COL_TO + c0, v);
+                tmem_ld_32x32b_x32(tl + P::COL_TO + half * DVH + c0, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-                tmem_st_32x32b_x32(tl + P::COL_TO + c0, v);
+                tmem_st_32x32b_x32(tl + P::COL_TO + half * DVH + c0, v);
               }
             }
           }
@@ -648,14 +692,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_OD), (g - 1) & 1u, W));
       if (!ok) break;
       tc_fence_after();
-      const bool empty = !(l_run > 0.f);
-      const float inv_l = empty ? 0.f : 1.f / lt_run;
+      // combine the two halves' partial sums through shared memory
+      float l_a, l_b, lt_a, lt_b, r_a, r_b;
+      f2_split(l2, l_a, l_b);
+      f2_split(lt2, lt_a, lt_b);
+      f2_split(r2, r_a, r_b);
+      float l_sum = l_a + l_b, lt_sum = lt_a + lt_b, r_sum = r_a + r_b;
+      ok = pair_sync();  // both halves are done with the max slots
+      if (!ok) break;
+      *my_x0 = lt_sum;
+      *my_x1 = r_sum;
+      ok = pair_sync();
+      if (!ok) break;
+      lt_sum += *other_x0;
+      r_sum += *other_x1;
+      ok = pair_sync();
+      if (!ok) break;
+      *my_x0 = l_sum;
+      ok = pair_sync();
+      if (!ok) break;
+      l_sum += *other_x0;
+      ok = pair_sync();  // slots free for the next unit
+      if (!ok) break;
+
+      const bool empty = !(l_sum > 0.f);
+      const float inv_l = empty ? 0.f : 1.f / lt_sum;
 #pragma unroll
-      for (int c0 = 0; c0 < DV; c0 += 32) {
+      for (int c0 = 0; c0 < DVH; c0 += 32) {
         uint32_t ov[32];
         uint32_t tv[32];
-        tmem_ld_32x32b_x32(tl + P::COL_O + c0, ov);
-        if constexpr (JVP) tmem_ld_32x32b_x32(tl + P::COL_TO + c0, tv);
+        tmem_ld_32x32b_x32(tl + P::COL_O + half * DVH + c0, ov);
+        if constexpr (JVP) tmem_ld_32x32b_x32(tl + P::COL_TO + half * DVH + c0, tv);
         tmem_wait_ld();
         uint32_t po[16], pt[16];
 #pragma unroll
@@ -664,8 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const float o1 = __uint_as_float(ov[i + 1]) * inv_l;
           po[i / 2] = pack_bf16x2(o0, o1);
           if constexpr (JVP) {
-            const float t0 = (__uint_as_float(tv[i]) - r_run * o0) * inv_l;
-            const float t1 = (__uint_as_float(tv[i + 1]) - r_run * o1) * inv_l;
+            const float t0 = (__uint_as_float(tv[i]) - r_sum * o0) * inv_l;
+            const float t1 = (__uint_as_float(tv[i + 1]) - r_sum * o1) * inv_l;
             pt[i / 2] = pack_bf16x2(t0, t1);
           }
         }
@@ -674,17 +741,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           if constexpr (JVP) store_row_bf16(torow + c0, pt, 16);
         }
       }
-      if (row_ok) p.lse[w.out0 + qi] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
+      if (row_ok && half == 0)
+        p.lse[w.out0 + qi] = empty ? -INFINITY : (m_run + __log2f(l_sum)) * kLn2;
     }
 
     // Jagged rows past max_seq_len inside their sequence: empty rows.
     if (ok && p.jagged) {
-      const int t128 = threadIdx.x - 64;
+      const int t256 = threadIdx.x - 64;
       for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         const int begin = __ldg(p.offsets + b), end = __ldg(p.offsets + b + 1);
         const int kept = min(end - begin, p.max_seq_len);
         for (int h = 0; h < p.H; ++h) {
-          for (int rr = begin + kept + t128; rr < end; rr += 128) {
+          for (int rr = begin + kept + t256; rr < end; rr += 256) {
             const long long o_row = static_cast<long long>(h) * p.T + rr;
             uint32_t z[DV / 2];
 #pragma unroll

@@ -23,7 +23,6 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -68,63 +67,93 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling in the background."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the SM clock and the clock-event (throttle) reasons of one GPU
+    every few milliseconds through NVML (read-only queries), in a thread.
+    mark() tags the samples taken from then on as the timed region."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index: int):
-        self.proc = None
-        self.lines = []
-        sel = []
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        import ctypes
+        import threading
+        self.period = period_s
+        self.samples = []  # (tag, sm_mhz, max_mhz, reasons)
+        self.tag = "warmup"
+        self.stop_evt = threading.Event()
+        self.thread = None
+        self.nvml = None
+        self.h = ctypes.c_void_p()
         try:
-            bus = torch.cuda.get_device_properties(device_index).pci_bus_id  # type: ignore[attr-defined]
-            sel = ["-i", bus]
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            ok = False
+            props = torch.cuda.get_device_properties(device_index)
+            uid = getattr(props, "uuid", None)
+            if uid is not None:
+                key = str(uid)
+                key = key if key.startswith("GPU-") else "GPU-" + key
+                ok = nv.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(self.h)) == 0
+            if not ok and hasattr(props, "pci_bus_id"):
+                bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                             getattr(props, "pci_device_id", 0))
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0
+            if not ok:
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.h)) == 0
+            if ok:
+                self.nvml = nv
         except Exception:
-            sel = ["-i", str(device_index)]
-        self.cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                    "-lms", "100"] + sel
+            self.nvml = None
+
+    def _read(self):
+        import ctypes
+        c, m, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        nv = self.nvml
+        if nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) != 0:
+            return None
+        nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(m))
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        fn(self.h, ctypes.byref(r))
+        return c.value, m.value, r.value
+
+    def _run(self):
+        while not self.stop_evt.is_set():
+            s = self._read()
+            if s is not None:
+                self.samples.append((self.tag,) + s)
+            time.sleep(self.period)
+
+    def mark(self, tag):
+        self.tag = tag
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
-                                         text=True)
-        except Exception:
-            self.proc = None
+        import threading
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
         return self
 
     def __exit__(self, *a):
-        if self.proc is None:
-            return
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            out = ""
-        self.lines = [ln for ln in (out or "").splitlines() if ln.strip()]
+        if self.thread is not None:
+            self.stop_evt.set()
+            self.thread.join(timeout=2)
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for nm, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "unavailable" if self.nvml is None else "nvml"}
+        timed = [s for s in self.samples if s[0] == "timed"]
+        use = timed if timed else self.samples
+        reasons = set()
+        for _, _, _, r in use:
+            for bit, nm in self.REASONS.items():
+                if r & bit:
                     reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        # samples under load: the upper half of the observed clocks
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "window": "warm-up + timed region"}
+        return {"sm_mhz": statistics.median(s[1] for s in use), "sm_max_mhz": max(s[2] for s in use),
+                "reasons": sorted(reasons), "samples": len(use),
+                "window": "timed region" if timed else "warm-up + timed region",
+                "source": "nvml, every %d ms" % round(self.period * 1000)}
 
 
 def dist_setup(impl):
@@ -267,12 +296,14 @@ def run_ours(args, w, world, rank, local):
         barrier(world)
         torch.cuda.synchronize()
         n0 = binding.launch_count()
+        clk.mark("timed")
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        clk.mark("after")
         barrier(world)
         launches = binding.launch_count() - n0
     st = binding.sync_check(stream)
