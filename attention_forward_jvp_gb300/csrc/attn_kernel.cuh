@@ -9,7 +9,7 @@
 // The epilogue writes O = O_acc / l, tO = (tO_acc - r O) / l and
 // LSE = (m + log2 l) ln 2.
 //
-// GB300 mapping (one CTA per SM, 10 warps):
+// GB300 mapping (one CTA per SM, 12 warps):
 //   warp 0      bulk-tensor (TMA) producer: Q, tQ once per work unit; K, tK
 //               into a ring of NK stages; V, tV into a ring of NV stages.
 //   warp 1      tcgen05 issuer, per key tile:
@@ -21,7 +21,8 @@
 //               accumulated into one tO.  S / tS are double buffered in
 //               TMEM; P and H (bf16) are written back over the S / tS
 //               columns they came from and read by the MMA from TMEM.
-//   warps 2..9  softmax / rescale / epilogue: two warps per TMEM lane
+//   warps 2, 3  idle (they complete warpgroup 0 for the register split).
+//   warps 4..11 softmax / rescale / epilogue: two warps per TMEM lane
 //               quadrant, each taking 32 of the 64 key columns of a row
 //               (row = TMEM lane).  The pair exchanges its partial row
 //               maximum through shared memory once per tile.  Rescaling
@@ -50,7 +51,16 @@ namespace attn {
 constexpr int kBM = 128;       // query rows per work unit (= TMEM lanes)
 constexpr int kBN = 64;        // keys per pipeline step
 constexpr int kHalf = kBN / 2; // key columns per softmax thread
-constexpr int kThreads = 320;  // 10 warps
+constexpr int kThreads = 384;  // 12 warps = 3 warpgroups
+// Register split (setmaxnreg): the kernel is launched with kLaunchRegs per
+// thread; warpgroup 0 (producer, MMA issuer, two idle warps) gives registers
+// back and the two softmax warpgroups take them:
+//   4 warps x 32 x kLowRegs + 8 warps x 32 x kHighRegs = 384 x kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kLowRegs = 56;
+constexpr int kHighRegs = 224;
+static_assert(4 * 32 * kLowRegs + 8 * 32 * kHighRegs == kThreads * kLaunchRegs,
+              "register split must use exactly the launch allocation");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
@@ -109,11 +119,12 @@ struct Plan {
   static constexpr int OFF_V = OFF_K + NK * K_STAGE;
   static constexpr int OFF_BAR = OFF_V + NV * V_STAGE;
   // barriers: q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-  //           s_full[2], p_full[2], o_done, mma_drain, pair[4] (the two
-  //           softmax warps of a TMEM quadrant)
+  //           s_full[2], p_full[2], o_done (every tile), o_final (last tile of
+  //           a unit), mma_drain, pair[4] (the two softmax warps of a quadrant)
   static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + NK, B_VF = B_KE + NK,
                        B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2, B_OD = B_PF + 2,
-                       B_DRAIN = B_OD + 1, B_PAIR = B_DRAIN + 1, NBAR = B_PAIR + 4;
+                       B_OF = B_OD + 1, B_DRAIN = B_OF + 1, B_PAIR = B_DRAIN + 1,
+                       NBAR = B_PAIR + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int OFF_XCHG = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = OFF_XCHG + XCHG_FLOATS * 4;
@@ -279,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bar(P::B_PF + i), 8);  // one arrival per softmax warp
     }
     mbar_init(bar(P::B_OD), 1);
+    mbar_init(bar(P::B_OF), 1);
     mbar_init(bar(P::B_DRAIN), 1);
     for (int i = 0; i < 4; ++i) mbar_init(bar(P::B_PAIR + i), 64);
     *abort_flag = 0;
@@ -304,6 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.err, p.timeout_ns};
 
+  if (warp < 4) {
+  setmaxnreg_dec<kLowRegs>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -454,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         if (!ok) break;
         ok = issue_pv(g - 1, w.nt == 1);
+        if (ok) tc_commit(bar(P::B_OF));
         ++quse;
       }
       // Teardown: all MMAs issued by this thread complete before TMEM is freed.
@@ -461,10 +476,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       drain_bar(bar(P::B_DRAIN), 0, p.timeout_ns);
     }
     __syncwarp();
+  }
   } else {
+    setmaxnreg_inc<kHighRegs>();
     // -------------------------------------------- softmax / rescale / epilogue
     const int quad = warp & 3;         // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;  // which 32 of the 64 key columns
+    const int half = (warp - 4) >> 2;  // which 32 of the 64 key columns
     const int row = quad * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     // Bounded rendezvous of the two warps of this quadrant (64 arrivals per
@@ -486,7 +503,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const float* other_x1 = xchg + (1 * 2 + (half ^ 1)) * kBM + row;
     constexpr int DVH = DV / 2;  // output columns per softmax thread
     const uint64_t scale2 = f2_make(p.sm_scale, p.sm_scale);
-    uint32_t g = 0;
+    uint32_t g = 0;           // global key-tile counter (same in every role)
+    uint32_t gen = 0;         // masked tiles seen (slot parity of the max exchange)
+    uint32_t units_done = 0;  // units with keys finished (o_final parity)
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const Unit w = decode_unit(p, u);
@@ -574,22 +593,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
         if (!ok) break;
         tc_fence_after();
+        // Unmasked tiles: each warp also reads the partner half's 32 score
+        // columns and takes the row maximum over all 64 itself, so the two
+        // warps of a quadrant never wait for each other.  Masked tiles
+        // (causal diagonal, ragged tail, bias / mask) exchange partial
+        // maxima through shared memory instead.
+        const bool diag = p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
+        const bool fast = !has_bias && !has_mask && !diag && (j * kBN + kBN <= w.kv_len);
         uint32_t sr[kHalf];
+        uint32_t so[kHalf];
         uint32_t tr[kHalf];
         tmem_ld_32x32b_x32(tl + sb * P::SBUF + half * kHalf, sr);
+        if (fast) tmem_ld_32x32b_x32(tl + sb * P::SBUF + (half ^ 1) * kHalf, so);
         if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
         tmem_wait_ld();
         float x[kHalf];
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) x[c] = __uint_as_float(sr[c]);
 
-        const bool diag = p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
-        const bool fast = !has_bias && !has_mask && !diag && (j * kBN + kBN <= w.kv_len);
         float sc;  // factor taking x to log2 units inside the exponent
         float mx;
         if (fast) {
           sc = p.scale_log2;
-          mx = rowmax32(x) * p.scale_log2;
+          float xo[kHalf];
+#pragma unroll
+          for (int c = 0; c < kHalf; ++c) xo[c] = __uint_as_float(so[c]);
+          mx = fmaxf(rowmax32(x), rowmax32(xo)) * p.scale_log2;
         } else {
           sc = 1.f;
 #pragma unroll
@@ -604,14 +633,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if constexpr (JVP) tr[c] = keep ? tr[c] : 0u;
           }
           mx = rowmax32(x);
+          // the pair's row maximum over all 64 columns of the tile; the slot
+          // alternates per masked tile, and a writer can only come back to a
+          // slot after the rendezvous of the masked tile in between
+          float* mine = (gen & 1u) ? my_x1 : my_x0;
+          const float* theirs = (gen & 1u) ? other_x1 : other_x0;
+          ++gen;
+          *mine = mx;
+          ok = pair_sync();
+          if (!ok) break;
+          mx = fmaxf(mx, *theirs);
         }
-        // the pair's row maximum over all 64 columns of the tile
-        float* mine = (g & 1u) ? my_x1 : my_x0;
-        const float* theirs = (g & 1u) ? other_x1 : other_x0;
-        *mine = mx;
-        ok = pair_sync();
-        if (!ok) break;
-        mx = fmaxf(mx, *theirs);
 
         // lazy online-softmax update (identical in both halves)
         const float m_new = fmaxf(m_run, mx);
@@ -655,13 +687,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tmem_st_32x32b_x16(tl + sb * P::SBUF + half * (kHalf / 2), pk);
         if constexpr (JVP) tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * (kHalf / 2), hk);
 
-        if (j > 0) {
-          // The previous tile's O/tO MMAs must be complete before O is
-          // touched here, and before this tile's P is released.
+        if (__any_sync(0xffffffffu, resc)) {
+          // O and tO are rescaled in place, so the previous tile's output
+          // MMAs must have completed.  S of this tile is complete, and the
+          // MMA issue order puts tile g-2's output MMAs before this tile's
+          // score MMAs, so o_done has completed g-1 or g phases: waiting on
+          // parity (g-1) is unambiguous.  (resc is never set on a unit's
+          // first tile, where m_run starts at -inf.)
           ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_OD), (g - 1) & 1u, W));
           if (!ok) break;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, resc)) {
+          {
             const float a = resc ? alpha : 1.f;
 #pragma unroll
             for (int c0 = 0; c0 < DVH; c0 += 32) {
@@ -689,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_OD), (g - 1) & 1u, W));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_OF), units_done & 1u, W));
+      ++units_done;
       if (!ok) break;
       tc_fence_after();
       // combine the two halves' partial sums through shared memory
@@ -747,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
     // Jagged rows past max_seq_len inside their sequence: empty rows.
     if (ok && p.jagged) {
-      const int t256 = threadIdx.x - 64;
+      const int t256 = threadIdx.x - 128;
       for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         const int begin = __ldg(p.offsets + b), end = __ldg(p.offsets + b + 1);
         const int kept = min(end - begin, p.max_seq_len);
@@ -780,6 +817,14 @@ cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_done[dev]) {
+    // The register split is only valid for the launch allocation it was
+    // computed for; a build that compiled to another count is refused
+    // (setmaxnreg.inc would otherwise wait for registers that never free).
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
+      return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES);
     if (e != cudaSuccess) return e;
