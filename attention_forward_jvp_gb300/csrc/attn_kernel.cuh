@@ -128,13 +128,19 @@ struct Plan {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int OFF_XCHG = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = OFF_XCHG + XCHG_FLOATS * 4;
-  // TMEM columns: buffer b holds S at [b*SBUF, b*SBUF + BN) and tS after it;
-  // then O_acc and tO_acc side by side.
-  static constexpr int SBUF = JVP ? 2 * kBN : kBN;
+  // TMEM columns: buffer b holds S at [b*SBUF, b*SBUF + BN) and tS (or, in
+  // the forward-only kernel, scratch) in the next BN columns; then O_acc and
+  // tO_acc side by side.  Softmax half h writes its bf16 P (16 columns) and
+  // H (16 columns) over its own 32 tS columns, which no other thread reads,
+  // so the S columns stay intact for both halves' row maxima.
+  static constexpr int SBUF = 2 * kBN;
   static constexpr int COL_O = 2 * SBUF;
   static constexpr int COL_TO = COL_O + DV;
   static constexpr int COLS_USED = COL_O + (JVP ? 2 : 1) * DV;
   static constexpr int TMEM_COLS = COLS_USED <= 256 ? 256 : 512;
+  // Requested dynamic shared memory: never less than half an SM's, so one
+  // CTA (and its TMEM allocation) owns an SM.
+  static constexpr int SMEM_LAUNCH = SMEM_BYTES > 120 * 1024 ? SMEM_BYTES : 120 * 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
   static_assert(COLS_USED <= 512, "tensor memory plan exceeds 512 columns");
   static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims are multiples of 64");
@@ -406,18 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!wait_bar(bar(P::B_VF + vs), (vuse / P::NV) & 1u, W)) return false;
         tc_fence_after();
         const uint32_t sV = sbase + P::OFF_V + vs * P::V_STAGE;
-        const uint32_t aP = tmem + sb * P::SBUF;  // P packed bf16 over BN/2 columns
+        // keys [16 kk, 16 kk + 16): P at column base + 32 (kk / 2) + 8 (kk % 2),
+        // H 16 columns further (the layout the softmax halves write)
+        const uint32_t aP = tmem + sb * P::SBUF + kBN;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
-          mma_ts(tmem + P::COL_O, aP + kk * 8, dv, idesc_o, (first && kk == 0) ? 0u : 1u);
+          mma_ts(tmem + P::COL_O, aP + 32 * (kk >> 1) + 8 * (kk & 1), dv, idesc_o,
+                 (first && kk == 0) ? 0u : 1u);
         }
         if (JVP) {
-          const uint32_t aH = aP + kBN;  // H = P o tS, packed in the tS columns
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
             const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
-            mma_ts(tmem + P::COL_TO, aH + kk * 8, dv, idesc_h, 1u);
+            mma_ts(tmem + P::COL_TO, aP + 32 * (kk >> 1) + 16 + 8 * (kk & 1), dv, idesc_h, 1u);
           }
         }
         tc_commit(bar(P::B_VE + vs));
@@ -684,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         l2 = f2_fma(l2, a2, ls);
         lt2 = f2_fma(lt2, a2, lts);
         if constexpr (JVP) r2 = f2_fma(r2, a2, rs);
-        tmem_st_32x32b_x16(tl + sb * P::SBUF + half * (kHalf / 2), pk);
-        if constexpr (JVP) tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * (kHalf / 2), hk);
+        tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, pk);
+        if constexpr (JVP) tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf + kHalf / 2, hk);
 
         if (__any_sync(0xffffffffu, resc)) {
           // O and tO are rescaled in place, so the previous tile's output
@@ -826,11 +834,11 @@ cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
       return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  attn_fwd_kernel<DQK, DV, JVP><<<grid, kThreads, P::SMEM_BYTES, stream>>>(kp);
+  attn_fwd_kernel<DQK, DV, JVP><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
   return cudaGetLastError();
 }
 
