@@ -23,6 +23,7 @@ from . import build as _build
 EXPORTS = (
     "attn_fwd_jvp",
     "attn_fwd",
+    "attn_fwd_jvp_noalloc",
     "attn_sync_check",
     "attn_status_string",
     "attn_launch_count",
@@ -67,6 +68,8 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd_jvp.restype = i32
     L.attn_fwd_jvp.argtypes = [ctypes.POINTER(AttnShape), vp, vp, vp, vp, vp, vp, vp,
                                ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp, vp]
+    L.attn_fwd_jvp_noalloc.restype = i32
+    L.attn_fwd_jvp_noalloc.argtypes = L.attn_fwd_jvp.argtypes
     L.attn_fwd.restype = i32
     L.attn_fwd.argtypes = [ctypes.POINTER(AttnShape), vp, vp, vp, vp,
                            ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp]

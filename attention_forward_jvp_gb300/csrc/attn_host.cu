@@ -85,7 +85,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 attn_status run(const attn_shape* s, const void* q, const void* k, const void* v, const void* tq,
                 const void* tk, const void* tv, const int32_t* offsets, const attn_bias* bias,
                 int causal, float sm_scale, void* o, void* to, float* lse, void* stream,
-                bool jvp) {
+                bool jvp, const DeviceState* fixed = nullptr) {
   if (s == nullptr) return ATTN_ERR_INVALID_ARG;
   const bool jagged = offsets != nullptr;
   if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0) return ATTN_ERR_INVALID_ARG;
@@ -121,8 +121,14 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
     return ATTN_ERR_MISALIGNED;
 
   DeviceState* ds = nullptr;
-  attn_status st = device_state(&ds);
-  if (st != ATTN_OK) return st;
+  DeviceState fixed_state;
+  if (fixed != nullptr) {
+    fixed_state = *fixed;
+    ds = &fixed_state;
+  } else {
+    attn_status st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+  }
 
   attn::KernelParams kp;
   std::memset(&kp, 0, sizeof(kp));
@@ -194,6 +200,10 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   if (grid < 1) grid = 1;  // the jagged tail fill still runs
 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // A caller-fixed scratch is shared by every call: its error word must
+  // start each launch at zero.
+  if (fixed != nullptr && cudaMemsetAsync(ds->scratch, 0, sizeof(int), cs) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   cudaError_t e = cudaErrorInvalidValue;
   const int key = (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
   if (jvp) {
@@ -213,6 +223,58 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   }
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+// ------------------------------------------------ allocation-free variant
+// Callers that may not allocate device memory (an embedding framework
+// that owns every allocation, a graph-building runtime that forbids
+// cudaMalloc while recording, a real-time path with a frozen memory budget)
+// use attn_fwd_jvp_noalloc.  Its only scratch -- the kernel's error word --
+// lives in this fixed device array instead of a cudaMalloc'd buffer.  Every
+// device that loads the library holds the array until the process exits.
+constexpr int kNoAllocScratchWords = 64;  // 256 bytes; the kernel uses word 0
+static __device__ __align__(256) int g_noalloc_scratch[kNoAllocScratchWords];
+
+// Scratch words one forward + JVP launch needs: the error word, whatever
+// the problem size.
+constexpr int kScratchWordsPerLaunch = 1;
+
+std::mutex g_noalloc_mu;
+DeviceState g_noalloc_dev[kMaxDevices];  // scratch = device address of the array
+
+// Per-device set-up, run on the first call on a device with that device
+// current: the array's device address (host code only sees a stand-in
+// symbol), the SM count and the descriptor-encoding entry point.  Nothing
+// here allocates.
+attn_status noalloc_state(DeviceState* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  DeviceState& d = g_noalloc_dev[dev];
+  if (d.scratch == nullptr) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return ATTN_ERR_CUDA;
+    d.num_sms = sms;
+    d.scratch = static_cast<int*>(ptr);
+  }
+  {
+    std::lock_guard<std::mutex> lk2(g_mu);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return ATTN_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  *out = d;
   return ATTN_OK;
 }
 
@@ -260,6 +322,22 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_TIMEOUT: return "a device pipeline wait ran out of time; outputs are undefined";
   }
   return "unknown status";
+}
+
+attn_status attn_fwd_jvp_noalloc(const attn_shape* shape, const void* q, const void* k,
+                                 const void* v, const void* tq, const void* tk, const void* tv,
+                                 const int32_t* offsets, const attn_bias* bias, int causal,
+                                 float sm_scale, void* o, void* to, float* lse, void* stream) {
+  static_assert(kScratchWordsPerLaunch <= kNoAllocScratchWords,
+                "the fixed scratch array is smaller than one launch needs");
+  if (kScratchWordsPerLaunch > kNoAllocScratchWords) return ATTN_ERR_UNSUPPORTED;
+  DeviceState fixed;
+  if (shape != nullptr) {
+    attn_status st = noalloc_state(&fixed);
+    if (st != ATTN_OK) return st;
+  }
+  return run(shape, q, k, v, tq, tk, tv, offsets, bias, causal, sm_scale, o, to, lse, stream, true,
+             shape != nullptr ? &fixed : nullptr);
 }
 
 uint64_t attn_launch_count(void) { return g_launches.load(); }

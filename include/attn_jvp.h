@@ -119,6 +119,33 @@ attn_status attn_fwd(const attn_shape* shape,
                      int causal, float sm_scale,
                      void* o, float* lse, void* stream);
 
+/* attn_fwd_jvp for callers that may not allocate device memory: a framework
+ * that owns every device allocation, a runtime that forbids cudaMalloc
+ * while it records work, a real-time path with a frozen memory budget.
+ * The pages have no counterpart of this entry point.
+ *
+ * Same arguments, layouts and results as attn_fwd_jvp.  The library's only
+ * scratch (the kernel's error word, one 4-byte word whatever the problem
+ * size) lives in a fixed 256-byte device array inside the library instead
+ * of a buffer from cudaMalloc; every device that loads the library holds it
+ * until the process exits.  A problem that would need more scratch than
+ * the array holds is rejected with ATTN_ERR_UNSUPPORTED; no problem the
+ * current kernels accept does.  Nothing here calls cudaMalloc, cudaFree or
+ * any allocating library routine.
+ *
+ * The first call on a device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * Each call clears the error word on `stream` before its launch.  All calls
+ * share the array, so calls that overlap on the GPU (other streams) race on
+ * it; a wait that runs out of time in this variant is not reported to the
+ * host (use attn_fwd_jvp with attn_sync_check where that matters). */
+attn_status attn_fwd_jvp_noalloc(const attn_shape* shape,
+                                 const void* q, const void* k, const void* v,
+                                 const void* tq, const void* tk, const void* tv,
+                                 const int32_t* offsets, const attn_bias* bias,
+                                 int causal, float sm_scale,
+                                 void* o, void* to, float* lse, void* stream);
+
 /* Synchronises `stream`, then reads and clears the error word of the
  * current device.  Returns ATTN_ERR_TIMEOUT if a launch since the last
  * check reported a timed-out wait, ATTN_ERR_CUDA on a CUDA error, else
