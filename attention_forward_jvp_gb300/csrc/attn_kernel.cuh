@@ -11,7 +11,8 @@
 //
 // GB300 mapping (one CTA per SM, 12 warps):
 //   warp 0      bulk-tensor (TMA) producer: Q, tQ once per work unit; K, tK
-//               into a ring of NK stages; V, tV into a ring of NV stages.
+//               into a ring of NK stages.
+//   warp 2      bulk-tensor producer of V, tV into a ring of NV stages.
 //   warp 1      tcgen05 issuer, per key tile:
 //                 [S | Q tK^T] = Q [K ; tK]^T      one N = 128 MMA chain
 //                 tS += tQ K^T                     N = 64
@@ -21,7 +22,7 @@
 //               accumulated into one tO.  S / tS are double buffered in
 //               TMEM; P and H (bf16) are written back over the S / tS
 //               columns they came from and read by the MMA from TMEM.
-//   warps 2, 3  idle (they complete warpgroup 0 for the register split).
+//   warp 3      idle (it completes warpgroup 0 for the register split).
 //   warps 4..11 softmax / rescale / epilogue: two warps per TMEM lane
 //               quadrant, each taking 32 of the 64 key columns of a row
 //               (row = TMEM lane).  The pair exchanges its partial row
@@ -32,7 +33,7 @@
 //               is exact because l, r and both accumulators share the
 //               same stale reference.
 //   Work units (query tile, head, batch or sequence) are walked by every
-//   CTA with a static stride over a longest-first order.
+//   CTA in a snake over a longest-first order.
 //
 // Every mbarrier wait is bounded: on expiry the thread records
 // ERR_TIMEOUT in the device error word, raises a CTA-wide abort flag and
@@ -53,7 +54,7 @@ constexpr int kBN = 64;        // keys per pipeline step
 constexpr int kHalf = kBN / 2; // key columns per softmax thread
 constexpr int kThreads = 384;  // 12 warps = 3 warpgroups
 // Register split (setmaxnreg): the kernel is launched with kLaunchRegs per
-// thread; warpgroup 0 (producer, MMA issuer, two idle warps) gives registers
+// thread; warpgroup 0 (producers, MMA issuer, one idle warp) gives registers
 // back and the two softmax warpgroups take them:
 //   4 warps x 32 x kLowRegs + 8 warps x 32 x kHighRegs = 384 x kLaunchRegs.
 constexpr int kLaunchRegs = 168;
@@ -203,6 +204,15 @@ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
   return w;
 }
 
+// The unit a CTA processes in its round `rnd`: rounds walk the longest-first
+// unit order in a snake (even rounds CTA 0 -> G-1, odd rounds G-1 -> 0), so
+// the CTA that took the costliest unit of one round takes the cheapest of
+// the next.  Every role of a CTA walks the same sequence.
+__device__ __forceinline__ int unit_of_round(int rnd) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return rnd * G + ((rnd & 1) ? (G - 1 - c) : c);
+}
+
 struct Waiter {
   volatile int* abort_flag;
   int* err;
@@ -331,7 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       bool last_q_loaded = false;
       bool skip = p.skip_first_load != 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_of_round(rnd);
+        if (u >= p.num_units) break;
         const Unit w = decode_unit(p, u);
         if (w.nt == 0) continue;
         ok = wait_bar(bar(P::B_QE), (qfill & 1u) ^ 1u, W);
@@ -366,6 +378,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                           w.z);
           }
           ++kfill;
+        }
+      }
+      // Teardown: every issued copy must have landed before the CTA exits.
+      for (uint32_t s = 0; s < P::NK && s < kfill; ++s) {
+        const uint32_t nf = (kfill - s + P::NK - 1) / P::NK;
+        drain_bar(bar(P::B_KF + s), (nf - 1) & 1u, p.timeout_ns);
+      }
+      if (qfill > 0 && last_q_loaded) drain_bar(bar(P::B_QF), (qfill - 1) & 1u, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ---------------------------------------------------- V / tV producer
+    // Separate from the K ring so that a K load never waits for a V slot.
+    if (lane == 0) {
+      uint32_t vfill = 0;
+      bool ok = true;
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_of_round(rnd);
+        if (u >= p.num_units) break;
+        const Unit w = decode_unit(p, u);
+        for (int j = 0; j < w.nt; ++j) {
+          const int r = w.row0 + j * kBN;
           const uint32_t vs = vfill % P::NV;
           ok = wait_bar(bar(P::B_VE + vs), ((vfill / P::NV) & 1u) ^ 1u, W);
           if (!ok) break;
@@ -381,16 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ++vfill;
         }
       }
-      // Teardown: every issued copy must have landed before the CTA exits.
-      for (uint32_t s = 0; s < P::NK && s < kfill; ++s) {
-        const uint32_t nf = (kfill - s + P::NK - 1) / P::NK;
-        drain_bar(bar(P::B_KF + s), (nf - 1) & 1u, p.timeout_ns);
-      }
       for (uint32_t s = 0; s < P::NV && s < vfill; ++s) {
         const uint32_t nf = (vfill - s + P::NV - 1) / P::NV;
         drain_bar(bar(P::B_VF + s), (nf - 1) & 1u, p.timeout_ns);
       }
-      if (qfill > 0 && last_q_loaded) drain_bar(bar(P::B_QF), (qfill - 1) & 1u, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -434,7 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         return true;
       };
 
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_of_round(rnd);
+        if (u >= p.num_units) break;
         const Unit w = decode_unit(p, u);
         if (w.nt == 0) continue;
         ok = wait_bar(bar(P::B_QF), quse & 1u, W);
@@ -515,7 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint32_t gen = 0;         // masked tiles seen (slot parity of the max exchange)
     uint32_t units_done = 0;  // units with keys finished (o_final parity)
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int rnd = 0; ok; ++rnd) {
+      const int u = unit_of_round(rnd);
+      if (u >= p.num_units) break;
       const Unit w = decode_unit(p, u);
       if (!w.active) continue;
       const int qi = w.mt * kBM + row;
@@ -612,9 +644,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         uint32_t so[kHalf];
         uint32_t tr[kHalf];
         tmem_ld_32x32b_x32(tl + sb * P::SBUF + half * kHalf, sr);
-        if (fast) tmem_ld_32x32b_x32(tl + sb * P::SBUF + (half ^ 1) * kHalf, so);
-        if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
-        tmem_wait_ld();
+        if (fast) {
+          tmem_ld_32x32b_x32(tl + sb * P::SBUF + (half ^ 1) * kHalf, so);
+          tmem_wait_ld_regs(sr);
+          tmem_regs_ready(so);
+          // the tangent scores are needed only after the exponentials, so
+          // their load overlaps the row maximum and exp2 below
+          if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
+        } else {
+          if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
+          tmem_wait_ld_regs(sr);
+          if constexpr (JVP) tmem_regs_ready(tr);
+        }
         float x[kHalf];
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) x[c] = __uint_as_float(sr[c]);
@@ -666,34 +707,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
         const uint64_t sc2 = f2_make(sc, sc), nm2 = f2_make(neg_m, neg_m);
-        uint64_t ls = 0, lts = 0, rs = 0;
+        uint64_t ls = 0;
+        float lt0 = 0.f, lt1 = 0.f, rt0 = 0.f, rt1 = 0.f;
         uint32_t pk[kHalf / 2];
-        uint32_t hk[kHalf / 2];
+        uint64_t pv[kHalf / 2];
 #pragma unroll
         for (int c = 0; c < kHalf; c += 2) {
           float a0, a1;
           f2_split(f2_fma(f2_make(x[c], x[c + 1]), sc2, nm2), a0, a1);
           const float p0 = ex2(a0), p1 = ex2(a1);
           const uint64_t pp = f2_make(p0, p1);
+          pv[c / 2] = pp;
           ls = f2_add(ls, pp);
           const uint32_t pw = pack_bf16x2(p0, p1);
           pk[c / 2] = pw;
-          lts = f2_add(lts, f2_make(bf16_lo(pw), bf16_hi(pw)));
-          if constexpr (JVP) {
-            const uint64_t ts = f2_mul(f2_make(__uint_as_float(tr[c]), __uint_as_float(tr[c + 1])), scale2);
+          add_bf16x2_f32(pw, lt0, lt1);
+        }
+        tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, pk);
+        if constexpr (JVP) {
+          uint32_t hk[kHalf / 2];
+          tmem_wait_ld_regs(tr);
+#pragma unroll
+          for (int c = 0; c < kHalf; c += 2) {
+            const uint64_t ts =
+                f2_mul(f2_make(__uint_as_float(tr[c]), __uint_as_float(tr[c + 1])), scale2);
             float h0, h1;
-            f2_split(f2_mul(pp, ts), h0, h1);
+            f2_split(f2_mul(pv[c / 2], ts), h0, h1);
             const uint32_t hw = pack_bf16x2(h0, h1);
             hk[c / 2] = hw;
-            rs = f2_add(rs, f2_make(bf16_lo(hw), bf16_hi(hw)));
+            add_bf16x2_f32(hw, rt0, rt1);
           }
+          tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf + kHalf / 2, hk);
         }
         const uint64_t a2 = f2_make(alpha, alpha);
         l2 = f2_fma(l2, a2, ls);
-        lt2 = f2_fma(lt2, a2, lts);
-        if constexpr (JVP) r2 = f2_fma(r2, a2, rs);
-        tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, pk);
-        if constexpr (JVP) tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf + kHalf / 2, hk);
+        lt2 = f2_fma(lt2, a2, f2_make(lt0, lt1));
+        if constexpr (JVP) r2 = f2_fma(r2, a2, f2_make(rt0, rt1));
 
         if (__any_sync(0xffffffffu, resc)) {
           // O and tO are rescaled in place, so the previous tile's output
@@ -711,13 +760,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             for (int c0 = 0; c0 < DVH; c0 += 32) {
               uint32_t v[32];
               tmem_ld_32x32b_x32(tl + P::COL_O + half * DVH + c0, v);
-              tmem_wait_ld();
+              tmem_wait_ld_regs(v);
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
               tmem_st_32x32b_x32(tl + P::COL_O + half * DVH + c0, v);
               if constexpr (JVP) {
                 tmem_ld_32x32b_x32(tl + P::COL_TO + half * DVH + c0, v);
-                tmem_wait_ld();
+                tmem_wait_ld_regs(v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
                 tmem_st_32x32b_x32(tl + P::COL_TO + half * DVH + c0, v);
@@ -768,7 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         uint32_t tv[32];
         tmem_ld_32x32b_x32(tl + P::COL_O + half * DVH + c0, ov);
         if constexpr (JVP) tmem_ld_32x32b_x32(tl + P::COL_TO + half * DVH + c0, tv);
-        tmem_wait_ld();
+        tmem_wait_ld_regs(ov);
+        if constexpr (JVP) tmem_regs_ready(tv);
         uint32_t po[16], pt[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
