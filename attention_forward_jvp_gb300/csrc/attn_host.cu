@@ -13,9 +13,17 @@
 #include "attn_jvp.h"
 #include "attn_kernel.cuh"
 
+// The kernels are instantiated once, in the attn_inst_*.cu files; these
+// declarations keep this file from instantiating its own copies.
 namespace attn {
-template <int DQK, int DV, bool JVP>
-cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream);
+extern template cudaError_t launch_attn<64, 64, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false>(const KernelParams&, int, cudaStream_t);
 }
 
 namespace {

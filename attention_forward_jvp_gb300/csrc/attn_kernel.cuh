@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t qfill = 0, kfill = 0, vfill = 0;
+      uint32_t qfill = 0, kfill = 0;
       bool last_q_loaded = false;
       bool skip = p.skip_first_load != 0;
       bool ok = true;
@@ -467,14 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (u >= p.num_units) break;
         const Unit w = decode_unit(p, u);
         if (w.nt == 0) continue;
+        // Q / K tiles arrive by bulk copy: the mbarrier wait alone orders
+        // them before the MMAs that read them (no tcgen05 fence needed).
         ok = wait_bar(bar(P::B_QF), quse & 1u, W);
         if (!ok) break;
-        tc_fence_after();
         for (int j = 0; j < w.nt; ++j) {
           const uint32_t ks = kuse % P::NK;
           ok = wait_bar(bar(P::B_KF + ks), (kuse / P::NK) & 1u, W);
           if (!ok) break;
-          tc_fence_after();
           const uint32_t sb = g & 1u;
           const uint32_t dS = tmem + sb * P::SBUF;
           const uint32_t sK = sbase + P::OFF_K + ks * P::K_STAGE;

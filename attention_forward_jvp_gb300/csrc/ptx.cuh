@@ -191,6 +191,12 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (tensor core, bulk copy) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Per-warpgroup register reallocation (all four warps of a warpgroup
 // execute the same instruction).
 template <int N>
