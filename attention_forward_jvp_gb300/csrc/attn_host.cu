@@ -5,6 +5,8 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <map>
+#include <utility>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -12,6 +14,10 @@
 
 #include "attn_jvp.h"
 #include "attn_kernel.cuh"
+#include "attn_plan.h"
+
+static_assert(attn::kPlanBM == attn::kBM && attn::kPlanBN == attn::kBN,
+              "the work list is planned with the kernel's tile sizes");
 
 // The kernels are instantiated once, in the attn_inst_*.cu files; these
 // declarations keep this file from instantiating its own copies.
@@ -30,10 +36,17 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Per-device scratch: word 0 = device error word.
 struct DeviceState {
-  int* scratch = nullptr;  // [0] = error word
+  int* scratch = nullptr;
   int num_sms = 0;
 };
+
+// Jagged work lists live in one buffer per (device, stream): word 0 = list
+// length, bytes [256, 256 + capacity * 8) = the list.  Calls on one stream
+// are ordered, so they can share it; calls on different streams never do.
+constexpr int kListOffsetBytes = 256;
+constexpr int kListCapacity = attn::kPlanListBytes / static_cast<int>(sizeof(int2));
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -70,6 +83,25 @@ attn_status device_state(DeviceState** out) {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   *out = &d;
+  return ATTN_OK;
+}
+
+std::mutex g_list_mu;
+std::map<std::pair<int, cudaStream_t>, int*> g_lists;
+
+// The work-list buffer of (current device, stream), allocated on first use
+// and kept until the process exits.
+attn_status stream_list(cudaStream_t stream, int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_list_mu);
+  int*& buf = g_lists[std::make_pair(dev, stream)];
+  if (buf == nullptr) {
+    void* p = nullptr;
+    if (cudaMalloc(&p, kListOffsetBytes + attn::kPlanListBytes) != cudaSuccess) return ATTN_ERR_CUDA;
+    buf = static_cast<int*>(p);
+  }
+  *out = buf;
   return ATTN_OK;
 }
 
@@ -212,6 +244,21 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   // start each launch at zero.
   if (fixed != nullptr && cudaMemsetAsync(ds->scratch, 0, sizeof(int), cs) != cudaSuccess)
     return ATTN_ERR_CUDA;
+  // Jagged: order the (sequence, query tile) pairs by cost on the device
+  // (the offsets live there) so the kernel can balance them.
+  // (The allocation-free entry point keeps the slot order.)
+  if (jagged && fixed == nullptr && attn::plan_jagged_supported(s->max_seq_len)) {
+    int* lbuf = nullptr;
+    const attn_status ls = stream_list(cs, &lbuf);
+    if (ls != ATTN_OK) return ls;
+    int2* list = reinterpret_cast<int2*>(reinterpret_cast<char*>(lbuf) + kListOffsetBytes);
+    if (attn::launch_plan_jagged(offsets, s->B, s->max_seq_len, causal ? 1 : 0, list, lbuf,
+                                 kListCapacity, cs) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1);
+    kp.unit_list = list;
+    kp.unit_count = lbuf;
+  }
   cudaError_t e = cudaErrorInvalidValue;
   const int key = (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
   if (jvp) {

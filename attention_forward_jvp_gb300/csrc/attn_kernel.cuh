@@ -73,7 +73,12 @@ struct KernelParams {
   int B, H, M, N;  // jagged: B = sequences, M = N = max_seq_len
   int jagged, causal;
   int n_mt;        // query tiles per (b, h) or per (sequence, h)
-  int num_units;
+  int num_units;   // units in the fixed slot order (B * H * n_mt)
+  // Jagged work list (optional): unit_count[0] (sequence, query tile) pairs,
+  // costliest first, at unit_list (x = sequence, y = tile); unit u is pair
+  // u / H, head u % H.  A count of -1 means the list was not written.
+  const int2* unit_list;
+  const int* unit_count;
   float scale_log2;  // sm_scale * log2(e)
   float sm_scale;
   const int* offsets;
@@ -160,9 +165,10 @@ struct Unit {
   bool active;
 };
 
-// Work unit u.  Causal dense units and jagged units are ordered by
-// descending query tile, so the costliest units start first.
-__device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
+// Work unit u.  Causal dense units and (without a work list) jagged units
+// are ordered by descending query tile, so the costliest units start first;
+// a jagged work list is already ordered by cost.
+__device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u, const int2* list) {
   Unit w;
   const int BH = p.B * p.H;
   if (!p.jagged) {
@@ -183,9 +189,18 @@ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
     w.kv_len = p.N;
     w.out0 = static_cast<long long>(bh) * p.M;
   } else {
-    const int mt = p.n_mt - 1 - u / BH;
-    const int r = u % BH;
-    const int b = r / p.H, h = r % p.H;
+    int mt, b, h;
+    if (list != nullptr) {
+      const int2 e = list[u / p.H];
+      b = e.x;
+      mt = e.y;
+      h = u % p.H;
+    } else {
+      mt = p.n_mt - 1 - u / BH;
+      const int r = u % BH;
+      b = r / p.H;
+      h = r % p.H;
+    }
     const int begin = __ldg(p.offsets + b), end = __ldg(p.offsets + b + 1);
     const int len = min(end - begin, p.max_seq_len);
     w.b = b;
@@ -331,6 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.err, p.timeout_ns};
+  // The units this launch walks: a jagged work list when one was written
+  // (by the planning kernel earlier on the stream), else the slot order.
+  const int2* list = nullptr;
+  int num_units = p.num_units;
+  if (p.unit_list != nullptr) {
+    const int c = __ldg(p.unit_count);
+    if (c >= 0) {
+      list = p.unit_list;
+      num_units = c * p.H;
+    }
+  }
 
   if (warp < 4) {
   setmaxnreg_dec<kLowRegs>();
@@ -343,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       bool ok = true;
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
-        if (u >= p.num_units) break;
-        const Unit w = decode_unit(p, u);
+        if (u >= num_units) break;
+        const Unit w = decode_unit(p, u, list);
         if (w.nt == 0) continue;
         ok = wait_bar(bar(P::B_QE), (qfill & 1u) ^ 1u, W);
         if (!ok) break;
@@ -396,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       bool ok = true;
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
-        if (u >= p.num_units) break;
-        const Unit w = decode_unit(p, u);
+        if (u >= num_units) break;
+        const Unit w = decode_unit(p, u, list);
         for (int j = 0; j < w.nt; ++j) {
           const int r = w.row0 + j * kBN;
           const uint32_t vs = vfill % P::NV;
@@ -464,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
-        if (u >= p.num_units) break;
-        const Unit w = decode_unit(p, u);
+        if (u >= num_units) break;
+        const Unit w = decode_unit(p, u, list);
         if (w.nt == 0) continue;
         // Q / K tiles arrive by bulk copy: the mbarrier wait alone orders
         // them before the MMAs that read them (no tcgen05 fence needed).
@@ -547,8 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_of_round(rnd);
-      if (u >= p.num_units) break;
-      const Unit w = decode_unit(p, u);
+      if (u >= num_units) break;
+      const Unit w = decode_unit(p, u, list);
       if (!w.active) continue;
       const int qi = w.mt * kBM + row;
       const bool row_ok = qi < w.q_len;

@@ -266,3 +266,28 @@ def test_timed_out_wait_is_reported_and_context_survives():
     assert binding.sync_check() == 0  # cleared
     O, tO, L = run_gpu(inp)
     assert_close(O, tO, L, *oracle_dense(inp), what="after timeout")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_jagged_work_list_writes_every_row(causal):
+    """The jagged launch walks a device-built, cost-ordered work list: with
+    NaN-prefilled outputs every row of every sequence must be written."""
+    lens = [700, 3, 129, 0, 512, 64, 65, 1000, 257, 31]
+    w = Workload("jl", B=len(lens), H=4, Dqk=64, Dv=64, jagged=True, max_seq_len=900,
+                 max_len_draw=1, causal=causal, sm_scale=0.125)
+    inp = make_inputs(w, seed=13, lengths=lens)
+    T = inp["q"].shape[1]
+    d = {n: inp[n].cuda() for n in ("q", "k", "v", "tq", "tk", "tv")}
+    o = torch.full((4, T, 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    to = torch.full((4, T, 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((4, T), float("nan"), dtype=torch.float32, device="cuda")
+    binding.attn_fwd_jvp(d["q"], d["k"], d["v"], d["tq"], d["tk"], d["tv"], causal=causal,
+                         sm_scale=0.125, offsets=inp["offsets"].cuda(), max_seq_len=900,
+                         out=(o, to, lse))
+    assert binding.sync_check() == 0
+    O, tO, L = (x.float().cpu().numpy() for x in (o, to, lse))
+    assert not np.isnan(O).any() and not np.isnan(tO).any() and not np.isnan(L).any()
+    Or, tOr, Lr = oracle.attention_fwd_jvp_jagged(
+        inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"], inp["offsets"], 900,
+        causal=causal, sm_scale=0.125)
+    assert_close(O, tO, L, Or, tOr, Lr, what=f"jagged list causal={causal}")
