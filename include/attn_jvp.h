@@ -54,8 +54,11 @@
  *     next attn_sync_check on that device.
  *   - Supported head dims: Dqk, Dv in {64, 128}; otherwise
  *     ATTN_ERR_UNSUPPORTED.
- *   - The library allocates one small per-device scratch buffer (error
- *     word) on first use and keeps it until the process exits.
+ *   - The library allocates, on first use, one small per-device scratch
+ *     buffer (error word) and, for jagged calls, one 1 MB work-list buffer
+ *     per (device, stream); it keeps them until the process exits.  A
+ *     jagged call launches a one-block planning kernel before the attention
+ *     kernel, on the same stream.
  */
 #ifndef ATTN_JVP_H
 #define ATTN_JVP_H
@@ -130,7 +133,9 @@ attn_status attn_fwd(const attn_shape* shape,
  * of a buffer from cudaMalloc; every device that loads the library holds it
  * until the process exits.  A problem that would need more scratch than
  * the array holds is rejected with ATTN_ERR_UNSUPPORTED; no problem the
- * current kernels accept does.  Nothing here calls cudaMalloc, cudaFree or
+ * current kernels accept does.  Jagged calls here skip the cost-ordered
+ * work list (it needs a buffer) and walk the units in the fixed slot order,
+ * which balances less well.  Nothing here calls cudaMalloc, cudaFree or
  * any allocating library routine.
  *
  * The first call on a device (with that device current) looks up the
