@@ -609,7 +609,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int j = 0; j < w.nt; ++j, ++g) {
         const uint32_t sb = g & 1u;
         const int key0 = j * kBN + half * kHalf;  // first key of this thread's columns
-        // Prefetch this tile's bias / mask entries before waiting on S.
+        // Bias rows stream from HBM once: pull this thread's segment of the
+        // tile two steps ahead into L2 (the first two tiles at unit start),
+        // then load this tile's entries before waiting on S.
+        if (has_bias && row_ok && p.bias_stride[3] == 1) {
+          const float* bp = brow + half * kHalf;
+          if (j == 0) {
+            prefetch_l2(bp);
+            if (w.nt > 1) prefetch_l2(bp + kBN);
+          }
+          if (j + 2 < w.nt) prefetch_l2(bp + (j + 2) * kBN);
+        }
         float bv[kHalf];
         uint32_t mv[kHalf / 4];
         if (has_bias) {

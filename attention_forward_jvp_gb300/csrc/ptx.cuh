@@ -45,6 +45,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Pull the cache line holding `p` into L2 (a hint; no data is returned).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------- bulk tensor copy
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
