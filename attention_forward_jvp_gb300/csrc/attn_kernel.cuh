@@ -449,93 +449,114 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(kBM, JVP ? 2 * kBN : kBN, false);  // [S | Q tK^T]
-      constexpr uint32_t idesc_t = idesc_bf16(kBM, kBN, false);                   // tQ K^T
-      constexpr uint32_t idesc_o = idesc_bf16(kBM, P::NQ * DV, true);             // [O | tO]
-      constexpr uint32_t idesc_h = idesc_bf16(kBM, DV, true);                     // H V
-      uint32_t quse = 0, kuse = 0, vuse = 0, g = 0;
-      bool ok = true;
-      const uint32_t sQ = sbase + P::OFF_Q, sTQ = sbase + P::OFF_TQ;
+    // The whole warp walks the issue loop, so descriptors and addresses are
+    // warp-uniform values; one lane, elected once, issues every tcgen05
+    // instruction.  (An issuer running alone in a diverged warp competes
+    // for issue slots with the softmax warps of its sub-partition and lets
+    // the tensor pipe run dry between MMAs.)
+    const bool leader = elect_one();
+    constexpr uint32_t idesc_s = idesc_bf16(kBM, JVP ? 2 * kBN : kBN, false);  // [S | Q tK^T]
+    constexpr uint32_t idesc_t = idesc_bf16(kBM, kBN, false);                   // tQ K^T
+    constexpr uint32_t idesc_o = idesc_bf16(kBM, P::NQ * DV, true);             // [O | tO]
+    constexpr uint32_t idesc_h = idesc_bf16(kBM, DV, true);                     // H V
+    uint32_t quse = 0, kuse = 0, vuse = 0, g = 0;
+    bool ok = true;
+    const uint32_t sQ = sbase + P::OFF_Q, sTQ = sbase + P::OFF_TQ;
+    auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, wait_bar(b, parity, W));
+    };
 
-      // [O | tO] += P [V | tV] ; tO += H V   for global tile index gi
-      auto issue_pv = [&](uint32_t gi, bool first) -> bool {
-        const uint32_t sb = gi & 1u;
-        if (!wait_bar(bar(P::B_PF + sb), (gi >> 1) & 1u, W)) return false;
-        const uint32_t vs = vuse % P::NV;
-        if (!wait_bar(bar(P::B_VF + vs), (vuse / P::NV) & 1u, W)) return false;
-        tc_fence_after();
-        const uint32_t sV = sbase + P::OFF_V + vs * P::V_STAGE;
-        // keys [16 kk, 16 kk + 16): P at column base + 32 (kk / 2) + 8 (kk % 2),
-        // H 16 columns further (the layout the softmax halves write)
-        const uint32_t aP = tmem + sb * P::SBUF + kBN;
+    // [O | tO] += P [V | tV] ; tO += H V   for global tile index gi
+    auto issue_pv = [&](uint32_t gi, bool first) -> bool {
+      const uint32_t sb = gi & 1u;
+      if (!wait_all(bar(P::B_PF + sb), (gi >> 1) & 1u)) return false;
+      const uint32_t vs = vuse % P::NV;
+      if (!wait_all(bar(P::B_VF + vs), (vuse / P::NV) & 1u)) return false;
+      tc_fence_after();
+      const uint32_t sV = sbase + P::OFF_V + vs * P::V_STAGE;
+      // keys [16 kk, 16 kk + 16): P at column base + 32 (kk / 2) + 8 (kk % 2),
+      // H 16 columns further (the layout the softmax halves write)
+      const uint32_t aP = tmem + sb * P::SBUF + kBN;
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
+        if (leader)
+          mma_ts(tmem + P::COL_O, aP + 32 * (kk >> 1) + 8 * (kk & 1), dv, idesc_o,
+                 (first && kk == 0) ? 0u : 1u);
+        __syncwarp();
+      }
+      if (JVP) {
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
-          mma_ts(tmem + P::COL_O, aP + 32 * (kk >> 1) + 8 * (kk & 1), dv, idesc_o,
-                 (first && kk == 0) ? 0u : 1u);
+          if (leader) mma_ts(tmem + P::COL_TO, aP + 32 * (kk >> 1) + 16 + 8 * (kk & 1), dv, idesc_h, 1u);
+          __syncwarp();
+        }
+      }
+      if (leader) {
+        tc_commit(bar(P::B_VE + vs));
+        tc_commit(bar(P::B_OD));
+      }
+      __syncwarp();
+      ++vuse;
+      return true;
+    };
+
+    for (int rnd = 0; ok; ++rnd) {
+      const int u = unit_of_round(rnd);
+      if (u >= num_units) break;
+      const Unit w = decode_unit(p, u, list);
+      if (w.nt == 0) continue;
+      // Q / K tiles arrive by bulk copy: the mbarrier wait alone orders
+      // them before the MMAs that read them (no tcgen05 fence needed).
+      ok = wait_all(bar(P::B_QF), quse & 1u);
+      if (!ok) break;
+      for (int j = 0; j < w.nt; ++j) {
+        const uint32_t ks = kuse % P::NK;
+        ok = wait_all(bar(P::B_KF + ks), (kuse / P::NK) & 1u);
+        if (!ok) break;
+        const uint32_t sb = g & 1u;
+        const uint32_t dS = tmem + sb * P::SBUF;
+        const uint32_t sK = sbase + P::OFF_K + ks * P::K_STAGE;
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t dq = sdesc_sw128(sQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
+          const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
+          if (leader) mma_ss(dS, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
+          __syncwarp();
         }
         if (JVP) {
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
-            mma_ts(tmem + P::COL_TO, aP + 32 * (kk >> 1) + 16 + 8 * (kk & 1), dv, idesc_h, 1u);
-          }
-        }
-        tc_commit(bar(P::B_VE + vs));
-        tc_commit(bar(P::B_OD));
-        ++vuse;
-        return true;
-      };
-
-      for (int rnd = 0; ok; ++rnd) {
-        const int u = unit_of_round(rnd);
-        if (u >= num_units) break;
-        const Unit w = decode_unit(p, u, list);
-        if (w.nt == 0) continue;
-        // Q / K tiles arrive by bulk copy: the mbarrier wait alone orders
-        // them before the MMAs that read them (no tcgen05 fence needed).
-        ok = wait_bar(bar(P::B_QF), quse & 1u, W);
-        if (!ok) break;
-        for (int j = 0; j < w.nt; ++j) {
-          const uint32_t ks = kuse % P::NK;
-          ok = wait_bar(bar(P::B_KF + ks), (kuse / P::NK) & 1u, W);
-          if (!ok) break;
-          const uint32_t sb = g & 1u;
-          const uint32_t dS = tmem + sb * P::SBUF;
-          const uint32_t sK = sbase + P::OFF_K + ks * P::K_STAGE;
-#pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = (kk & 3) * 32;
-            const uint64_t dq = sdesc_sw128(sQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
+            const uint64_t dtq = sdesc_sw128(sTQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
             const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
-            mma_ss(dS, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
+            if (leader) mma_ss(dS + kBN, dtq, dk, idesc_t, 1u);
+            __syncwarp();
           }
-          if (JVP) {
-#pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint32_t off = (kk & 3) * 32;
-              const uint64_t dtq = sdesc_sw128(sTQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
-              const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
-              mma_ss(dS + kBN, dtq, dk, idesc_t, 1u);
-            }
-          }
+        }
+        if (leader) {
           tc_commit(bar(P::B_SF + sb));
           tc_commit(bar(P::B_KE + ks));
-          ++kuse;
           if (j == w.nt - 1) tc_commit(bar(P::B_QE));
-          if (j > 0) {
-            ok = issue_pv(g - 1, j == 1);
-            if (!ok) break;
-          }
-          ++g;
         }
-        if (!ok) break;
-        ok = issue_pv(g - 1, w.nt == 1);
-        if (ok) tc_commit(bar(P::B_OF));
-        ++quse;
+        __syncwarp();
+        ++kuse;
+        if (j > 0) {
+          ok = issue_pv(g - 1, j == 1);
+          if (!ok) break;
+        }
+        ++g;
       }
-      // Teardown: all MMAs issued by this thread complete before TMEM is freed.
+      if (!ok) break;
+      ok = issue_pv(g - 1, w.nt == 1);
+      if (ok && leader) tc_commit(bar(P::B_OF));
+      __syncwarp();
+      ++quse;
+    }
+    // Teardown: all MMAs issued by the leader complete before TMEM is freed.
+    if (leader) {
       tc_commit(bar(P::B_DRAIN));
       drain_bar(bar(P::B_DRAIN), 0, p.timeout_ns);
     }

@@ -212,7 +212,7 @@ def oracle_sample(w, inp, n_units: int, start: int = 0):
         dt = time.perf_counter() - t0
         lens = np.minimum(off[1:] - off[:-1], w.max_seq_len)[seqs].astype(np.float64)
         fl = 6.0 * (w.Dqk + w.Dv) * float((lens ** 2).sum()) * w.H * (0.5 if w.causal else 1.0)
-        return dt, fl, f"{n_units} sequences x {w.H} heads of the {w.name} workload"
+        return dt, fl, oracle_sample_desc(w, n_units)
     BH = w.B * w.H
     units = [(start + i) % BH for i in range(n_units)]
     q64 = {n: None for n in ("q", "k", "v", "tq", "tk", "tv")}
@@ -231,8 +231,14 @@ def oracle_sample(w, inp, n_units: int, start: int = 0):
                             inp["sm_scale"], w.causal, bias, mask)
     dt = time.perf_counter() - t0
     fl = 6.0 * (w.Dqk + w.Dv) * w.M * w.N * n_units * (0.5 if w.causal else 1.0)
-    return dt, fl, (f"{n_units} of {BH} (batch, head) pairs of the {w.name} workload, all rows, "
-                    "float64 NumPy (the oracle computes the full score matrix even when causal)")
+    return dt, fl, oracle_sample_desc(w, n_units)
+
+
+def oracle_sample_desc(w, n_units: int) -> str:
+    if w.jagged:
+        return f"{n_units} sequences x {w.H} heads of the {w.name} workload"
+    return (f"{n_units} of {w.B * w.H} (batch, head) pairs of the {w.name} workload, all rows, "
+            "float64 NumPy (the oracle computes the full score matrix even when causal)")
 
 
 def run_reference(args, w, world, rank):
@@ -355,8 +361,17 @@ def run_ours(args, w, world, rank, local):
             "hbm_gbs": min_hbm_bytes(w, inp) / (ms * 1e-3) / 1e9}
     cpu = None
     if world == 1 and not args.skip_cpu_baseline:
-        n_units = args.cpu_sample
-        dt, fl, desc = oracle_sample(w, inp, n_units)
+        # heads (jagged: sequences) one at a time until about cpu_seconds of
+        # oracle work, or the whole workload, whichever comes first
+        n_all = w.B if w.jagged else w.B * w.H
+        dt = fl = 0.0
+        n = 0
+        while n < n_all and (n == 0 or dt < args.cpu_seconds):
+            d1, f1, _ = oracle_sample(w, inp, 1, start=n)
+            dt += d1
+            fl += f1
+            n += 1
+        desc = oracle_sample_desc(w, n)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                "sample": desc, "seconds": dt}
     line = {
@@ -382,11 +397,12 @@ def run_ours(args, w, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="causal", choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-sample", type=int, default=4, help="heads in the CPU-baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="approximate seconds of oracle work in the CPU-baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
