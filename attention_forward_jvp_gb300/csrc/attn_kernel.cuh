@@ -22,7 +22,8 @@
 //               accumulated into one tO.  S / tS are double buffered in
 //               TMEM; P and H (bf16) are written back over the S / tS
 //               columns they came from and read by the MMA from TMEM.
-//   warp 3      idle (it completes warpgroup 0 for the register split).
+//   warp 3      release warp: frees each K stage (and Q at the end of a
+//               unit) as soon as the score MMAs that read it are done.
 //   warps 4..11 softmax / rescale / epilogue: two warps per TMEM lane
 //               quadrant, each taking 32 of the 64 key columns of a row
 //               (row = TMEM lane).  The pair exchanges its partial row
@@ -54,7 +55,7 @@ constexpr int kBN = 64;        // keys per pipeline step
 constexpr int kHalf = kBN / 2; // key columns per softmax thread
 constexpr int kThreads = 384;  // 12 warps = 3 warpgroups
 // Register split (setmaxnreg): the kernel is launched with kLaunchRegs per
-// thread; warpgroup 0 (producers, MMA issuer, one idle warp) gives registers
+// thread; warpgroup 0 (producers, MMA issuer, release warp) gives registers
 // back and the two softmax warpgroups take them:
 //   4 warps x 32 x kLowRegs + 8 warps x 32 x kHighRegs = 384 x kLaunchRegs.
 constexpr int kLaunchRegs = 168;
@@ -125,12 +126,16 @@ struct Plan {
   static constexpr int OFF_V = OFF_K + NK * K_STAGE;
   static constexpr int OFF_BAR = OFF_V + NV * V_STAGE;
   // barriers: q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-  //           s_full[2], p_full[2], o_done (every tile), o_final (last tile of
-  //           a unit), mma_drain, pair[4] (the two softmax warps of a quadrant)
+  //           s_full[2], p_full[2], mma_drain, pair[4] (the two softmax warps
+  //           of a quadrant).  v_empty of tile t's stage completes when the
+  //           output MMAs of tile t (and every MMA before them) are done; the
+  //           softmax warps wait on it too (lazy rescale, epilogue).
+  //           k_empty and q_empty are arrived on by the release warp once the
+  //           score MMAs that read the stage (Q: of the unit's last tile) are
+  //           done.
   static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + NK, B_VF = B_KE + NK,
-                       B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2, B_OD = B_PF + 2,
-                       B_OF = B_OD + 1, B_DRAIN = B_OF + 1, B_PAIR = B_DRAIN + 1,
-                       NBAR = B_PAIR + 4;
+                       B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2,
+                       B_DRAIN = B_PF + 2, B_PAIR = B_DRAIN + 1, NBAR = B_PAIR + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int OFF_XCHG = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = OFF_XCHG + XCHG_FLOATS * 4;
@@ -251,6 +256,21 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
   }
 }
 
+// wait_bar for a warp with nothing else to do: it sleeps inside the poll.
+__device__ __forceinline__ bool wait_bar_sleep(uint32_t bar, uint32_t parity, const Waiter& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*w.abort_flag) return false;
+    if (globaltimer_ns() - t0 > w.timeout_ns) {
+      *w.abort_flag = 1;
+      atomicCAS(w.err, 0, ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Bounded wait that ignores the abort flag (teardown drains).
 __device__ __forceinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigned long long ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -318,10 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(P::B_SF + i), 1);
-      mbar_init(bar(P::B_PF + i), 8);  // one arrival per softmax warp
+      mbar_init(bar(P::B_PF + i), 9);  // one arrival per softmax warp + the release warp
     }
-    mbar_init(bar(P::B_OD), 1);
-    mbar_init(bar(P::B_OF), 1);
     mbar_init(bar(P::B_DRAIN), 1);
     for (int i = 0; i < 4; ++i) mbar_init(bar(P::B_PAIR + i), 64);
     *abort_flag = 0;
@@ -447,33 +465,108 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
     }
     __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------- release warp
+    // Frees the K stage of tile g (and Q after a unit's last tile) as soon
+    // as the score MMAs of tile g are done, without costing the MMA issuer
+    // a commit.  It also arrives on p_full of tile g, so the output MMAs of
+    // tile g -- and hence the score MMAs of tile g+2, the next phase of the
+    // same s_full barrier -- cannot be issued before it has seen s_full of
+    // tile g: its parity waits are unambiguous.
+    uint32_t g = 0;
+    bool ok = true;
+    for (int rnd = 0; ok; ++rnd) {
+      const int u = unit_of_round(rnd);
+      if (u >= num_units) break;
+      const Unit w = decode_unit(p, u, list);
+      for (int j = 0; j < w.nt; ++j, ++g) {
+        ok = __all_sync(0xffffffffu, wait_bar_sleep(bar(P::B_SF + (g & 1u)), (g >> 1) & 1u, W));
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive(bar(P::B_KE + g % P::NK));
+          if (j == w.nt - 1) mbar_arrive(bar(P::B_QE));
+          mbar_arrive(bar(P::B_PF + (g & 1u)));
+        }
+        __syncwarp();
+      }
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     // The whole warp walks the issue loop, so descriptors and addresses are
     // warp-uniform values; one lane, elected once, issues every tcgen05
     // instruction.  (An issuer running alone in a diverged warp competes
     // for issue slots with the softmax warps of its sub-partition and lets
-    // the tensor pipe run dry between MMAs.)
+    // the tensor pipe run dry between MMAs.)  Each mbarrier poll stalls
+    // issue for a round trip even when the barrier is already complete, so
+    // the waits for the K / V tiles of the next batches are placed in the
+    // middle of a batch, while the tensor pipe still holds queued MMAs.
     const bool leader = elect_one();
     constexpr uint32_t idesc_s = idesc_bf16(kBM, JVP ? 2 * kBN : kBN, false);  // [S | Q tK^T]
     constexpr uint32_t idesc_t = idesc_bf16(kBM, kBN, false);                   // tQ K^T
     constexpr uint32_t idesc_o = idesc_bf16(kBM, P::NQ * DV, true);             // [O | tO]
     constexpr uint32_t idesc_h = idesc_bf16(kBM, DV, true);                     // H V
-    uint32_t quse = 0, kuse = 0, vuse = 0, g = 0;
-    bool ok = true;
     const uint32_t sQ = sbase + P::OFF_Q, sTQ = sbase + P::OFF_TQ;
     auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, wait_bar(b, parity, W));
     };
+    // K tile t sits in stage t % NK (fill round t / NK), V tile t in stage
+    // t % NV.  Q / K / V arrive by bulk copy: the mbarrier wait alone orders
+    // them before the MMAs that read them (no tcgen05 fence needed).
+    // In the middle of a batch the tiles of the next batch are only polled
+    // once (k_seen / v_seen record a tile found resident); a tile not yet
+    // resident is waited for just before the batch that reads it, so a slow
+    // copy never holds back the rest of the current batch.
+    uint32_t k_seen = 0xffffffffu, v_seen = 0xffffffffu;
+    auto poll_k = [&](uint32_t t) {
+      if (__all_sync(0xffffffffu, mbar_try_wait(bar(P::B_KF + t % P::NK), (t / P::NK) & 1u))) k_seen = t;
+    };
+    auto poll_v = [&](uint32_t t) {
+      if (__all_sync(0xffffffffu, mbar_try_wait(bar(P::B_VF + t % P::NV), (t / P::NV) & 1u))) v_seen = t;
+    };
+    auto wait_k = [&](uint32_t t) {
+      return k_seen == t || wait_all(bar(P::B_KF + t % P::NK), (t / P::NK) & 1u);
+    };
+    auto wait_v = [&](uint32_t t) {
+      return v_seen == t || wait_all(bar(P::B_VF + t % P::NV), (t / P::NV) & 1u);
+    };
 
-    // [O | tO] += P [V | tV] ; tO += H V   for global tile index gi
-    auto issue_pv = [&](uint32_t gi, bool first) -> bool {
-      const uint32_t sb = gi & 1u;
-      if (!wait_all(bar(P::B_PF + sb), (gi >> 1) & 1u)) return false;
-      const uint32_t vs = vuse % P::NV;
-      if (!wait_all(bar(P::B_VF + vs), (vuse / P::NV) & 1u)) return false;
+    // [S | Q tK^T] = Q [K ; tK]^T, tS += tQ K^T for tile t; `mid` runs after
+    // the first half of the first chain.
+    auto issue_s = [&](uint32_t t, auto&& mid) -> bool {
+      if (!wait_k(t)) return false;
+      const uint32_t dS = tmem + (t & 1u) * P::SBUF;
+      const uint32_t sK = sbase + P::OFF_K + (t % P::NK) * P::K_STAGE;
+#pragma unroll
+      for (int kk = 0; kk < DQK / 16; ++kk) {
+        const uint32_t off = (kk & 3) * 32;
+        const uint64_t dq = sdesc_sw128(sQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
+        const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
+        if (leader) mma_ss(dS, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
+        __syncwarp();
+        if (kk == DQK / 32 - 1) mid();
+      }
+      if (JVP) {
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t dtq = sdesc_sw128(sTQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
+          const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
+          if (leader) mma_ss(dS + kBN, dtq, dk, idesc_t, 1u);
+          __syncwarp();
+        }
+      }
+      if (leader) tc_commit(bar(P::B_SF + (t & 1u)));
+      __syncwarp();
+      return true;
+    };
+
+    // [O | tO] += P [V | tV] ; tO += H V for tile t, once its P and H are
+    // written; `mid` runs after the first half of the first chain.
+    auto issue_pv = [&](uint32_t t, bool first, auto&& mid) -> bool {
+      const uint32_t sb = t & 1u;
+      if (!wait_v(t) || !wait_all(bar(P::B_PF + sb), (t >> 1) & 1u)) return false;
       tc_fence_after();
-      const uint32_t sV = sbase + P::OFF_V + vs * P::V_STAGE;
+      const uint32_t sV = sbase + P::OFF_V + (t % P::NV) * P::V_STAGE;
       // keys [16 kk, 16 kk + 16): P at column base + 32 (kk / 2) + 8 (kk % 2),
       // H 16 columns further (the layout the softmax halves write)
       const uint32_t aP = tmem + sb * P::SBUF + kBN;
@@ -484,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           mma_ts(tmem + P::COL_O, aP + 32 * (kk >> 1) + 8 * (kk & 1), dv, idesc_o,
                  (first && kk == 0) ? 0u : 1u);
         __syncwarp();
+        if (kk == kBN / 32 - 1) mid();
       }
       if (JVP) {
 #pragma unroll
@@ -493,66 +587,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           __syncwarp();
         }
       }
-      if (leader) {
-        tc_commit(bar(P::B_VE + vs));
-        tc_commit(bar(P::B_OD));
-      }
+      if (leader) tc_commit(bar(P::B_VE + t % P::NV));
       __syncwarp();
-      ++vuse;
       return true;
     };
 
+    // Issue order per unit: S(t0), S(t0+1), PV(t0), S(t0+2), PV(t0+1), ...,
+    // PV(last).  The K tile of S(t+1) is polled inside the batch before it
+    // (S(t0) for t0+1, else PV(t-1)); the V tile of PV(t) inside S(t+1)
+    // (S(last) for the unit's last tile).
+    uint32_t quse = 0, g = 0;  // g: global tile counter (same in every role)
+    bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_of_round(rnd);
       if (u >= num_units) break;
       const Unit w = decode_unit(p, u, list);
       if (w.nt == 0) continue;
-      // Q / K tiles arrive by bulk copy: the mbarrier wait alone orders
-      // them before the MMAs that read them (no tcgen05 fence needed).
       ok = wait_all(bar(P::B_QF), quse & 1u);
       if (!ok) break;
-      for (int j = 0; j < w.nt; ++j) {
-        const uint32_t ks = kuse % P::NK;
-        ok = wait_all(bar(P::B_KF + ks), (kuse / P::NK) & 1u);
+      for (int j = 0; j < w.nt; ++j, ++g) {
+        ok = issue_s(g, [&]() {
+          if (j > 0) poll_v(g - 1);
+          if (j == w.nt - 1) poll_v(g);
+          else if (j == 0) poll_k(g + 1);
+        });
         if (!ok) break;
-        const uint32_t sb = g & 1u;
-        const uint32_t dS = tmem + sb * P::SBUF;
-        const uint32_t sK = sbase + P::OFF_K + ks * P::K_STAGE;
-#pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          const uint64_t dq = sdesc_sw128(sQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
-          const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
-          if (leader) mma_ss(dS, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
-          __syncwarp();
-        }
-        if (JVP) {
-#pragma unroll
-          for (int kk = 0; kk < DQK / 16; ++kk) {
-            const uint32_t off = (kk & 3) * 32;
-            const uint64_t dtq = sdesc_sw128(sTQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
-            const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
-            if (leader) mma_ss(dS + kBN, dtq, dk, idesc_t, 1u);
-            __syncwarp();
-          }
-        }
-        if (leader) {
-          tc_commit(bar(P::B_SF + sb));
-          tc_commit(bar(P::B_KE + ks));
-          if (j == w.nt - 1) tc_commit(bar(P::B_QE));
-        }
-        __syncwarp();
-        ++kuse;
         if (j > 0) {
-          ok = issue_pv(g - 1, j == 1);
+          ok = issue_pv(g - 1, j == 1, [&]() {
+            if (j + 1 < w.nt) poll_k(g + 1);
+          });
           if (!ok) break;
         }
-        ++g;
       }
       if (!ok) break;
-      ok = issue_pv(g - 1, w.nt == 1);
-      if (ok && leader) tc_commit(bar(P::B_OF));
-      __syncwarp();
+      ok = issue_pv(g - 1, w.nt == 1, []() {});
       ++quse;
     }
     // Teardown: all MMAs issued by the leader complete before TMEM is freed.
@@ -590,7 +658,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint64_t scale2 = f2_make(p.sm_scale, p.sm_scale);
     uint32_t g = 0;           // global key-tile counter (same in every role)
     uint32_t gen = 0;         // masked tiles seen (slot parity of the max exchange)
-    uint32_t units_done = 0;  // units with keys finished (o_final parity)
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_of_round(rnd);
@@ -803,12 +870,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
         if (__any_sync(0xffffffffu, resc)) {
           // O and tO are rescaled in place, so the previous tile's output
-          // MMAs must have completed.  S of this tile is complete, and the
-          // MMA issue order puts tile g-2's output MMAs before this tile's
-          // score MMAs, so o_done has completed g-1 or g phases: waiting on
-          // parity (g-1) is unambiguous.  (resc is never set on a unit's
+          // MMAs must have completed: phase (g-1) / NV of v_empty of its
+          // stage.  The phase after it needs the output MMAs of tile
+          // g-1+NV > g, whose P this thread has not written yet, so the
+          // parity wait is unambiguous.  (resc is never set on a unit's
           // first tile, where m_run starts at -inf.)
-          ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_OD), (g - 1) & 1u, W));
+          ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + (g - 1) % P::NV), ((g - 1) / P::NV) & 1u, W));
           if (!ok) break;
           tc_fence_after();
           {
@@ -839,8 +906,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_OF), units_done & 1u, W));
-      ++units_done;
+      // every MMA of the unit is done once the output MMAs of its last tile
+      // (g - 1) are (same unambiguous parity argument as above)
+      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + (g - 1) % P::NV), ((g - 1) / P::NV) & 1u, W));
       if (!ok) break;
       tc_fence_after();
       // combine the two halves' partial sums through shared memory
