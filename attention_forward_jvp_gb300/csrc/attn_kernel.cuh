@@ -294,6 +294,19 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
     d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
 }
 
+// The same with 32-byte stores (dst 32-byte aligned, n32 a multiple of 8):
+// a warp storing one row segment per thread then writes whole 32-byte
+// sectors, with half the store instructions.
+__device__ __forceinline__ void store_row_bf16_32B(__nv_bfloat16* dst, const uint32_t* packed, int n32) {
+#pragma unroll
+  for (int i = 0; i < n32 / 8; ++i)
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * i),
+                 "r"(packed[8 * i]), "r"(packed[8 * i + 1]), "r"(packed[8 * i + 2]),
+                 "r"(packed[8 * i + 3]), "r"(packed[8 * i + 4]), "r"(packed[8 * i + 5]),
+                 "r"(packed[8 * i + 6]), "r"(packed[8 * i + 7])
+                 : "memory");
+}
+
 // Row maximum of 32 values, 3-input max tree.
 __device__ __forceinline__ float rowmax32(const float* x) {
   float a[11];
@@ -656,6 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const float* other_x1 = xchg + (1 * 2 + (half ^ 1)) * kBM + row;
     constexpr int DVH = DV / 2;  // output columns per softmax thread
     const uint64_t scale2 = f2_make(p.sm_scale, p.sm_scale);
+    const bool out32 = ((reinterpret_cast<uintptr_t>(p.o) | (JVP ? reinterpret_cast<uintptr_t>(p.to) : 0)) & 31u) == 0;
     uint32_t g = 0;           // global key-tile counter (same in every role)
     uint32_t gen = 0;         // masked tiles seen (slot parity of the max exchange)
     bool ok = true;
@@ -957,8 +971,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
         }
         if (row_ok) {
-          store_row_bf16(orow + c0, po, 16);
-          if constexpr (JVP) store_row_bf16(torow + c0, pt, 16);
+          // every row segment starts on a multiple of 64 bytes from the base
+          if (out32) {
+            store_row_bf16_32B(orow + c0, po, 16);
+            if constexpr (JVP) store_row_bf16_32B(torow + c0, pt, 16);
+          } else {
+            store_row_bf16(orow + c0, po, 16);
+            if constexpr (JVP) store_row_bf16(torow + c0, pt, 16);
+          }
         }
       }
       if (row_ok && half == 0)
