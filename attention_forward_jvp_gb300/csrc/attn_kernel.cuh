@@ -294,17 +294,50 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
     d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
 }
 
-// The same with 32-byte stores (dst 32-byte aligned, n32 a multiple of 8):
-// a warp storing one row segment per thread then writes whole 32-byte
-// sectors, with half the store instructions.
-__device__ __forceinline__ void store_row_bf16_32B(__nv_bfloat16* dst, const uint32_t* packed, int n32) {
+
+// Transpose 4 x 4 blocks across each quad of lanes: lane q of a quad holds
+// chunks 0..3 (C words each) of its own row; afterwards it holds chunk q of
+// the quad's four rows, slot k taken from lane k.  Two rounds of paired
+// shuffles (lanes q, q^2 then q, q^1), indices fixed at compile time.
+template <int C>
+__device__ __forceinline__ void quad_transpose(uint32_t (&a)[4 * C], int q) {
+  const bool hi2 = (q & 2) != 0;
 #pragma unroll
-  for (int i = 0; i < n32 / 8; ++i)
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * i),
-                 "r"(packed[8 * i]), "r"(packed[8 * i + 1]), "r"(packed[8 * i + 2]),
-                 "r"(packed[8 * i + 3]), "r"(packed[8 * i + 4]), "r"(packed[8 * i + 5]),
-                 "r"(packed[8 * i + 6]), "r"(packed[8 * i + 7])
+  for (int j = 0; j < 2; ++j) {
+#pragma unroll
+    for (int w = 0; w < C; ++w) {
+      const uint32_t send = hi2 ? a[j * C + w] : a[(j + 2) * C + w];
+      const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 2);
+      if (hi2) a[j * C + w] = got;
+      else a[(j + 2) * C + w] = got;
+    }
+  }
+  const bool hi1 = (q & 1) != 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+#pragma unroll
+    for (int w = 0; w < C; ++w) {
+      const uint32_t send = hi1 ? a[2 * j * C + w] : a[(2 * j + 1) * C + w];
+      const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 1);
+      if (hi1) a[2 * j * C + w] = got;
+      else a[(2 * j + 1) * C + w] = got;
+    }
+  }
+}
+
+// C packed words to global memory: one 32-byte store when C == 8 and the
+// address is 32-byte aligned, else 16-byte stores.
+template <int C>
+__device__ __forceinline__ void store_chunk(__nv_bfloat16* dst, const uint32_t* w, bool aligned32) {
+  if (C == 8 && aligned32) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                  : "memory");
+  } else {
+#pragma unroll
+    for (int i = 0; i < C / 4; ++i)
+      reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
 }
 
 // Row maximum of 32 values, 3-input max tree.
@@ -920,12 +953,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      // every MMA of the unit is done once the output MMAs of its last tile
-      // (g - 1) are (same unambiguous parity argument as above)
-      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + (g - 1) % P::NV), ((g - 1) / P::NV) & 1u, W));
-      if (!ok) break;
-      tc_fence_after();
-      // combine the two halves' partial sums through shared memory
+      // combine the two halves' partial sums through shared memory (this
+      // overlaps the output MMAs of the unit's last tile)
       float l_a, l_b, lt_a, lt_b, r_a, r_b;
       f2_split(l2, l_a, l_b);
       f2_split(lt2, lt_a, lt_b);
@@ -947,9 +976,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       l_sum += *other_x0;
       ok = pair_sync();  // slots free for the next unit
       if (!ok) break;
+      // every MMA of the unit is done once the output MMAs of its last tile
+      // (g - 1) are (same unambiguous parity argument as above)
+      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + (g - 1) % P::NV), ((g - 1) / P::NV) & 1u, W));
+      if (!ok) break;
+      tc_fence_after();
 
+      // O = O_acc / lt, tO = (tO_acc - r O) / lt as packed bf16 pairs, this
+      // thread's DVH columns of its row
       const bool empty = !(l_sum > 0.f);
       const float inv_l = empty ? 0.f : 1.f / lt_sum;
+      constexpr int NW = DVH / 2;  // packed words per half row
+      constexpr int CW = NW / 4;   // words per chunk (four chunks per half row)
+      uint32_t po[NW], pt[NW];
 #pragma unroll
       for (int c0 = 0; c0 < DVH; c0 += 32) {
         uint32_t ov[32];
@@ -958,31 +997,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if constexpr (JVP) tmem_ld_32x32b_x32(tl + P::COL_TO + half * DVH + c0, tv);
         tmem_wait_ld_regs(ov);
         if constexpr (JVP) tmem_regs_ready(tv);
-        uint32_t po[16], pt[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const float o0 = __uint_as_float(ov[i]) * inv_l;
           const float o1 = __uint_as_float(ov[i + 1]) * inv_l;
-          po[i / 2] = pack_bf16x2(o0, o1);
+          po[c0 / 2 + i / 2] = pack_bf16x2(o0, o1);
           if constexpr (JVP) {
             const float t0 = (__uint_as_float(tv[i]) - r_sum * o0) * inv_l;
             const float t1 = (__uint_as_float(tv[i + 1]) - r_sum * o1) * inv_l;
-            pt[i / 2] = pack_bf16x2(t0, t1);
-          }
-        }
-        if (row_ok) {
-          // every row segment starts on a multiple of 64 bytes from the base
-          if (out32) {
-            store_row_bf16_32B(orow + c0, po, 16);
-            if constexpr (JVP) store_row_bf16_32B(torow + c0, pt, 16);
-          } else {
-            store_row_bf16(orow + c0, po, 16);
-            if constexpr (JVP) store_row_bf16(torow + c0, pt, 16);
+            pt[c0 / 2 + i / 2] = pack_bf16x2(t0, t1);
           }
         }
       }
       if (row_ok && half == 0)
         p.lse[w.out0 + qi] = empty ? -INFINITY : (m_run + __log2f(l_sum)) * kLn2;
+      // Rows are stored a quad of lanes at a time: after the transpose lane q
+      // of a quad holds chunk q of the quad's four rows, so each store
+      // instruction writes eight whole row segments (contiguous per quad).
+      const int q = lane & 3;
+      quad_transpose<CW>(po, q);
+      if constexpr (JVP) quad_transpose<CW>(pt, q);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int qk = w.mt * kBM + quad * 32 + (lane & ~3) + k;  // row of slot k
+        if (qk < w.q_len) {
+          const long long off = (w.out0 + qk) * DV + half * DVH + q * 2 * CW;
+          store_chunk<CW>(p.o + off, po + k * CW, out32);
+          if constexpr (JVP) store_chunk<CW>(p.to + off, pt + k * CW, out32);
+        }
+      }
     }
 
     // Jagged rows past max_seq_len inside their sequence: empty rows.
