@@ -22,17 +22,44 @@ static_assert(attn::kPlanBM == attn::kBM && attn::kPlanBN == attn::kBN,
 // The kernels are instantiated once, in the attn_inst_*.cu files; these
 // declarations keep this file from instantiating its own copies.
 namespace attn {
-extern template cudaError_t launch_attn<64, 64, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, true>(const KernelParams&, int, cudaStream_t);
 }
 
 namespace {
+
+// The kernel instantiation for (Dqk, Dv) = key (bit 1: Dqk = 128, bit 0:
+// Dv = 128), tangents, bias / mask.
+template <bool JVP, bool BM>
+cudaError_t dispatch_dims(int key, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
+  switch (key) {
+    case 0: return attn::launch_attn<64, 64, JVP, BM>(kp, grid, cs);
+    case 1: return attn::launch_attn<64, 128, JVP, BM>(kp, grid, cs);
+    case 2: return attn::launch_attn<128, 64, JVP, BM>(kp, grid, cs);
+    case 3: return attn::launch_attn<128, 128, JVP, BM>(kp, grid, cs);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t dispatch_attn(int key, bool jvp, bool bm, const attn::KernelParams& kp, int grid,
+                          cudaStream_t cs) {
+  if (jvp) return bm ? dispatch_dims<true, true>(key, kp, grid, cs) : dispatch_dims<true, false>(key, kp, grid, cs);
+  return bm ? dispatch_dims<false, true>(key, kp, grid, cs) : dispatch_dims<false, false>(key, kp, grid, cs);
+}
 
 constexpr int kMaxDevices = 64;
 
@@ -261,21 +288,8 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   }
   cudaError_t e = cudaErrorInvalidValue;
   const int key = (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
-  if (jvp) {
-    switch (key) {
-      case 0: e = attn::launch_attn<64, 64, true>(kp, grid, cs); break;
-      case 1: e = attn::launch_attn<64, 128, true>(kp, grid, cs); break;
-      case 2: e = attn::launch_attn<128, 64, true>(kp, grid, cs); break;
-      case 3: e = attn::launch_attn<128, 128, true>(kp, grid, cs); break;
-    }
-  } else {
-    switch (key) {
-      case 0: e = attn::launch_attn<64, 64, false>(kp, grid, cs); break;
-      case 1: e = attn::launch_attn<64, 128, false>(kp, grid, cs); break;
-      case 2: e = attn::launch_attn<128, 64, false>(kp, grid, cs); break;
-      case 3: e = attn::launch_attn<128, 128, false>(kp, grid, cs); break;
-    }
-  }
+  const bool bm = kp.bias != nullptr || kp.mask != nullptr;
+  e = dispatch_attn(key, jvp, bm, kp, grid, cs);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   g_launches.fetch_add(1);
   return ATTN_OK;

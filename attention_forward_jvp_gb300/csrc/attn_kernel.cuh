@@ -351,7 +351,10 @@ __device__ __forceinline__ float rowmax32(const float* x) {
   return fmaxf(max3f(b0, b1, b2), b3);
 }
 
-template <int DQK, int DV, bool JVP>
+// BM: the launch carries an additive bias and / or a boolean mask.  Without
+// them the row maximum of every tile is taken locally (no exchange between
+// the two warps of a row), and none of the bias / mask code is compiled in.
+template <int DQK, int DV, bool JVP, bool BM>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KernelParams p) {
   using P = Plan<DQK, DV, JVP>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -694,8 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tc_fence_after();
       return r;
     };
-    const bool has_bias = p.bias != nullptr;
-    const bool has_mask = p.mask != nullptr;
+    const bool has_bias = BM && p.bias != nullptr;
+    const bool has_mask = BM && p.mask != nullptr;
     float* my_x0 = xchg + (0 * 2 + half) * kBM + row;
     float* my_x1 = xchg + (1 * 2 + half) * kBM + row;
     const float* other_x0 = xchg + (0 * 2 + (half ^ 1)) * kBM + row;
@@ -804,13 +807,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
         if (!ok) break;
         tc_fence_after();
-        // Unmasked tiles: each warp also reads the partner half's 32 score
-        // columns and takes the row maximum over all 64 itself, so the two
-        // warps of a quadrant never wait for each other.  Masked tiles
-        // (causal diagonal, ragged tail, bias / mask) exchange partial
-        // maxima through shared memory instead.
+        // Each warp also reads the partner half's 32 score columns and takes
+        // the row maximum over all 64 itself, so the two warps of a quadrant
+        // never wait for each other: unmasked tiles (`fast`) and, without
+        // bias or mask, causal-diagonal and ragged tiles (`local`, the mask
+        // applied to both halves).  With bias or mask the two warps exchange
+        // partial maxima through shared memory instead.
         const bool diag = p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
-        const bool fast = !has_bias && !has_mask && !diag && (j * kBN + kBN <= w.kv_len);
+        const bool fast = !BM && !diag && (j * kBN + kBN <= w.kv_len);
+        const bool local = !BM && !fast;
         uint32_t sr[kHalf];
         uint32_t so[kHalf];
         uint32_t tr[kHalf];
@@ -823,8 +828,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           // their load overlaps the row maximum and exp2 below
           if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
         } else {
+          if (local) tmem_ld_32x32b_x32(tl + sb * P::SBUF + (half ^ 1) * kHalf, so);
           if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
           tmem_wait_ld_regs(sr);
+          tmem_regs_ready(so);
           if constexpr (JVP) tmem_regs_ready(tr);
         }
         float x[kHalf];
@@ -853,16 +860,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if constexpr (JVP) tr[c] = keep ? tr[c] : 0u;
           }
           mx = rowmax32(x);
-          // the pair's row maximum over all 64 columns of the tile; the slot
-          // alternates per masked tile, and a writer can only come back to a
-          // slot after the rendezvous of the masked tile in between
-          float* mine = (gen & 1u) ? my_x1 : my_x0;
-          const float* theirs = (gen & 1u) ? other_x1 : other_x0;
-          ++gen;
-          *mine = mx;
-          ok = pair_sync();
-          if (!ok) break;
-          mx = fmaxf(mx, *theirs);
+          if constexpr (!BM) {
+            // the partner's columns under the same causal / key-length mask
+            const int keyo = j * kBN + (half ^ 1) * kHalf;
+            float xo[kHalf];
+#pragma unroll
+            for (int c = 0; c < kHalf; ++c) {
+              const int ko = keyo + c;
+              const bool keepo = ko < w.kv_len && (!p.causal || ko <= qi);
+              xo[c] = keepo ? __uint_as_float(so[c]) * p.scale_log2 : -INFINITY;
+            }
+            mx = fmaxf(mx, rowmax32(xo));
+          } else {
+            // the pair's row maximum over all 64 columns of the tile; the
+            // slot alternates per tile, and a writer can only come back to a
+            // slot after the rendezvous of the tile in between
+            float* mine = (gen & 1u) ? my_x1 : my_x0;
+            const float* theirs = (gen & 1u) ? other_x1 : other_x0;
+            ++gen;
+            *mine = mx;
+            ok = pair_sync();
+            if (!ok) break;
+            mx = fmaxf(mx, *theirs);
+          }
         }
 
         // lazy online-softmax update (identical in both halves)
@@ -1055,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, P::TMEM_COLS);
 }
 
-template <int DQK, int DV, bool JVP>
+template <int DQK, int DV, bool JVP, bool BM>
 cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
   using P = Plan<DQK, DV, JVP>;
   static bool attr_done[64] = {};
@@ -1067,16 +1087,16 @@ cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
     // computed for; a build that compiled to another count is refused
     // (setmaxnreg.inc would otherwise wait for registers that never free).
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP>);
+    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP, BM>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP, BM>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  attn_fwd_kernel<DQK, DV, JVP><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
+  attn_fwd_kernel<DQK, DV, JVP, BM><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
   return cudaGetLastError();
 }
 
