@@ -22,43 +22,60 @@ static_assert(attn::kPlanBM == attn::kBM && attn::kPlanBN == attn::kBN,
 // The kernels are instantiated once, in the attn_inst_*.cu files; these
 // declarations keep this file from instantiating its own copies.
 namespace attn {
-extern template cudaError_t launch_attn<64, 64, true, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, true, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kNoBias>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kBiasRing>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, kNoBias>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, kBiasRing>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, kNoBias>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, kBiasRing>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, kNoBias>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, kBiasRing>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kNoBias>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kBiasRing>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, kNoBias>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, kBiasRing>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, kNoBias>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, kBiasRing>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kNoBias>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kBiasRing>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
 }
 
 namespace {
 
 // The kernel instantiation for (Dqk, Dv) = key (bit 1: Dqk = 128, bit 0:
 // Dv = 128), tangents, bias / mask.
-template <bool JVP, bool BM>
+template <bool JVP, int BMODE>
 cudaError_t dispatch_dims(int key, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
   switch (key) {
-    case 0: return attn::launch_attn<64, 64, JVP, BM>(kp, grid, cs);
-    case 1: return attn::launch_attn<64, 128, JVP, BM>(kp, grid, cs);
-    case 2: return attn::launch_attn<128, 64, JVP, BM>(kp, grid, cs);
-    case 3: return attn::launch_attn<128, 128, JVP, BM>(kp, grid, cs);
+    case 0: return attn::launch_attn<64, 64, JVP, BMODE>(kp, grid, cs);
+    case 1: return attn::launch_attn<64, 128, JVP, BMODE>(kp, grid, cs);
+    case 2: return attn::launch_attn<128, 64, JVP, BMODE>(kp, grid, cs);
+    case 3: return attn::launch_attn<128, 128, JVP, BMODE>(kp, grid, cs);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t dispatch_attn(int key, bool jvp, bool bm, const attn::KernelParams& kp, int grid,
+template <bool JVP>
+cudaError_t dispatch_mode(int key, int mode, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
+  switch (mode) {
+    case attn::kNoBias: return dispatch_dims<JVP, attn::kNoBias>(key, kp, grid, cs);
+    case attn::kBiasRing: return dispatch_dims<JVP, attn::kBiasRing>(key, kp, grid, cs);
+    case attn::kBiasGlobal: return dispatch_dims<JVP, attn::kBiasGlobal>(key, kp, grid, cs);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t dispatch_attn(int key, bool jvp, int mode, const attn::KernelParams& kp, int grid,
                           cudaStream_t cs) {
-  if (jvp) return bm ? dispatch_dims<true, true>(key, kp, grid, cs) : dispatch_dims<true, false>(key, kp, grid, cs);
-  return bm ? dispatch_dims<false, true>(key, kp, grid, cs) : dispatch_dims<false, false>(key, kp, grid, cs);
+  return jvp ? dispatch_mode<true>(key, mode, kp, grid, cs) : dispatch_mode<false>(key, mode, kp, grid, cs);
 }
 
 constexpr int kMaxDevices = 64;
@@ -149,6 +166,36 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t d, uint64_t rows, uin
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// 4-D fp32 view of the bias [b][h][m][n] (n innermost), box 32 x 128 x 1 x
+// 1, 128-byte swizzle, keys / rows past the end read as zeros.  A broadcast
+// (stride 0) head or batch dimension becomes a size-1 dimension.  Returns
+// false (the kernel then reads the bias per thread) when the layout does not
+// fit a tensor map: key stride other than 1, a row / head / batch stride
+// that is not a multiple of 4 elements, a broadcast query-row dimension, or
+// a base that is not 16-byte aligned.
+bool encode_bias_map(CUtensorMap* m, const float* base, const int64_t* st, uint64_t B, uint64_t H,
+                     uint64_t M, uint64_t N, int* bcast_h, int* bcast_b) {
+  if (base == nullptr || !aligned16(base) || st[3] != 1 || st[2] <= 0 || N == 0 || M == 0)
+    return false;
+  for (int i = 0; i < 3; ++i)
+    if (st[i] < 0 || (st[i] % 4) != 0) return false;
+  *bcast_h = st[1] == 0 ? 1 : 0;
+  *bcast_b = st[0] == 0 ? 1 : 0;
+  cuuint64_t dims[4] = {N, M, *bcast_h ? 1 : H, *bcast_b ? 1 : B};
+  // strides of size-1 dimensions are never stepped; give them the extent
+  // of the dimension below
+  const uint64_t s2 = static_cast<uint64_t>(st[2]) * 4;
+  const uint64_t s1 = *bcast_h ? s2 * M : static_cast<uint64_t>(st[1]) * 4;
+  const uint64_t s0 = *bcast_b ? s1 * dims[2] : static_cast<uint64_t>(st[0]) * 4;
+  cuuint64_t strides[3] = {s2, s1, s0};
+  cuuint32_t box[4] = {32, static_cast<cuuint32_t>(attn::kBM), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 attn_status run(const attn_shape* s, const void* q, const void* k, const void* v, const void* tq,
                 const void* tk, const void* tv, const int32_t* offsets, const attn_bias* bias,
                 int causal, float sm_scale, void* o, void* to, float* lse, void* stream,
@@ -220,6 +267,11 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
       kp.bias_stride[i] = bias->bias_stride[i];
       kp.mask_stride[i] = bias->mask_stride[i];
     }
+    if (kp.bias != nullptr && !jagged)
+      kp.bias_tma = encode_bias_map(&kp.tm_bias, kp.bias, bias->bias_stride, s->B, s->H, s->M, s->N,
+                                    &kp.bias_bcast_h, &kp.bias_bcast_b)
+                        ? 1
+                        : 0;
   }
   const uint64_t dqk = s->Dqk, dvv = s->Dv;
   bool ok = true;
@@ -288,8 +340,12 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   }
   cudaError_t e = cudaErrorInvalidValue;
   const int key = (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
-  const bool bm = kp.bias != nullptr || kp.mask != nullptr;
-  e = dispatch_attn(key, jvp, bm, kp, grid, cs);
+  // bias through the shared-memory ring when a tensor map describes it,
+  // else per-thread loads; a mask alone also takes the ring mode
+  const int mode = (kp.bias == nullptr && kp.mask == nullptr) ? attn::kNoBias
+                   : (kp.bias != nullptr && kp.bias_tma == 0) ? attn::kBiasGlobal
+                                                               : attn::kBiasRing;
+  e = dispatch_attn(key, jvp, mode, kp, grid, cs);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   g_launches.fetch_add(1);
   return ATTN_OK;

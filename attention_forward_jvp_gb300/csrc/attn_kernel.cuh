@@ -71,6 +71,11 @@ constexpr int ERR_SMEM_ALIGN = 2;
 
 struct KernelParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_tq, tm_tk, tm_tv;
+  // fp32 bias as a 4-D view {key, query row, head, batch}, box 32 x 128
+  // (used when bias_tma is set); a broadcast head / batch dimension has
+  // size 1 and is addressed at coordinate 0.
+  CUtensorMap tm_bias;
+  int bias_tma, bias_bcast_h, bias_bcast_b;
   int B, H, M, N;  // jagged: B = sequences, M = N = max_seq_len
   int jagged, causal;
   int n_mt;        // query tiles per (b, h) or per (sequence, h)
@@ -97,10 +102,24 @@ struct KernelParams {
   int skip_first_load;
 };
 
+// Bias / mask handling of a kernel instantiation.
+//   kNoBias:     neither; every tile's row maximum is local.
+//   kBiasRing:   bias tiles copied by tensor copies into a shared-memory
+//                ring (and / or a boolean mask read per thread); both halves
+//                of a row see every column, so the row maximum is local.
+//   kBiasGlobal: bias read per thread from global memory (layouts a tensor
+//                map cannot describe); the two warps of a row exchange their
+//                partial maxima.
+constexpr int kNoBias = 0, kBiasRing = 1, kBiasGlobal = 2;
+
 // Shared-memory and tensor-memory plan for one instantiation.
-template <int DQK, int DV, bool JVP>
+template <int DQK, int DV, bool JVP, int BMODE>
 struct Plan {
   static constexpr int NQ = JVP ? 2 : 1;   // primal (+ tangent) operands
+  // Bias stage: the fp32 bias of one key tile, two 128-row x 32-key boxes
+  // (one per softmax half), 128-byte swizzled rows.
+  static constexpr int BIAS_BOX = kBM * 32 * 4;
+  static constexpr int BIAS_STAGE = 2 * BIAS_BOX;
   static constexpr int Q_SUB = kBM * 128;  // one 64-column swizzled sub-tile
   static constexpr int K_SUB = kBN * 128;
   static constexpr int V_SUB = kBN * 128;
@@ -116,15 +135,22 @@ struct Plan {
   static constexpr int FIXED = NQ * Q_TILE;
   static constexpr int XCHG_FLOATS = 2 * 2 * kBM;  // [parity][half][row]
   static constexpr int BUDGET = 227 * 1024 - 512 - XCHG_FLOATS * 4;
-  static constexpr int NK = (FIXED + 4 * K_STAGE + 4 * V_STAGE <= BUDGET) ? 4 : 3;
-  static constexpr int NV = (FIXED + NK * K_STAGE + 4 * V_STAGE <= BUDGET)   ? 4
-                            : (FIXED + NK * K_STAGE + 3 * V_STAGE <= BUDGET) ? 3
-                                                                             : 2;
+  // bias stages (kernels with bias / mask only): two when two K and two V
+  // stages still fit beside them, else one
+  static constexpr int NB = BMODE != kBiasRing ? 0 : (FIXED + 2 * BIAS_STAGE + 2 * K_STAGE + 2 * V_STAGE <= BUDGET) ? 2 : 1;
+  static constexpr int RING = BUDGET - NB * BIAS_STAGE;
+  static constexpr int NK = (FIXED + 4 * K_STAGE + 4 * V_STAGE <= RING)   ? 4
+                            : (FIXED + 3 * K_STAGE + 2 * V_STAGE <= RING) ? 3
+                                                                          : 2;
+  static constexpr int NV = (FIXED + NK * K_STAGE + 4 * V_STAGE <= RING)   ? 4
+                            : (FIXED + NK * K_STAGE + 3 * V_STAGE <= RING) ? 3
+                                                                           : 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_TQ = Q_TILE;
   static constexpr int OFF_K = FIXED;
   static constexpr int OFF_V = OFF_K + NK * K_STAGE;
-  static constexpr int OFF_BAR = OFF_V + NV * V_STAGE;
+  static constexpr int OFF_BIAS = OFF_V + NV * V_STAGE;  // 1024-byte aligned (stages are)
+  static constexpr int OFF_BAR = OFF_BIAS + NB * BIAS_STAGE;
   // barriers: q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
   //           s_full[2], p_full[2], mma_drain, pair[4] (the two softmax warps
   //           of a quadrant).  v_empty of tile t's stage completes when the
@@ -135,7 +161,8 @@ struct Plan {
   //           done.
   static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + NK, B_VF = B_KE + NK,
                        B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2,
-                       B_DRAIN = B_PF + 2, B_PAIR = B_DRAIN + 1, NBAR = B_PAIR + 4;
+                       B_DRAIN = B_PF + 2, B_PAIR = B_DRAIN + 1, B_BF = B_PAIR + 4,
+                       B_BE = B_BF + NB, NBAR = B_BE + NB;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int OFF_XCHG = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = OFF_XCHG + XCHG_FLOATS * 4;
@@ -232,6 +259,9 @@ __device__ __forceinline__ int unit_of_round(int rnd) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   return rnd * G + ((rnd & 1) ? (G - 1 - c) : c);
 }
+
+// Key tiles ahead of its use at which a bias box is pulled into L2.
+constexpr int kBiasLead = 4;
 
 struct Waiter {
   volatile int* abort_flag;
@@ -340,6 +370,51 @@ __device__ __forceinline__ void store_chunk(__nv_bfloat16* dst, const uint32_t* 
   }
 }
 
+// Mask bytes of 32 keys from key0 (nonzero = attend), four per word; keys
+// at or past kv_len read as 0.
+__device__ __forceinline__ void load_mask32(const unsigned char* mrow, int key0, int kv_len,
+                                            long long stride, bool row_ok, uint32_t (&mv)[8]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) mv[c] = 0u;
+  if (!row_ok) return;
+  const unsigned char* mp = mrow + static_cast<long long>(key0) * stride;
+  if (stride == 1 && (reinterpret_cast<uintptr_t>(mp) & 15u) == 0 && key0 + 32 <= kv_len) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint4 t4 = __ldg(reinterpret_cast<const uint4*>(mp) + c);
+      mv[4 * c] = t4.x;
+      mv[4 * c + 1] = t4.y;
+      mv[4 * c + 2] = t4.z;
+      mv[4 * c + 3] = t4.w;
+    }
+  } else {
+    for (int c = 0; c < 32; ++c)
+      if (key0 + c < kv_len && __ldg(mp + c * stride) != 0) mv[c >> 2] |= 1u << ((c & 3) * 8);
+  }
+}
+
+// Bit c set when key key_start + c (c < 32) is below kv_len and, for
+// causal attention, at most qi.
+__device__ __forceinline__ uint32_t keep_bits(int key_start, int kv_len, int qi, bool causal) {
+  int n = kv_len - key_start;
+  if (causal) n = min(n, qi - key_start + 1);
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+
+// Bit c set when mask byte c (byte c % 4 of word c / 4) is nonzero: a
+// per-byte compare, then the four 0/1 bytes of a word gathered into four
+// adjacent bits by one multiply (0x01020408 moves byte i's bit 8i to bit
+// 24 + i; no other partial product lands on bits 24..27).
+__device__ __forceinline__ uint32_t mask_bits32(const uint32_t (&mv)[8]) {
+  uint32_t bits = 0;
+#pragma unroll
+  for (int wd = 0; wd < 8; ++wd) {
+    const uint32_t nz = __vcmpne4(mv[wd], 0u) & 0x01010101u;
+    bits |= ((nz * 0x01020408u) >> 24) << (4 * wd);
+  }
+  return bits;
+}
+
 // Row maximum of 32 values, 3-input max tree.
 __device__ __forceinline__ float rowmax32(const float* x) {
   float a[11];
@@ -351,12 +426,14 @@ __device__ __forceinline__ float rowmax32(const float* x) {
   return fmaxf(max3f(b0, b1, b2), b3);
 }
 
-// BM: the launch carries an additive bias and / or a boolean mask.  Without
-// them the row maximum of every tile is taken locally (no exchange between
-// the two warps of a row), and none of the bias / mask code is compiled in.
-template <int DQK, int DV, bool JVP, bool BM>
+// BMODE: kNoBias, kBiasRing or kBiasGlobal (see Plan).  Each mode compiles
+// only its own bias / mask code, which keeps the per-tile loop small.
+template <int DQK, int DV, bool JVP, int BMODE>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KernelParams p) {
-  using P = Plan<DQK, DV, JVP>;
+  using P = Plan<DQK, DV, JVP, BMODE>;
+  constexpr bool BM = BMODE != kNoBias;
+  constexpr bool RING = BMODE == kBiasRing;
+  constexpr bool GLOB = BMODE == kBiasGlobal;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -391,6 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     mbar_init(bar(P::B_DRAIN), 1);
     for (int i = 0; i < 4; ++i) mbar_init(bar(P::B_PAIR + i), 64);
+    for (int i = 0; i < P::NB; ++i) {
+      mbar_init(bar(P::B_BF + i), 1);
+      mbar_init(bar(P::B_BE + i), 8);  // one arrival per softmax warp
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -484,8 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else if (warp == 2) {
     // ---------------------------------------------------- V / tV producer
     // Separate from the K ring so that a K load never waits for a V slot.
+    // With a bias that has a tensor map it also loads each key tile's bias
+    // (two 128 x 32 fp32 boxes) into the bias ring.
     if (lane == 0) {
       uint32_t vfill = 0;
+      const bool bias_ring = P::NB > 0 && p.bias_tma != 0;
       bool ok = true;
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
@@ -505,12 +589,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               tma_load_3d(vdst + P::V_TILE + c * P::V_SUB, &p.tm_tv, bar(P::B_VF + vs), c * 64, r,
                           w.z);
           }
+          if constexpr (P::NB > 0) {
+            if (bias_ring) {
+              // the bias streams from HBM once: its boxes are pulled into L2
+              // kBiasLead tiles ahead of their copy into the ring
+              const int hb = p.bias_bcast_h ? 0 : w.h, bb = p.bias_bcast_b ? 0 : w.b;
+              for (int jj = (j == 0 ? 0 : j + kBiasLead); jj <= j + kBiasLead && jj < w.nt; ++jj) {
+                tma_prefetch_l2_4d(&p.tm_bias, jj * kBN, w.mt * kBM, hb, bb);
+                tma_prefetch_l2_4d(&p.tm_bias, jj * kBN + 32, w.mt * kBM, hb, bb);
+              }
+              const uint32_t bs = vfill % P::NB;
+              ok = wait_bar(bar(P::B_BE + bs), ((vfill / P::NB) & 1u) ^ 1u, W);
+              if (!ok) break;
+              mbar_arrive_expect_tx(bar(P::B_BF + bs), P::BIAS_STAGE);
+              const uint32_t bdst = sbase + P::OFF_BIAS + bs * P::BIAS_STAGE;
+              tma_load_4d(bdst, &p.tm_bias, bar(P::B_BF + bs), j * kBN, w.mt * kBM, hb, bb);
+              tma_load_4d(bdst + P::BIAS_BOX, &p.tm_bias, bar(P::B_BF + bs), j * kBN + 32,
+                          w.mt * kBM, hb, bb);
+            }
+          }
           ++vfill;
         }
       }
       for (uint32_t s = 0; s < P::NV && s < vfill; ++s) {
         const uint32_t nf = (vfill - s + P::NV - 1) / P::NV;
         drain_bar(bar(P::B_VF + s), (nf - 1) & 1u, p.timeout_ns);
+      }
+      if constexpr (P::NB > 0) {
+        if (bias_ring) {
+          for (uint32_t s = 0; s < static_cast<uint32_t>(P::NB) && s < vfill; ++s) {
+            const uint32_t nf = (vfill - s + P::NB - 1) / P::NB;
+            drain_bar(bar(P::B_BF + s), (nf - 1) & 1u, p.timeout_ns);
+          }
+        }
       }
     }
     __syncwarp();
@@ -750,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // Bias rows stream from HBM once: pull this thread's segment of the
         // tile two steps ahead into L2 (the first two tiles at unit start),
         // then load this tile's entries before waiting on S.
-        if (has_bias && row_ok && p.bias_stride[3] == 1) {
+        if (GLOB && has_bias && row_ok && p.bias_stride[3] == 1) {
           const float* bp = brow + half * kHalf;
           if (j == 0) {
             prefetch_l2(bp);
@@ -760,7 +871,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         float bv[kHalf];
         uint32_t mv[kHalf / 4];
-        if (has_bias) {
+        uint32_t mvo[kHalf / 4];  // the partner's columns (local row maximum)
+        if (GLOB && has_bias) {
 #pragma unroll
           for (int c = 0; c < kHalf; ++c) bv[c] = 0.f;
           if (row_ok) {
@@ -782,26 +894,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
         }
         if (has_mask) {
-#pragma unroll
-          for (int c = 0; c < kHalf / 4; ++c) mv[c] = 0u;
-          if (row_ok) {
-            const unsigned char* mp = mrow + static_cast<long long>(key0) * p.mask_stride[3];
-            if (p.mask_stride[3] == 1 && (reinterpret_cast<uintptr_t>(mp) & 15u) == 0 &&
-                key0 + kHalf <= w.kv_len) {
-#pragma unroll
-              for (int c = 0; c < kHalf / 16; ++c) {
-                const uint4 t4 = __ldg(reinterpret_cast<const uint4*>(mp) + c);
-                mv[4 * c] = t4.x;
-                mv[4 * c + 1] = t4.y;
-                mv[4 * c + 2] = t4.z;
-                mv[4 * c + 3] = t4.w;
-              }
-            } else {
-              for (int c = 0; c < kHalf; ++c)
-                if (key0 + c < w.kv_len && __ldg(mp + c * p.mask_stride[3]) != 0)
-                  mv[c >> 2] |= 1u << ((c & 3) * 8);
-            }
-          }
+          load_mask32(mrow, key0, w.kv_len, p.mask_stride[3], row_ok, mv);
+          if (RING) load_mask32(mrow, j * kBN + (half ^ 1) * kHalf, w.kv_len, p.mask_stride[3], row_ok, mvo);
         }
 
         ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
@@ -809,13 +903,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_fence_after();
         // Each warp also reads the partner half's 32 score columns and takes
         // the row maximum over all 64 itself, so the two warps of a quadrant
-        // never wait for each other: unmasked tiles (`fast`) and, without
-        // bias or mask, causal-diagonal and ragged tiles (`local`, the mask
-        // applied to both halves).  With bias or mask the two warps exchange
-        // partial maxima through shared memory instead.
+        // never wait for each other: unmasked tiles (`fast`) and masked tiles
+        // (`local`: causal diagonal, ragged tail, mask, and bias read from
+        // the shared-memory ring), the mask applied to both halves.  Only a
+        // bias read per thread from global memory makes the two warps
+        // exchange partial maxima through shared memory instead.
         const bool diag = p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
         const bool fast = !BM && !diag && (j * kBN + kBN <= w.kv_len);
-        const bool local = !BM && !fast;
+        const bool local = !GLOB && !fast;
         uint32_t sr[kHalf];
         uint32_t so[kHalf];
         uint32_t tr[kHalf];
@@ -846,32 +941,77 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
           for (int c = 0; c < kHalf; ++c) xo[c] = __uint_as_float(so[c]);
           mx = fmaxf(rowmax32(x), rowmax32(xo)) * p.scale_log2;
+        } else if (RING) {
+          // bias from the shared-memory ring (rows 128-byte swizzled: 16-byte
+          // chunk k of row r at chunk k ^ (r mod 8)) for both halves'
+          // columns, so the row maximum needs no exchange
+          sc = 1.f;
+          constexpr int NBR = P::NB > 0 ? P::NB : 1;
+          const int keyo = j * kBN + (half ^ 1) * kHalf;
+          uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
+          uint32_t kmo = keep_bits(keyo, w.kv_len, qi, p.causal);
+          if (has_mask) {
+            km &= mask_bits32(mv);
+            kmo &= mask_bits32(mvo);
+          }
+          if (has_bias) {
+            ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_BF + g % NBR), (g / NBR) & 1u, W));
+            if (!ok) break;
+          }
+          const uint8_t* bbase = smem + P::OFF_BIAS + (g % NBR) * P::BIAS_STAGE + row * 128;
+          float xo[kHalf];
+#pragma unroll
+          for (int k4 = 0; k4 < kHalf / 4; ++k4) {
+            float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), bo4 = b4;
+            if (has_bias) {
+              const int phys = (k4 ^ (row & 7)) * 16;
+              b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
+              bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
+            }
+            const float bo[4] = {bo4.x, bo4.y, bo4.z, bo4.w};
+            const float bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * k4 + e;
+              const float v = fmaf(bw[e], kLog2e, x[c] * p.scale_log2);
+              const float vo = fmaf(bo[e], kLog2e, __uint_as_float(so[c]) * p.scale_log2);
+              x[c] = ((km >> c) & 1u) ? v : -INFINITY;
+              xo[c] = ((kmo >> c) & 1u) ? vo : -INFINITY;
+              if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
+            }
+          }
+          if (has_bias) {
+            // this warp is done with the tile's bias
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(P::B_BE + g % NBR));
+          }
+          mx = fmaxf(rowmax32(x), rowmax32(xo));
         } else {
           sc = 1.f;
-#pragma unroll
-          for (int c = 0; c < kHalf; ++c) {
-            const int kj = key0 + c;
-            bool keep = kj < w.kv_len;
-            if (p.causal) keep = keep && (kj <= qi);
-            if (has_mask) keep = keep && (((mv[c >> 2] >> ((c & 3) * 8)) & 0xffu) != 0u);
-            float v = x[c] * p.scale_log2;
-            if (has_bias) v = fmaf(bv[c], kLog2e, v);
-            x[c] = keep ? v : -INFINITY;
-            if constexpr (JVP) tr[c] = keep ? tr[c] : 0u;
-          }
-          mx = rowmax32(x);
           if constexpr (!BM) {
-            // the partner's columns under the same causal / key-length mask
+            // causal diagonal / ragged tail: both halves under the same mask
             const int keyo = j * kBN + (half ^ 1) * kHalf;
+            const uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
+            const uint32_t kmo = keep_bits(keyo, w.kv_len, qi, p.causal);
             float xo[kHalf];
 #pragma unroll
             for (int c = 0; c < kHalf; ++c) {
-              const int ko = keyo + c;
-              const bool keepo = ko < w.kv_len && (!p.causal || ko <= qi);
-              xo[c] = keepo ? __uint_as_float(so[c]) * p.scale_log2 : -INFINITY;
+              x[c] = ((km >> c) & 1u) ? x[c] * p.scale_log2 : -INFINITY;
+              xo[c] = ((kmo >> c) & 1u) ? __uint_as_float(so[c]) * p.scale_log2 : -INFINITY;
+              if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
             }
-            mx = fmaxf(mx, rowmax32(xo));
+            mx = fmaxf(rowmax32(x), rowmax32(xo));
           } else {
+            uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
+            if (has_mask) km &= mask_bits32(mv);
+#pragma unroll
+            for (int c = 0; c < kHalf; ++c) {
+              float v = x[c] * p.scale_log2;
+              if (has_bias) v = fmaf(bv[c], kLog2e, v);
+              x[c] = ((km >> c) & 1u) ? v : -INFINITY;
+              if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
+            }
+            mx = rowmax32(x);
             // the pair's row maximum over all 64 columns of the tile; the
             // slot alternates per tile, and a writer can only come back to a
             // slot after the rendezvous of the tile in between
@@ -946,8 +1086,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           if (!ok) break;
           tc_fence_after();
           {
+            // (rare: kept as a rolled loop so the tile loop's code stays small)
             const float a = resc ? alpha : 1.f;
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < DVH; c0 += 32) {
               uint32_t v[32];
               tmem_ld_32x32b_x32(tl + P::COL_O + half * DVH + c0, v);
@@ -1075,9 +1216,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, P::TMEM_COLS);
 }
 
-template <int DQK, int DV, bool JVP, bool BM>
+template <int DQK, int DV, bool JVP, int BMODE>
 cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
-  using P = Plan<DQK, DV, JVP>;
+  using P = Plan<DQK, DV, JVP, BMODE>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1087,16 +1228,16 @@ cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
     // computed for; a build that compiled to another count is refused
     // (setmaxnreg.inc would otherwise wait for registers that never free).
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP, BM>);
+    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP, BMODE>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP, BM>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP, BMODE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  attn_fwd_kernel<DQK, DV, JVP, BM><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
+  attn_fwd_kernel<DQK, DV, JVP, BMODE><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
   return cudaGetLastError();
 }
 

@@ -182,6 +182,56 @@ def test_broadcast_bias_strides():
     assert_close(*run_gpu(inp), *oracle_dense(inp), what="broadcast bias")
 
 
+def test_bias_ring_shared_by_heads_causal():
+    # bias [2, 1, 200, 200] shared by all heads, with causal attention: the
+    # bias goes through a tensor map (rows 800 bytes apart) whose head
+    # dimension has size 1
+    w = Workload("bh", B=2, H=3, M=200, N=200, Dqk=128, Dv=128, causal=True)
+    inp = make_inputs(w, seed=11)
+    g = torch.Generator().manual_seed(12)
+    inp["bias"] = torch.randn((2, 1, 200, 200), generator=g)
+    assert_close(*run_gpu(inp), *oracle_dense(inp), what="bias shared by heads, causal")
+
+
+def test_bias_ring_shared_by_batch_with_full_mask():
+    # bias [1, 2, 260, 132] shared by the batch, with a full random mask
+    # [3, 2, 260, 132]; ragged last query and key tiles
+    w = Workload("bb2", B=3, H=2, M=260, N=132, Dqk=64, Dv=128)
+    inp = make_inputs(w, seed=13)
+    g = torch.Generator().manual_seed(14)
+    inp["bias"] = torch.randn((1, 2, 260, 132), generator=g)
+    inp["mask"] = (torch.rand((3, 2, 260, 132), generator=g) < 0.7).to(torch.uint8)
+    assert_close(*run_gpu(inp), *oracle_dense(inp), what="bias shared by batch + mask")
+
+
+def test_mask_without_bias():
+    w = Workload("mo", B=2, H=2, M=190, N=300, Dqk=128, Dv=64)
+    inp = make_inputs(w, seed=15)
+    g = torch.Generator().manual_seed(16)
+    inp["mask"] = (torch.rand((2, 1, 190, 300), generator=g) < 0.5).to(torch.uint8)
+    assert_close(*run_gpu(inp), *oracle_dense(inp), what="mask only")
+
+
+@pytest.mark.parametrize("Dv", [64, 128])
+def test_outputs_16_byte_but_not_32_byte_aligned(Dv):
+    # the epilogue uses 32-byte stores only when both outputs allow them
+    w = Workload("al", B=1, H=2, M=200, N=130, Dqk=64, Dv=Dv)
+    inp = make_inputs(w, seed=17)
+    q, k, v, tq, tk, tv = (dev(inp[n]) for n in ("q", "k", "v", "tq", "tk", "tv"))
+    n = w.B * w.H * w.M * Dv
+    ob = torch.full((n + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tb = torch.full((n + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = ob[8:].view(w.B, w.H, w.M, Dv)
+    to = tb[8:].view(w.B, w.H, w.M, Dv)
+    assert o.data_ptr() % 32 == 16 and to.data_ptr() % 32 == 16
+    lse = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device="cuda")
+    binding.attn_fwd_jvp(q, k, v, tq, tk, tv, sm_scale=inp["sm_scale"], out=(o, to, lse))
+    assert binding.sync_check() == 0
+    assert torch.isnan(ob[:8].float()).all() and torch.isnan(tb[:8].float()).all()
+    assert_close(o.float().cpu().numpy(), to.float().cpu().numpy(), lse.cpu().numpy(),
+                 *oracle_dense(inp), what=f"16-byte aligned outputs Dv={Dv}")
+
+
 # -------------------------------------------------------- kernel invariants
 @pytest.mark.parametrize("name", ["tiny", "edge_causal", "edge_bias"])
 def test_forward_only_matches_jvp_primal_bitwise(name):
