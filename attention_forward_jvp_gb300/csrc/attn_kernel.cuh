@@ -132,9 +132,17 @@ struct Plan {
   // V stage: [V chunks | tV chunks], uniform 64-column stride, so that
   // [V | tV] is one N = 2 Dv operand.
   static constexpr int V_STAGE = NQ * V_TILE;
-  static constexpr int FIXED = NQ * Q_TILE;
-  static constexpr int XCHG_FLOATS = 2 * 2 * kBM;  // [parity][half][row]
+  static constexpr int QSET = NQ * Q_TILE;  // one Q (+ tQ) buffer
+  // exchange slots between the two softmax warps of a row:
+  // [parity][half][row] plus one [row] array (the epilogue's third value)
+  static constexpr int XCHG_FLOATS = 2 * 2 * kBM + kBM;
   static constexpr int BUDGET = 227 * 1024 - 512 - XCHG_FLOATS * 4;
+  // Q buffers: two (the next unit's Q loads while the current unit runs and
+  // score MMAs flow across unit boundaries) when they fit beside three K and
+  // two V stages, else one.  Kernels with a bias ring keep one.
+  static constexpr int NQB =
+      (BMODE != kBiasRing && 2 * QSET + 3 * K_STAGE + 2 * V_STAGE <= BUDGET) ? 2 : 1;
+  static constexpr int FIXED = NQB * QSET;
   // bias stages (kernels with bias / mask only): two when two K and two V
   // stages still fit beside them, else one
   static constexpr int NB = BMODE != kBiasRing ? 0 : (FIXED + 2 * BIAS_STAGE + 2 * K_STAGE + 2 * V_STAGE <= BUDGET) ? 2 : 1;
@@ -145,8 +153,8 @@ struct Plan {
   static constexpr int NV = (FIXED + NK * K_STAGE + 4 * V_STAGE <= RING)   ? 4
                             : (FIXED + NK * K_STAGE + 3 * V_STAGE <= RING) ? 3
                                                                            : 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_TQ = Q_TILE;
+  static constexpr int OFF_Q = 0;       // buffer b at OFF_Q + b * QSET
+  static constexpr int OFF_TQ = Q_TILE;  // buffer b at OFF_TQ + b * QSET
   static constexpr int OFF_K = FIXED;
   static constexpr int OFF_V = OFF_K + NK * K_STAGE;
   static constexpr int OFF_BIAS = OFF_V + NV * V_STAGE;  // 1024-byte aligned (stages are)
@@ -159,22 +167,28 @@ struct Plan {
   //           k_empty and q_empty are arrived on by the release warp once the
   //           score MMAs that read the stage (Q: of the unit's last tile) are
   //           done.
-  static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + NK, B_VF = B_KE + NK,
-                       B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2,
+  //           With two O buffers, o_empty[b] completes when the softmax
+  //           warps have read buffer b in a unit's epilogue.
+  static constexpr int SBUF = 2 * kBN;
+  static constexpr int COL_O = 2 * SBUF;
+  static constexpr int OBUF = (JVP ? 2 : 1) * DV;  // columns of one [O | tO] buffer
+  // O buffers: two (a unit's epilogue runs after the next unit's first tile,
+  // whose output MMAs write the other buffer) with two Q buffers, when the
+  // tensor memory holds them.
+  static constexpr int NOB = (NQB == 2 && COL_O + 2 * OBUF <= 512) ? 2 : 1;
+  static constexpr int B_QF = 0, B_QE = B_QF + NQB, B_KF = B_QE + NQB, B_KE = B_KF + NK,
+                       B_VF = B_KE + NK, B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2,
                        B_DRAIN = B_PF + 2, B_PAIR = B_DRAIN + 1, B_BF = B_PAIR + 4,
-                       B_BE = B_BF + NB, NBAR = B_BE + NB;
+                       B_BE = B_BF + NB, B_OE = B_BE + NB, NBAR = B_OE + NOB;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int OFF_XCHG = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = OFF_XCHG + XCHG_FLOATS * 4;
   // TMEM columns: buffer b holds S at [b*SBUF, b*SBUF + BN) and tS (or, in
-  // the forward-only kernel, scratch) in the next BN columns; then O_acc and
-  // tO_acc side by side.  Softmax half h writes its bf16 P (16 columns) and
+  // the forward-only kernel, scratch) in the next BN columns; then NOB
+  // buffers of O_acc and tO_acc side by side (buffer b at COL_O + b * OBUF).  Softmax half h writes its bf16 P (16 columns) and
   // H (16 columns) over its own 32 tS columns, which no other thread reads,
   // so the S columns stay intact for both halves' row maxima.
-  static constexpr int SBUF = 2 * kBN;
-  static constexpr int COL_O = 2 * SBUF;
-  static constexpr int COL_TO = COL_O + DV;
-  static constexpr int COLS_USED = COL_O + (JVP ? 2 : 1) * DV;
+  static constexpr int COLS_USED = COL_O + NOB * OBUF;
   static constexpr int TMEM_COLS = COLS_USED <= 256 ? 256 : 512;
   // Requested dynamic shared memory: never less than half an SM's, so one
   // CTA (and its TMEM allocation) owns an SM.
@@ -452,8 +466,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   float* xchg = reinterpret_cast<float*>(smem + P::OFF_XCHG);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(P::B_QF), 1);
-    mbar_init(bar(P::B_QE), 1);
+    for (int i = 0; i < P::NQB; ++i) {
+      mbar_init(bar(P::B_QF + i), 1);
+      mbar_init(bar(P::B_QE + i), 1);
+    }
+    for (int i = 0; i < P::NOB; ++i) mbar_init(bar(P::B_OE + i), 8);  // one arrival per softmax warp
     for (int i = 0; i < P::NK; ++i) {
       mbar_init(bar(P::B_KF + i), 1);
       mbar_init(bar(P::B_KE + i), 1);
@@ -512,28 +529,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t qfill = 0, kfill = 0;
-      bool last_q_loaded = false;
-      bool skip = p.skip_first_load != 0;
+      const bool first_q_loaded = p.skip_first_load == 0;
+      bool skip = !first_q_loaded;
       bool ok = true;
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
         const Unit w = decode_unit(p, u, list);
         if (w.nt == 0) continue;
-        ok = wait_bar(bar(P::B_QE), (qfill & 1u) ^ 1u, W);
+        const uint32_t qb = qfill % P::NQB;
+        ok = wait_bar(bar(P::B_QE + qb), ((qfill / P::NQB) & 1u) ^ 1u, W);
         if (!ok) break;
         if (!skip) {
-          mbar_arrive_expect_tx(bar(P::B_QF), P::NQ * P::Q_TILE);
+          mbar_arrive_expect_tx(bar(P::B_QF + qb), P::QSET);
           const int r = w.row0 + w.mt * kBM;
+          const uint32_t qdst = sbase + qb * P::QSET;
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c) {
-            tma_load_3d(sbase + P::OFF_Q + c * P::Q_SUB, &p.tm_q, bar(P::B_QF), c * 64, r, w.z);
+            tma_load_3d(qdst + P::OFF_Q + c * P::Q_SUB, &p.tm_q, bar(P::B_QF + qb), c * 64, r, w.z);
             if (JVP)
-              tma_load_3d(sbase + P::OFF_TQ + c * P::Q_SUB, &p.tm_tq, bar(P::B_QF), c * 64, r, w.z);
+              tma_load_3d(qdst + P::OFF_TQ + c * P::Q_SUB, &p.tm_tq, bar(P::B_QF + qb), c * 64, r,
+                          w.z);
           }
-          last_q_loaded = true;
-        } else {
-          last_q_loaded = false;
         }
         skip = false;
         ++qfill;
@@ -559,7 +576,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint32_t nf = (kfill - s + P::NK - 1) / P::NK;
         drain_bar(bar(P::B_KF + s), (nf - 1) & 1u, p.timeout_ns);
       }
-      if (qfill > 0 && last_q_loaded) drain_bar(bar(P::B_QF), (qfill - 1) & 1u, p.timeout_ns);
+      // (a skipped first load leaves its buffer's barrier incomplete)
+      for (uint32_t s = 0; s < static_cast<uint32_t>(P::NQB) && s < qfill; ++s) {
+        const uint32_t f = qfill - 1 - s;  // the last fill of buffer f % NQB
+        if (f == 0 && !first_q_loaded) continue;
+        drain_bar(bar(P::B_QF + f % P::NQB), (f / P::NQB) & 1u, p.timeout_ns);
+      }
     }
     __syncwarp();
   } else if (warp == 2) {
@@ -633,22 +655,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // tile g -- and hence the score MMAs of tile g+2, the next phase of the
     // same s_full barrier -- cannot be issued before it has seen s_full of
     // tile g: its parity waits are unambiguous.
-    uint32_t g = 0;
+    uint32_t g = 0, qu = 0;  // tiles, units with keys
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_of_round(rnd);
       if (u >= num_units) break;
       const Unit w = decode_unit(p, u, list);
+      if (w.nt == 0) continue;
       for (int j = 0; j < w.nt; ++j, ++g) {
         ok = __all_sync(0xffffffffu, wait_bar_sleep(bar(P::B_SF + (g & 1u)), (g >> 1) & 1u, W));
         if (!ok) break;
         if (lane == 0) {
           mbar_arrive(bar(P::B_KE + g % P::NK));
-          if (j == w.nt - 1) mbar_arrive(bar(P::B_QE));
+          if (j == w.nt - 1) mbar_arrive(bar(P::B_QE + qu % P::NQB));
           mbar_arrive(bar(P::B_PF + (g & 1u)));
         }
         __syncwarp();
       }
+      ++qu;
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -665,7 +689,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     constexpr uint32_t idesc_t = idesc_bf16(kBM, kBN, false);                   // tQ K^T
     constexpr uint32_t idesc_o = idesc_bf16(kBM, P::NQ * DV, true);             // [O | tO]
     constexpr uint32_t idesc_h = idesc_bf16(kBM, DV, true);                     // H V
-    const uint32_t sQ = sbase + P::OFF_Q, sTQ = sbase + P::OFF_TQ;
     auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, wait_bar(b, parity, W));
     };
@@ -692,8 +715,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
     // [S | Q tK^T] = Q [K ; tK]^T, tS += tQ K^T for tile t; `mid` runs after
     // the first half of the first chain.
-    auto issue_s = [&](uint32_t t, auto&& mid) -> bool {
+    auto issue_s = [&](uint32_t t, uint32_t qb, auto&& mid) -> bool {
       if (!wait_k(t)) return false;
+      const uint32_t sQ = sbase + qb * P::QSET + P::OFF_Q, sTQ = sbase + qb * P::QSET + P::OFF_TQ;
       const uint32_t dS = tmem + (t & 1u) * P::SBUF;
       const uint32_t sK = sbase + P::OFF_K + (t % P::NK) * P::K_STAGE;
 #pragma unroll
@@ -720,12 +744,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       return true;
     };
 
-    // [O | tO] += P [V | tV] ; tO += H V for tile t, once its P and H are
-    // written; `mid` runs after the first half of the first chain.
-    auto issue_pv = [&](uint32_t t, bool first, auto&& mid) -> bool {
+    // [O | tO] += P [V | tV] ; tO += H V for tile t of unit un (O buffer
+    // un % NOB), once its P and H are written; `mid` runs after the first
+    // half of the first chain.  The first output MMAs of a unit overwrite
+    // the O buffer: with two buffers they wait until the epilogue of unit
+    // un - 2 has read it.
+    auto issue_pv = [&](uint32_t t, bool first, uint32_t un, auto&& mid) -> bool {
       const uint32_t sb = t & 1u;
       if (!wait_v(t) || !wait_all(bar(P::B_PF + sb), (t >> 1) & 1u)) return false;
+      if (P::NOB == 2 && first && !wait_all(bar(P::B_OE + un % P::NOB), ((un / P::NOB) & 1u) ^ 1u))
+        return false;
       tc_fence_after();
+      const uint32_t colo = P::COL_O + (un % P::NOB) * P::OBUF;
       const uint32_t sV = sbase + P::OFF_V + (t % P::NV) * P::V_STAGE;
       // keys [16 kk, 16 kk + 16): P at column base + 32 (kk / 2) + 8 (kk % 2),
       // H 16 columns further (the layout the softmax halves write)
@@ -734,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int kk = 0; kk < kBN / 16; ++kk) {
         const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
         if (leader)
-          mma_ts(tmem + P::COL_O, aP + 32 * (kk >> 1) + 8 * (kk & 1), dv, idesc_o,
+          mma_ts(tmem + colo, aP + 32 * (kk >> 1) + 8 * (kk & 1), dv, idesc_o,
                  (first && kk == 0) ? 0u : 1u);
         __syncwarp();
         if (kk == kBN / 32 - 1) mid();
@@ -743,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
-          if (leader) mma_ts(tmem + P::COL_TO, aP + 32 * (kk >> 1) + 16 + 8 * (kk & 1), dv, idesc_h, 1u);
+          if (leader) mma_ts(tmem + colo + DV, aP + 32 * (kk >> 1) + 16 + 8 * (kk & 1), dv, idesc_h, 1u);
           __syncwarp();
         }
       }
@@ -752,36 +782,71 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       return true;
     };
 
-    // Issue order per unit: S(t0), S(t0+1), PV(t0), S(t0+2), PV(t0+1), ...,
-    // PV(last).  The K tile of S(t+1) is polled inside the batch before it
-    // (S(t0) for t0+1, else PV(t-1)); the V tile of PV(t) inside S(t+1)
-    // (S(last) for the unit's last tile).
-    uint32_t quse = 0, g = 0;  // g: global tile counter (same in every role)
+    uint32_t quse = 0, g = 0;  // units with keys; g: global tile counter (same in every role)
     bool ok = true;
-    for (int rnd = 0; ok; ++rnd) {
-      const int u = unit_of_round(rnd);
-      if (u >= num_units) break;
-      const Unit w = decode_unit(p, u, list);
-      if (w.nt == 0) continue;
-      ok = wait_all(bar(P::B_QF), quse & 1u);
-      if (!ok) break;
-      for (int j = 0; j < w.nt; ++j, ++g) {
-        ok = issue_s(g, [&]() {
-          if (j > 0) poll_v(g - 1);
-          if (j == w.nt - 1) poll_v(g);
-          else if (j == 0) poll_k(g + 1);
-        });
+    if constexpr (P::NQB == 1) {
+      // Issue order per unit: S(t0), S(t0+1), PV(t0), S(t0+2), PV(t0+1), ...,
+      // PV(last).  The K tile of S(t+1) is polled inside the batch before it
+      // (S(t0) for t0+1, else PV(t-1)); the V tile of PV(t) inside S(t+1)
+      // (S(last) for the unit's last tile).
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_of_round(rnd);
+        if (u >= num_units) break;
+        const Unit w = decode_unit(p, u, list);
+        if (w.nt == 0) continue;
+        ok = wait_all(bar(P::B_QF), quse & 1u);
         if (!ok) break;
-        if (j > 0) {
-          ok = issue_pv(g - 1, j == 1, [&]() {
-            if (j + 1 < w.nt) poll_k(g + 1);
+        for (int j = 0; j < w.nt; ++j, ++g) {
+          ok = issue_s(g, 0, [&]() {
+            if (j > 0) poll_v(g - 1);
+            if (j == w.nt - 1) poll_v(g);
+            else if (j == 0) poll_k(g + 1);
           });
           if (!ok) break;
+          if (j > 0) {
+            ok = issue_pv(g - 1, j == 1, quse, [&]() {
+              if (j + 1 < w.nt) poll_k(g + 1);
+            });
+            if (!ok) break;
+          }
         }
+        if (!ok) break;
+        ok = issue_pv(g - 1, w.nt == 1, quse, []() {});
+        ++quse;
       }
-      if (!ok) break;
-      ok = issue_pv(g - 1, w.nt == 1, []() {});
-      ++quse;
+    } else {
+      // Two Q buffers: the tiles of consecutive units form one stream,
+      // S(t+1) issued before PV(t) also when t ends a unit.  The pending
+      // output batch (tile pt of unit pu, first tile of its unit: pfirst)
+      // is issued after the next score batch; polls as above.
+      bool pend = false, pfirst = false;
+      uint32_t pt = 0, pu = 0;
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_of_round(rnd);
+        if (u >= num_units) break;
+        const Unit w = decode_unit(p, u, list);
+        if (w.nt == 0) continue;
+        const uint32_t qb = quse % P::NQB;
+        ok = wait_all(bar(P::B_QF + qb), (quse / P::NQB) & 1u);
+        if (!ok) break;
+        for (int j = 0; j < w.nt; ++j, ++g) {
+          ok = issue_s(g, qb, [&]() {
+            if (pend) poll_v(pt);
+          });
+          if (!ok) break;
+          if (pend) {
+            ok = issue_pv(pt, pfirst, pu, [&]() { poll_k(g + 1); });
+            if (!ok) break;
+          }
+          pend = true;
+          pt = g;
+          pfirst = j == 0;
+          pu = quse;
+        }
+        if (!ok) break;
+        ++quse;
+      }
+      if (ok && pend) ok = issue_pv(pt, pfirst, pu, []() {});
     }
     // Teardown: all MMAs issued by the leader complete before TMEM is freed.
     if (leader) {
@@ -817,6 +882,106 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     constexpr int DVH = DV / 2;  // output columns per softmax thread
     const uint64_t scale2 = f2_make(p.sm_scale, p.sm_scale);
     const bool out32 = ((reinterpret_cast<uintptr_t>(p.o) | (JVP ? reinterpret_cast<uintptr_t>(p.to) : 0)) & 31u) == 0;
+    // One unit's row state, kept until its epilogue runs.
+    struct Epi {
+      int mt, q_len;
+      long long out0;
+      float m_run;
+      uint64_t l2, lt2, r2;
+      uint32_t g_end;  // one past the unit's last tile
+      uint32_t un;     // unit index among units with keys (O buffer un % NOB)
+    };
+    float* my_xl = xchg + 4 * kBM + row;  // the epilogue's third value (l of half 1)
+    // Normalise and store one unit's O, tO and LSE rows.
+    auto epilogue = [&](const Epi& e) -> bool {
+      const int qi = e.mt * kBM + row;
+      const bool row_ok = qi < e.q_len;
+      // combine the two halves' partial sums through shared memory (this
+      // overlaps the output MMAs of the unit's last tile): both write lt and
+      // r, the second half also its l, which only the first half needs
+      float l_a, l_b, lt_a, lt_b, r_a, r_b;
+      f2_split(e.l2, l_a, l_b);
+      f2_split(e.lt2, lt_a, lt_b);
+      f2_split(e.r2, r_a, r_b);
+      float l_sum = l_a + l_b, lt_sum = lt_a + lt_b, r_sum = r_a + r_b;
+      if constexpr (GLOB) {
+        if (!pair_sync()) return false;  // both halves are done with the max slots
+      }
+      *my_x0 = lt_sum;
+      *my_x1 = r_sum;
+      if (half == 1) *my_xl = l_sum;
+      if (!pair_sync()) return false;
+      lt_sum += *other_x0;
+      r_sum += *other_x1;
+      if (half == 0) l_sum += *my_xl;
+      if (!pair_sync()) return false;  // slots free for the next use
+      // every MMA of the unit is done once the output MMAs of its last tile
+      // are; the phase after that one needs a P that this thread has not
+      // written yet (at most the next unit's first tile is done), so the
+      // parity wait is unambiguous
+      const uint32_t gl = e.g_end - 1;
+      if (!__all_sync(0xffffffffu, wait_bar(bar(P::B_VE + gl % P::NV), (gl / P::NV) & 1u, W))) return false;
+      tc_fence_after();
+
+      // O = O_acc / lt, tO = (tO_acc - r O) / lt as packed bf16 pairs, this
+      // thread's DVH columns of its row
+      const uint32_t colo = P::COL_O + (e.un % P::NOB) * P::OBUF;
+      // (both halves hold the full lt; only the first half has the full l.
+      // lt > 0 exactly when the row has a valid key: its largest weight is
+      // at least 1 because the reference max trails the row max by < 8)
+      const bool empty = !(lt_sum > 0.f);
+      const float inv_l = empty ? 0.f : 1.f / lt_sum;
+      constexpr int NW = DVH / 2;  // packed words per half row
+      constexpr int CW = NW / 4;   // words per chunk (four chunks per half row)
+      uint32_t po[NW], pt[NW];
+#pragma unroll
+      for (int c0 = 0; c0 < DVH; c0 += 32) {
+        uint32_t ov[32];
+        uint32_t tv[32];
+        tmem_ld_32x32b_x32(tl + colo + half * DVH + c0, ov);
+        if constexpr (JVP) tmem_ld_32x32b_x32(tl + colo + DV + half * DVH + c0, tv);
+        tmem_wait_ld_regs(ov);
+        if constexpr (JVP) tmem_regs_ready(tv);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float o0 = __uint_as_float(ov[i]) * inv_l;
+          const float o1 = __uint_as_float(ov[i + 1]) * inv_l;
+          po[c0 / 2 + i / 2] = pack_bf16x2(o0, o1);
+          if constexpr (JVP) {
+            const float t0 = (__uint_as_float(tv[i]) - r_sum * o0) * inv_l;
+            const float t1 = (__uint_as_float(tv[i + 1]) - r_sum * o1) * inv_l;
+            pt[c0 / 2 + i / 2] = pack_bf16x2(t0, t1);
+          }
+        }
+      }
+      if constexpr (P::NOB == 2) {
+        // this warp has read the O buffer: the unit after next may reuse it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(P::B_OE + e.un % P::NOB));
+      }
+      if (row_ok && half == 0)
+        p.lse[e.out0 + qi] = empty ? -INFINITY : (e.m_run + __log2f(l_sum)) * kLn2;
+      // Rows are stored a quad of lanes at a time: after the transpose lane q
+      // of a quad holds chunk q of the quad's four rows, so each store
+      // instruction writes eight whole row segments (contiguous per quad).
+      const int q = lane & 3;
+      quad_transpose<CW>(po, q);
+      if constexpr (JVP) quad_transpose<CW>(pt, q);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int qk = e.mt * kBM + quad * 32 + (lane & ~3) + k;  // row of slot k
+        if (qk < e.q_len) {
+          const long long off = (e.out0 + qk) * DV + half * DVH + q * 2 * CW;
+          store_chunk<CW>(p.o + off, po + k * CW, out32);
+          if constexpr (JVP) store_chunk<CW>(p.to + off, pt + k * CW, out32);
+        }
+      }
+      return true;
+    };
+    uint32_t un = 0;         // units with keys seen so far
+    Epi pend{};              // with two O buffers: the unit whose epilogue is due
+    bool has_pend = false;
     uint32_t g = 0;           // global key-tile counter (same in every role)
     uint32_t gen = 0;         // masked tiles seen (slot parity of the max exchange)
     bool ok = true;
@@ -855,6 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // normalised by the weights actually used.  Pairs of fp32 lanes.
       float m_run = -INFINITY;
       uint64_t l2 = 0, lt2 = 0, r2 = 0;
+      const uint32_t colo_cur = P::COL_O + (un % P::NOB) * P::OBUF;  // this unit's O buffer
       for (int j = 0; j < w.nt; ++j, ++g) {
         const uint32_t sb = g & 1u;
         const int key0 = j * kBN + half * kHalf;  // first key of this thread's columns
@@ -1091,17 +1257,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll 1
             for (int c0 = 0; c0 < DVH; c0 += 32) {
               uint32_t v[32];
-              tmem_ld_32x32b_x32(tl + P::COL_O + half * DVH + c0, v);
+              tmem_ld_32x32b_x32(tl + colo_cur + half * DVH + c0, v);
               tmem_wait_ld_regs(v);
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-              tmem_st_32x32b_x32(tl + P::COL_O + half * DVH + c0, v);
+              tmem_st_32x32b_x32(tl + colo_cur + half * DVH + c0, v);
               if constexpr (JVP) {
-                tmem_ld_32x32b_x32(tl + P::COL_TO + half * DVH + c0, v);
+                tmem_ld_32x32b_x32(tl + colo_cur + DV + half * DVH + c0, v);
                 tmem_wait_ld_regs(v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-                tmem_st_32x32b_x32(tl + P::COL_TO + half * DVH + c0, v);
+                tmem_st_32x32b_x32(tl + colo_cur + DV + half * DVH + c0, v);
               }
             }
           }
@@ -1110,84 +1276,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(P::B_PF + sb));
+        if (P::NOB == 2 && j == 0 && has_pend) {
+          // the previous unit's epilogue, now that this unit's first output
+          // MMAs can run
+          has_pend = false;
+          ok = epilogue(pend);
+          if (!ok) break;
+        }
       }
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      // combine the two halves' partial sums through shared memory (this
-      // overlaps the output MMAs of the unit's last tile)
-      float l_a, l_b, lt_a, lt_b, r_a, r_b;
-      f2_split(l2, l_a, l_b);
-      f2_split(lt2, lt_a, lt_b);
-      f2_split(r2, r_a, r_b);
-      float l_sum = l_a + l_b, lt_sum = lt_a + lt_b, r_sum = r_a + r_b;
-      ok = pair_sync();  // both halves are done with the max slots
-      if (!ok) break;
-      *my_x0 = lt_sum;
-      *my_x1 = r_sum;
-      ok = pair_sync();
-      if (!ok) break;
-      lt_sum += *other_x0;
-      r_sum += *other_x1;
-      ok = pair_sync();
-      if (!ok) break;
-      *my_x0 = l_sum;
-      ok = pair_sync();
-      if (!ok) break;
-      l_sum += *other_x0;
-      ok = pair_sync();  // slots free for the next unit
-      if (!ok) break;
-      // every MMA of the unit is done once the output MMAs of its last tile
-      // (g - 1) are (same unambiguous parity argument as above)
-      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + (g - 1) % P::NV), ((g - 1) / P::NV) & 1u, W));
-      if (!ok) break;
-      tc_fence_after();
-
-      // O = O_acc / lt, tO = (tO_acc - r O) / lt as packed bf16 pairs, this
-      // thread's DVH columns of its row
-      const bool empty = !(l_sum > 0.f);
-      const float inv_l = empty ? 0.f : 1.f / lt_sum;
-      constexpr int NW = DVH / 2;  // packed words per half row
-      constexpr int CW = NW / 4;   // words per chunk (four chunks per half row)
-      uint32_t po[NW], pt[NW];
-#pragma unroll
-      for (int c0 = 0; c0 < DVH; c0 += 32) {
-        uint32_t ov[32];
-        uint32_t tv[32];
-        tmem_ld_32x32b_x32(tl + P::COL_O + half * DVH + c0, ov);
-        if constexpr (JVP) tmem_ld_32x32b_x32(tl + P::COL_TO + half * DVH + c0, tv);
-        tmem_wait_ld_regs(ov);
-        if constexpr (JVP) tmem_regs_ready(tv);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float o0 = __uint_as_float(ov[i]) * inv_l;
-          const float o1 = __uint_as_float(ov[i + 1]) * inv_l;
-          po[c0 / 2 + i / 2] = pack_bf16x2(o0, o1);
-          if constexpr (JVP) {
-            const float t0 = (__uint_as_float(tv[i]) - r_sum * o0) * inv_l;
-            const float t1 = (__uint_as_float(tv[i + 1]) - r_sum * o1) * inv_l;
-            pt[c0 / 2 + i / 2] = pack_bf16x2(t0, t1);
-          }
-        }
-      }
-      if (row_ok && half == 0)
-        p.lse[w.out0 + qi] = empty ? -INFINITY : (m_run + __log2f(l_sum)) * kLn2;
-      // Rows are stored a quad of lanes at a time: after the transpose lane q
-      // of a quad holds chunk q of the quad's four rows, so each store
-      // instruction writes eight whole row segments (contiguous per quad).
-      const int q = lane & 3;
-      quad_transpose<CW>(po, q);
-      if constexpr (JVP) quad_transpose<CW>(pt, q);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int qk = w.mt * kBM + quad * 32 + (lane & ~3) + k;  // row of slot k
-        if (qk < w.q_len) {
-          const long long off = (w.out0 + qk) * DV + half * DVH + q * 2 * CW;
-          store_chunk<CW>(p.o + off, po + k * CW, out32);
-          if constexpr (JVP) store_chunk<CW>(p.to + off, pt + k * CW, out32);
-        }
+      const Epi cur{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g, un};
+      ++un;
+      if constexpr (P::NOB == 2) {
+        // runs after the next unit's first tile
+        pend = cur;
+        has_pend = true;
+      } else {
+        ok = epilogue(cur);
+        if (!ok) break;
       }
     }
+    if (ok && has_pend) ok = epilogue(pend);
 
     // Jagged rows past max_seq_len inside their sequence: empty rows.
     if (ok && p.jagged) {
