@@ -203,8 +203,8 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   if (s == nullptr) return ATTN_ERR_INVALID_ARG;
   const bool jagged = offsets != nullptr;
   if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0) return ATTN_ERR_INVALID_ARG;
-  if ((s->Dqk != 64 && s->Dqk != 128) || (s->Dv != 64 && s->Dv != 128))
-    return ATTN_ERR_UNSUPPORTED;
+  auto dim_ok = [](int d) { return d == 16 || d == 32 || d == 64 || d == 128; };
+  if (!dim_ok(s->Dqk) || !dim_ok(s->Dv)) return ATTN_ERR_UNSUPPORTED;
   if (!std::isnan(sm_scale) && !(sm_scale > 0.f && std::isfinite(sm_scale)))
     return ATTN_ERR_INVALID_ARG;
   const bool has_bias = bias != nullptr && (bias->bias != nullptr || bias->mask != nullptr);
@@ -257,6 +257,7 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   kp.o = static_cast<__nv_bfloat16*>(o);
   kp.to = static_cast<__nv_bfloat16*>(to);
   kp.lse = lse;
+  kp.dv_out = s->Dv;
   kp.err = ds->scratch;
   kp.timeout_ns = g_timeout_ns.load();
   kp.skip_first_load = g_skip_first_load.load();
@@ -339,6 +340,8 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
     kp.unit_count = lbuf;
   }
   cudaError_t e = cudaErrorInvalidValue;
+  // head dims 16 and 32 run the 64-wide kernels: the tensor maps keep the
+  // true dims and their 64-column boxes read zeros past them
   const int key = (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
   // bias through the shared-memory ring when a tensor map describes it,
   // else per-thread loads; a mask alone also takes the ring mode

@@ -97,6 +97,10 @@ struct KernelParams {
   float* lse;
   long long T;
   int max_seq_len;
+  // output head dim (row stride of o / to): DV, or 16 / 32 when the kernel
+  // runs a smaller head dim zero-padded to DV = 64 (columns past dv_out are
+  // computed as zeros and not stored)
+  int dv_out;
   int* err;
   unsigned long long timeout_ns;
   int skip_first_load;
@@ -330,7 +334,8 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// n32 packed bf16x2 words to global memory with 16-byte stores.
+// n32 packed bf16x2 words (a multiple of 4) to global memory with 16-byte
+// stores.
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* packed, int n32) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -971,8 +976,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int qk = e.mt * kBM + quad * 32 + (lane & ~3) + k;  // row of slot k
-        if (qk < e.q_len) {
-          const long long off = (e.out0 + qk) * DV + half * DVH + q * 2 * CW;
+        const int col = half * DVH + q * 2 * CW;                   // first column of the chunk
+        if (qk < e.q_len && col < p.dv_out) {
+          const long long off = (e.out0 + qk) * p.dv_out + col;
           store_chunk<CW>(p.o + off, po + k * CW, out32);
           if constexpr (JVP) store_chunk<CW>(p.to + off, pt + k * CW, out32);
         }
@@ -992,17 +998,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!w.active) continue;
       const int qi = w.mt * kBM + row;
       const bool row_ok = qi < w.q_len;
-      __nv_bfloat16* orow = p.o + (w.out0 + qi) * DV + half * DVH;
-      __nv_bfloat16* torow = JVP ? p.to + (w.out0 + qi) * DV + half * DVH : nullptr;
       if (w.nt == 0) {  // no keys at all: empty rows
-        if (row_ok) {
+        // this half's output columns: [half * DVH, min((half + 1) * DVH, dv_out))
+        const int ncol = min(DVH, p.dv_out - half * DVH);
+        if (row_ok && ncol > 0) {
+          __nv_bfloat16* orow = p.o + (w.out0 + qi) * p.dv_out + half * DVH;
+          __nv_bfloat16* torow = JVP ? p.to + (w.out0 + qi) * p.dv_out + half * DVH : nullptr;
           uint32_t z[DVH / 2];
 #pragma unroll
           for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
-          store_row_bf16(orow, z, DVH / 2);
-          if (JVP) store_row_bf16(torow, z, DVH / 2);
-          if (half == 0) p.lse[w.out0 + qi] = -INFINITY;
+          store_row_bf16(orow, z, ncol / 2);
+          if (JVP) store_row_bf16(torow, z, ncol / 2);
         }
+        if (row_ok && half == 0) p.lse[w.out0 + qi] = -INFINITY;
         continue;
       }
       const float* brow = nullptr;
@@ -1312,8 +1320,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             uint32_t z[DV / 2];
 #pragma unroll
             for (int i = 0; i < DV / 2; ++i) z[i] = 0u;
-            store_row_bf16(p.o + o_row * DV, z, DV / 2);
-            if (JVP) store_row_bf16(p.to + o_row * DV, z, DV / 2);
+            store_row_bf16(p.o + o_row * p.dv_out, z, p.dv_out / 2);
+            if (JVP) store_row_bf16(p.to + o_row * p.dv_out, z, p.dv_out / 2);
             p.lse[o_row] = -INFINITY;
           }
         }

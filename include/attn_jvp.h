@@ -52,8 +52,9 @@
  *     launch nothing.  A device-side failure (a pipeline wait that ran out
  *     of time) is recorded in a per-device error word and reported by the
  *     next attn_sync_check on that device.
- *   - Supported head dims: Dqk, Dv in {64, 128}; otherwise
- *     ATTN_ERR_UNSUPPORTED.
+ *   - Supported head dims: Dqk, Dv in {16, 32, 64, 128} (16 and 32 run
+ *     zero-padded to 64 inside the kernel); otherwise ATTN_ERR_UNSUPPORTED.
+ *     Rows of every tensor are D elements, contiguous.
  *   - The library allocates, on first use, one small per-device scratch
  *     buffer (error word) and, for jagged calls, one 1 MB work-list buffer
  *     per (device, stream); it keeps them until the process exits.  A
@@ -72,7 +73,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, causal with M != N (dense) */
-  ATTN_ERR_UNSUPPORTED = 2,   /* head dim outside {64, 128} */
+  ATTN_ERR_UNSUPPORTED = 2,   /* head dim outside {16, 32, 64, 128} */
   ATTN_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
   ATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (no GPU, launch error) */
   ATTN_ERR_TIMEOUT = 5        /* a device pipeline wait ran out of time; outputs undefined */

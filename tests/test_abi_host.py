@@ -63,9 +63,10 @@ def test_rejects_null_shape(L):
 
 
 def test_rejects_unsupported_head_dims(L):
-    assert _call(L, _shape(Dqk=32)) == 2
+    assert _call(L, _shape(Dqk=8)) == 2
     assert _call(L, _shape(Dv=256)) == 2
     assert _call(L, _shape(Dqk=96)) == 2
+    assert _call(L, _shape(Dv=48)) == 2
 
 
 def test_rejects_causal_cross_attention(L):
@@ -110,7 +111,7 @@ def test_empty_problem_is_a_no_op(L):
 
 
 def test_forward_only_validation(L):
-    s = _shape(Dqk=128, Dv=32)
+    s = _shape(Dqk=128, Dv=24)
     assert L.attn_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, None, None, 0, float("nan"), FAKE, FAKE, None) == 2
 
 

@@ -128,6 +128,14 @@ EDGE = [
     (1, 2, 200, 1, 128, 128, False),
     (1, 1, 300, 300, 128, 128, True),
     (3, 2, 64, 200, 64, 128, False),
+    # cross-attention shapes of the Triton fused-attention JVP tests
+    # (M, N, Dqk, Dv), including head dims 16 and 32
+    (1, 2, 1000, 15, 128, 32, False),
+    (1, 2, 512, 512, 16, 32, False),
+    (1, 2, 515, 999, 16, 32, False),
+    (2, 3, 300, 300, 32, 32, True),
+    (1, 2, 200, 260, 32, 128, False),
+    (1, 2, 130, 70, 128, 16, False),
 ]
 
 
@@ -157,6 +165,18 @@ def test_jagged_edge_lengths(causal):
         inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"], inp["offsets"], 200,
         causal=causal, sm_scale=0.125)
     assert_close(O, tO, L, Or, tOr, Lr, what=f"jagged causal={causal}")
+
+
+def test_jagged_small_head_dims():
+    lens = [1, 64, 65, 200, 0, 129]
+    w = Workload("jag16", B=len(lens), H=2, Dqk=16, Dv=32, jagged=True, max_seq_len=160,
+                 max_len_draw=1, sm_scale=0.25)
+    inp = make_inputs(w, seed=21, lengths=lens)
+    O, tO, L = run_gpu(inp)
+    Or, tOr, Lr = oracle.attention_fwd_jvp_jagged(
+        inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"], inp["offsets"], 160,
+        sm_scale=0.25)
+    assert_close(O, tO, L, Or, tOr, Lr, what="jagged Dqk16 Dv32")
 
 
 def test_bias_and_mask_with_fully_masked_row():
