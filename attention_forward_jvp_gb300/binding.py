@@ -23,6 +23,8 @@ from . import build as _build
 EXPORTS = (
     "attn_fwd_jvp",
     "attn_fwd",
+    "attn_fwd_jvp_f16",
+    "attn_fwd_f16",
     "attn_fwd_jvp_noalloc",
     "attn_sync_check",
     "attn_status_string",
@@ -70,9 +72,13 @@ def lib() -> ctypes.CDLL:
                                ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp, vp]
     L.attn_fwd_jvp_noalloc.restype = i32
     L.attn_fwd_jvp_noalloc.argtypes = L.attn_fwd_jvp.argtypes
+    L.attn_fwd_jvp_f16.restype = i32
+    L.attn_fwd_jvp_f16.argtypes = L.attn_fwd_jvp.argtypes
     L.attn_fwd.restype = i32
     L.attn_fwd.argtypes = [ctypes.POINTER(AttnShape), vp, vp, vp, vp,
                            ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp]
+    L.attn_fwd_f16.restype = i32
+    L.attn_fwd_f16.argtypes = L.attn_fwd.argtypes
     L.attn_sync_check.restype = i32
     L.attn_sync_check.argtypes = [vp]
     L.attn_status_string.restype = ctypes.c_char_p
@@ -112,6 +118,12 @@ def set_wait_timeout_ns(ns: int):
 
 def debug_skip_first_load(enable: bool):
     lib().attn_debug_skip_first_load(1 if enable else 0)
+
+
+def _elem_type(q: torch.Tensor):
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"inputs must be bfloat16 or float16, got {q.dtype}")
+    return q.dtype
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -198,21 +210,23 @@ def attn_fwd_jvp(q, k, v, tq, tk, tv, causal: bool = False, sm_scale: Optional[f
             causal=causal, sm_scale=sm_scale, offsets=offsets, max_seq_len=max_seq_len,
             bias=bias, mask=mask), n_out=3)
     dev = q.device
+    dt = _elem_type(q)
     for name, t in (("q", q), ("k", k), ("v", v), ("tq", tq), ("tk", tk), ("tv", tv)):
-        _need(t, name, torch.bfloat16, dev)
+        _need(t, name, dt, dev)
     if tq.shape != q.shape or tk.shape != k.shape or tv.shape != v.shape:
         raise ValueError("tangents must have the primals' shapes")
     if offsets is not None:
         _need(offsets, "offsets", torch.int32, dev)
     sh, bs, out_shape, keep = _describe(q, k, v, offsets, max_seq_len, bias, mask)
     if out is None:
-        o = torch.empty(out_shape, dtype=torch.bfloat16, device=dev)
-        to = torch.empty(out_shape, dtype=torch.bfloat16, device=dev)
+        o = torch.empty(out_shape, dtype=dt, device=dev)
+        to = torch.empty(out_shape, dtype=dt, device=dev)
         lse = torch.empty(out_shape[:-1], dtype=torch.float32, device=dev)
     else:
         o, to, lse = out
     stream = torch.cuda.current_stream(dev).cuda_stream
-    st = lib().attn_fwd_jvp(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(tq), _ptr(tk),
+    fn = lib().attn_fwd_jvp_f16 if dt == torch.float16 else lib().attn_fwd_jvp
+    st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(tq), _ptr(tk),
                             _ptr(tv), _ptr(offsets), ctypes.byref(bs) if bs is not None else None,
                             1 if causal else 0, _scale(sm_scale), _ptr(o), _ptr(to), _ptr(lse),
                             ctypes.c_void_p(stream))
@@ -230,18 +244,20 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: Optional[float] = None,
             causal=causal, sm_scale=sm_scale, offsets=offsets, max_seq_len=max_seq_len,
             bias=bias, mask=mask), n_out=2)
     dev = q.device
+    dt = _elem_type(q)
     for name, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, name, torch.bfloat16, dev)
+        _need(t, name, dt, dev)
     if offsets is not None:
         _need(offsets, "offsets", torch.int32, dev)
     sh, bs, out_shape, keep = _describe(q, k, v, offsets, max_seq_len, bias, mask)
     if out is None:
-        o = torch.empty(out_shape, dtype=torch.bfloat16, device=dev)
+        o = torch.empty(out_shape, dtype=dt, device=dev)
         lse = torch.empty(out_shape[:-1], dtype=torch.float32, device=dev)
     else:
         o, lse = out
     stream = torch.cuda.current_stream(dev).cuda_stream
-    st = lib().attn_fwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(offsets),
+    fn = lib().attn_fwd_f16 if dt == torch.float16 else lib().attn_fwd
+    st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(offsets),
                         ctypes.byref(bs) if bs is not None else None, 1 if causal else 0,
                         _scale(sm_scale), _ptr(o), _ptr(lse), ctypes.c_void_p(stream))
     del keep

@@ -22,60 +22,86 @@ static_assert(attn::kPlanBM == attn::kBM && attn::kPlanBN == attn::kBN,
 // The kernels are instantiated once, in the attn_inst_*.cu files; these
 // declarations keep this file from instantiating its own copies.
 namespace attn {
-extern template cudaError_t launch_attn<64, 64, true, kNoBias>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, true, kBiasRing>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, true, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, kNoBias>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, kBiasRing>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, kNoBias>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, kBiasRing>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, kNoBias>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, kBiasRing>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, kNoBias>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, kBiasRing>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, kNoBias>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, kBiasRing>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, kNoBias>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, kBiasRing>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, kNoBias>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, kBiasRing>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, kBiasGlobal>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kNoBias, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, kNoBias, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, true, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, kNoBias, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, true, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, kNoBias, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, true, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 128, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 64, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
 }
 
 namespace {
 
 // The kernel instantiation for (Dqk, Dv) = key (bit 1: Dqk = 128, bit 0:
 // Dv = 128), tangents, bias / mask.
-template <bool JVP, int BMODE>
+template <bool JVP, int BMODE, bool F16>
 cudaError_t dispatch_dims(int key, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
   switch (key) {
-    case 0: return attn::launch_attn<64, 64, JVP, BMODE>(kp, grid, cs);
-    case 1: return attn::launch_attn<64, 128, JVP, BMODE>(kp, grid, cs);
-    case 2: return attn::launch_attn<128, 64, JVP, BMODE>(kp, grid, cs);
-    case 3: return attn::launch_attn<128, 128, JVP, BMODE>(kp, grid, cs);
+    case 0: return attn::launch_attn<64, 64, JVP, BMODE, F16>(kp, grid, cs);
+    case 1: return attn::launch_attn<64, 128, JVP, BMODE, F16>(kp, grid, cs);
+    case 2: return attn::launch_attn<128, 64, JVP, BMODE, F16>(kp, grid, cs);
+    case 3: return attn::launch_attn<128, 128, JVP, BMODE, F16>(kp, grid, cs);
   }
   return cudaErrorInvalidValue;
 }
 
-template <bool JVP>
+template <bool JVP, bool F16>
 cudaError_t dispatch_mode(int key, int mode, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
   switch (mode) {
-    case attn::kNoBias: return dispatch_dims<JVP, attn::kNoBias>(key, kp, grid, cs);
-    case attn::kBiasRing: return dispatch_dims<JVP, attn::kBiasRing>(key, kp, grid, cs);
-    case attn::kBiasGlobal: return dispatch_dims<JVP, attn::kBiasGlobal>(key, kp, grid, cs);
+    case attn::kNoBias: return dispatch_dims<JVP, attn::kNoBias, F16>(key, kp, grid, cs);
+    case attn::kBiasRing: return dispatch_dims<JVP, attn::kBiasRing, F16>(key, kp, grid, cs);
+    case attn::kBiasGlobal: return dispatch_dims<JVP, attn::kBiasGlobal, F16>(key, kp, grid, cs);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t dispatch_attn(int key, bool jvp, int mode, const attn::KernelParams& kp, int grid,
+cudaError_t dispatch_attn(int key, bool jvp, int mode, bool f16, const attn::KernelParams& kp, int grid,
                           cudaStream_t cs) {
-  return jvp ? dispatch_mode<true>(key, mode, kp, grid, cs) : dispatch_mode<false>(key, mode, kp, grid, cs);
+  if (f16)
+    return jvp ? dispatch_mode<true, true>(key, mode, kp, grid, cs) : dispatch_mode<false, true>(key, mode, kp, grid, cs);
+  return jvp ? dispatch_mode<true, false>(key, mode, kp, grid, cs) : dispatch_mode<false, false>(key, mode, kp, grid, cs);
 }
 
 constexpr int kMaxDevices = 64;
@@ -149,15 +175,17 @@ attn_status stream_list(cudaStream_t stream, int** out) {
   return ATTN_OK;
 }
 
-// 3-D bf16 view [z][rows][d] (d innermost), box 64 x box_rows x 1,
-// 128-byte swizzle; rows past `rows` read as zeros.
+// 3-D view [z][rows][d] (d innermost) of bf16 (f16 = false) or fp16
+// elements, box 64 x box_rows x 1, 128-byte swizzle; rows past `rows` and
+// columns past `d` read as zeros.
 bool encode_map(CUtensorMap* m, const void* base, uint64_t d, uint64_t rows, uint64_t z,
-                uint32_t box_rows) {
+                uint32_t box_rows, bool f16) {
   cuuint64_t dims[3] = {d, rows, z};
   cuuint64_t strides[2] = {d * 2, d * rows * 2};
   cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -199,7 +227,7 @@ bool encode_bias_map(CUtensorMap* m, const float* base, const int64_t* st, uint6
 attn_status run(const attn_shape* s, const void* q, const void* k, const void* v, const void* tq,
                 const void* tk, const void* tv, const int32_t* offsets, const attn_bias* bias,
                 int causal, float sm_scale, void* o, void* to, float* lse, void* stream,
-                bool jvp, const DeviceState* fixed = nullptr) {
+                bool jvp, const DeviceState* fixed = nullptr, bool f16 = false) {
   if (s == nullptr) return ATTN_ERR_INVALID_ARG;
   const bool jagged = offsets != nullptr;
   if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0) return ATTN_ERR_INVALID_ARG;
@@ -254,8 +282,8 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   kp.sm_scale = scale;
   kp.scale_log2 = scale * attn::kLog2e;
   kp.offsets = offsets;
-  kp.o = static_cast<__nv_bfloat16*>(o);
-  kp.to = static_cast<__nv_bfloat16*>(to);
+  kp.o = static_cast<uint16_t*>(o);
+  kp.to = static_cast<uint16_t*>(to);
   kp.lse = lse;
   kp.dv_out = s->Dv;
   kp.err = ds->scratch;
@@ -282,13 +310,13 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
     kp.max_seq_len = s->max_seq_len;
     kp.n_mt = (s->max_seq_len + attn::kBM - 1) / attn::kBM;
     const uint64_t T = static_cast<uint64_t>(s->T), H = static_cast<uint64_t>(s->H);
-    ok = ok && encode_map(&kp.tm_q, q, dqk, T, H, attn::kBM);
-    ok = ok && encode_map(&kp.tm_k, k, dqk, T, H, attn::kBN);
-    ok = ok && encode_map(&kp.tm_v, v, dvv, T, H, attn::kBN);
+    ok = ok && encode_map(&kp.tm_q, q, dqk, T, H, attn::kBM, f16);
+    ok = ok && encode_map(&kp.tm_k, k, dqk, T, H, attn::kBN, f16);
+    ok = ok && encode_map(&kp.tm_v, v, dvv, T, H, attn::kBN, f16);
     if (jvp) {
-      ok = ok && encode_map(&kp.tm_tq, tq, dqk, T, H, attn::kBM);
-      ok = ok && encode_map(&kp.tm_tk, tk, dqk, T, H, attn::kBN);
-      ok = ok && encode_map(&kp.tm_tv, tv, dvv, T, H, attn::kBN);
+      ok = ok && encode_map(&kp.tm_tq, tq, dqk, T, H, attn::kBM, f16);
+      ok = ok && encode_map(&kp.tm_tk, tk, dqk, T, H, attn::kBN, f16);
+      ok = ok && encode_map(&kp.tm_tv, tv, dvv, T, H, attn::kBN, f16);
     }
   } else {
     kp.M = s->M;
@@ -301,15 +329,15 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
     const void* kb = s->N > 0 ? k : q;
     const void* vb = s->N > 0 ? v : q;
     const uint64_t dvk = s->N > 0 ? dvv : dqk;
-    ok = ok && encode_map(&kp.tm_q, q, dqk, M, BH, attn::kBM);
-    ok = ok && encode_map(&kp.tm_k, kb, dqk, N, BH, attn::kBN);
-    ok = ok && encode_map(&kp.tm_v, vb, dvk, N, BH, attn::kBN);
+    ok = ok && encode_map(&kp.tm_q, q, dqk, M, BH, attn::kBM, f16);
+    ok = ok && encode_map(&kp.tm_k, kb, dqk, N, BH, attn::kBN, f16);
+    ok = ok && encode_map(&kp.tm_v, vb, dvk, N, BH, attn::kBN, f16);
     if (jvp) {
       const void* tkb = s->N > 0 ? tk : tq;
       const void* tvb = s->N > 0 ? tv : tq;
-      ok = ok && encode_map(&kp.tm_tq, tq, dqk, M, BH, attn::kBM);
-      ok = ok && encode_map(&kp.tm_tk, tkb, dqk, N, BH, attn::kBN);
-      ok = ok && encode_map(&kp.tm_tv, tvb, dvk, N, BH, attn::kBN);
+      ok = ok && encode_map(&kp.tm_tq, tq, dqk, M, BH, attn::kBM, f16);
+      ok = ok && encode_map(&kp.tm_tk, tkb, dqk, N, BH, attn::kBN, f16);
+      ok = ok && encode_map(&kp.tm_tv, tvb, dvk, N, BH, attn::kBN, f16);
     }
   }
   if (!ok) return ATTN_ERR_CUDA;
@@ -348,7 +376,7 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   const int mode = (kp.bias == nullptr && kp.mask == nullptr) ? attn::kNoBias
                    : (kp.bias != nullptr && kp.bias_tma == 0) ? attn::kBiasGlobal
                                                                : attn::kBiasRing;
-  e = dispatch_attn(key, jvp, mode, kp, grid, cs);
+  e = dispatch_attn(key, jvp, mode, f16, kp, grid, cs);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   g_launches.fetch_add(1);
   return ATTN_OK;
@@ -423,6 +451,21 @@ attn_status attn_fwd(const attn_shape* shape, const void* q, const void* k, cons
                      void* o, float* lse, void* stream) {
   return run(shape, q, k, v, nullptr, nullptr, nullptr, offsets, bias, causal, sm_scale, o,
              nullptr, lse, stream, false);
+}
+
+attn_status attn_fwd_jvp_f16(const attn_shape* shape, const void* q, const void* k, const void* v,
+                             const void* tq, const void* tk, const void* tv, const int32_t* offsets,
+                             const attn_bias* bias, int causal, float sm_scale, void* o, void* to,
+                             float* lse, void* stream) {
+  return run(shape, q, k, v, tq, tk, tv, offsets, bias, causal, sm_scale, o, to, lse, stream,
+             true, nullptr, true);
+}
+
+attn_status attn_fwd_f16(const attn_shape* shape, const void* q, const void* k, const void* v,
+                         const int32_t* offsets, const attn_bias* bias, int causal, float sm_scale,
+                         void* o, float* lse, void* stream) {
+  return run(shape, q, k, v, nullptr, nullptr, nullptr, offsets, bias, causal, sm_scale, o,
+             nullptr, lse, stream, false, nullptr, true);
 }
 
 attn_status attn_sync_check(void* stream) {

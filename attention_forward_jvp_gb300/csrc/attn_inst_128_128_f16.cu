@@ -1,0 +1,13 @@
+// Instantiations of the attention kernel for Dqk = 128, Dv = 128, f16
+// storage (with and without tangents, each bias / mask mode); one file per
+// head-dim pair and element type so the build compiles them in parallel.
+#include "attn_kernel.cuh"
+
+namespace attn {
+template cudaError_t launch_attn<128, 128, true, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+template cudaError_t launch_attn<128, 128, true, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+template cudaError_t launch_attn<128, 128, true, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+template cudaError_t launch_attn<128, 128, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+template cudaError_t launch_attn<128, 128, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+template cudaError_t launch_attn<128, 128, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+}  // namespace attn

@@ -92,8 +92,8 @@ struct KernelParams {
   long long bias_stride[4];
   const unsigned char* mask;
   long long mask_stride[4];
-  __nv_bfloat16* o;
-  __nv_bfloat16* to;
+  uint16_t* o;   // bf16 or fp16 storage (the kernel's element type)
+  uint16_t* to;
   float* lse;
   long long T;
   int max_seq_len;
@@ -336,7 +336,7 @@ __device__ __forceinline__ float ex2(float x) {
 
 // n32 packed bf16x2 words (a multiple of 4) to global memory with 16-byte
 // stores.
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* packed, int n32) {
+__device__ __forceinline__ void store_row_bf16(uint16_t* dst, const uint32_t* packed, int n32) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < n32 / 4; ++i)
@@ -377,7 +377,7 @@ __device__ __forceinline__ void quad_transpose(uint32_t (&a)[4 * C], int q) {
 // C packed words to global memory: one 32-byte store when C == 8 and the
 // address is 32-byte aligned, else 16-byte stores.
 template <int C>
-__device__ __forceinline__ void store_chunk(__nv_bfloat16* dst, const uint32_t* w, bool aligned32) {
+__device__ __forceinline__ void store_chunk(uint16_t* dst, const uint32_t* w, bool aligned32) {
   if (C == 8 && aligned32) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
                  "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
@@ -447,7 +447,8 @@ __device__ __forceinline__ float rowmax32(const float* x) {
 
 // BMODE: kNoBias, kBiasRing or kBiasGlobal (see Plan).  Each mode compiles
 // only its own bias / mask code, which keeps the per-tile loop small.
-template <int DQK, int DV, bool JVP, int BMODE>
+// F16: fp16 inputs, MMA operands and outputs instead of bf16.
+template <int DQK, int DV, bool JVP, int BMODE, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KernelParams p) {
   using P = Plan<DQK, DV, JVP, BMODE>;
   constexpr bool BM = BMODE != kNoBias;
@@ -690,10 +691,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // the waits for the K / V tiles of the next batches are placed in the
     // middle of a batch, while the tensor pipe still holds queued MMAs.
     const bool leader = elect_one();
-    constexpr uint32_t idesc_s = idesc_bf16(kBM, JVP ? 2 * kBN : kBN, false);  // [S | Q tK^T]
-    constexpr uint32_t idesc_t = idesc_bf16(kBM, kBN, false);                   // tQ K^T
-    constexpr uint32_t idesc_o = idesc_bf16(kBM, P::NQ * DV, true);             // [O | tO]
-    constexpr uint32_t idesc_h = idesc_bf16(kBM, DV, true);                     // H V
+    constexpr uint32_t idesc_s = idesc_16(kBM, JVP ? 2 * kBN : kBN, false, F16);  // [S | Q tK^T]
+    constexpr uint32_t idesc_t = idesc_16(kBM, kBN, false, F16);                   // tQ K^T
+    constexpr uint32_t idesc_o = idesc_16(kBM, P::NQ * DV, true, F16);             // [O | tO]
+    constexpr uint32_t idesc_h = idesc_16(kBM, DV, true, F16);                     // H V
     auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, wait_bar(b, parity, W));
     };
@@ -951,11 +952,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int i = 0; i < 32; i += 2) {
           const float o0 = __uint_as_float(ov[i]) * inv_l;
           const float o1 = __uint_as_float(ov[i + 1]) * inv_l;
-          po[c0 / 2 + i / 2] = pack_bf16x2(o0, o1);
+          po[c0 / 2 + i / 2] = pack2<F16>(o0, o1);
           if constexpr (JVP) {
             const float t0 = (__uint_as_float(tv[i]) - r_sum * o0) * inv_l;
             const float t1 = (__uint_as_float(tv[i + 1]) - r_sum * o1) * inv_l;
-            pt[c0 / 2 + i / 2] = pack_bf16x2(t0, t1);
+            pt[c0 / 2 + i / 2] = pack2<F16>(t0, t1);
           }
         }
       }
@@ -1002,8 +1003,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // this half's output columns: [half * DVH, min((half + 1) * DVH, dv_out))
         const int ncol = min(DVH, p.dv_out - half * DVH);
         if (row_ok && ncol > 0) {
-          __nv_bfloat16* orow = p.o + (w.out0 + qi) * p.dv_out + half * DVH;
-          __nv_bfloat16* torow = JVP ? p.to + (w.out0 + qi) * p.dv_out + half * DVH : nullptr;
+          uint16_t* orow = p.o + (w.out0 + qi) * p.dv_out + half * DVH;
+          uint16_t* torow = JVP ? p.to + (w.out0 + qi) * p.dv_out + half * DVH : nullptr;
           uint32_t z[DVH / 2];
 #pragma unroll
           for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
@@ -1224,9 +1225,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const uint64_t pp = f2_make(p0, p1);
           pv[c / 2] = pp;
           ls = f2_add(ls, pp);
-          const uint32_t pw = pack_bf16x2(p0, p1);
+          const uint32_t pw = pack2<F16>(p0, p1);
           pk[c / 2] = pw;
-          add_bf16x2_f32(pw, lt0, lt1);
+          add2_f32<F16>(pw, lt0, lt1);
         }
         tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, pk);
         if constexpr (JVP) {
@@ -1238,9 +1239,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 f2_mul(f2_make(__uint_as_float(tr[c]), __uint_as_float(tr[c + 1])), scale2);
             float h0, h1;
             f2_split(f2_mul(pv[c / 2], ts), h0, h1);
-            const uint32_t hw = pack_bf16x2(h0, h1);
+            const uint32_t hw = pack2<F16>(h0, h1);
             hk[c / 2] = hw;
-            add_bf16x2_f32(hw, rt0, rt1);
+            add2_f32<F16>(hw, rt0, rt1);
           }
           tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf + kHalf / 2, hk);
         }
@@ -1335,7 +1336,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, P::TMEM_COLS);
 }
 
-template <int DQK, int DV, bool JVP, int BMODE>
+template <int DQK, int DV, bool JVP, int BMODE, bool F16>
 cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
   using P = Plan<DQK, DV, JVP, BMODE>;
   static bool attr_done[64] = {};
@@ -1347,16 +1348,16 @@ cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
     // computed for; a build that compiled to another count is refused
     // (setmaxnreg.inc would otherwise wait for registers that never free).
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP, BMODE>);
+    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP, BMODE, F16>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP, BMODE>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP, BMODE, F16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  attn_fwd_kernel<DQK, DV, JVP, BMODE><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
+  attn_fwd_kernel<DQK, DV, JVP, BMODE, F16><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
   return cudaGetLastError();
 }
 

@@ -4,6 +4,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace attn {
@@ -165,12 +166,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
-// A is K-major; B is K-major or MN-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
+// Instruction descriptor, kind::f16: A and B both bf16 (f16 = false) or
+// both fp16, fp32 D, dense.  A is K-major; B is K-major or MN-major.
+__host__ __device__ constexpr uint32_t idesc_16(int m, int n, bool b_mn_major, bool f16) {
   return (1u << 4)                                  // D = f32
-         | (1u << 7)                                // A = bf16
-         | (1u << 10)                               // B = bf16
+         | ((f16 ? 0u : 1u) << 7)                   // A = f16 (0) / bf16 (1)
+         | ((f16 ? 0u : 1u) << 10)                  // B = f16 (0) / bf16 (1)
          | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
          | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
@@ -290,6 +291,32 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// acc0 += low fp16 half of w, acc1 += high half.
+__device__ __forceinline__ void add_f16x2_f32(uint32_t w, float& acc0, float& acc1) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Round a pair to the 16-bit operand type (round to nearest even) and pack.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+// acc += the two 16-bit values of w, widened exactly.
+template <bool F16>
+__device__ __forceinline__ void add2_f32(uint32_t w, float& acc0, float& acc1) {
+  if constexpr (F16) add_f16x2_f32(w, acc0, acc1);
+  else add_bf16x2_f32(w, acc0, acc1);
 }
 
 }  // namespace attn

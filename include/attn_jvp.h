@@ -33,7 +33,8 @@
  *   - Pointers q..lse are DEVICE pointers owned by the caller; the library
  *     keeps none of them after the call returns.  Every one of them must be
  *     16-byte aligned (bulk tensor copies), else ATTN_ERR_MISALIGNED.
- *   - q, k, v, tq, tk, tv, o, to are bf16 (raw 16-bit storage), lse fp32.
+ *   - q, k, v, tq, tk, tv, o, to are bf16 (raw 16-bit storage), lse fp32;
+ *     the *_f16 entry points take fp16 instead of bf16.
  *   - Dense layouts (offsets == NULL), all contiguous, row-major:
  *       q, tq [B, H, M, Dqk]   k, tk [B, H, N, Dqk]   v, tv [B, H, N, Dv]
  *       o, to [B, H, M, Dv]    lse   [B, H, M]
@@ -122,6 +123,25 @@ attn_status attn_fwd(const attn_shape* shape,
                      const int32_t* offsets, const attn_bias* bias,
                      int causal, float sm_scale,
                      void* o, float* lse, void* stream);
+
+/* attn_fwd_jvp and attn_fwd with fp16 storage: q, k, v, tq, tk, tv, o and
+ * to are IEEE half precision instead of bf16 (lse stays fp32); P and its
+ * tangent product enter the output MMAs as fp16.  Everything else is as
+ * above.  The Triton kernels of "Flash Attention v2 with JVP" and of the
+ * fused-attention JVP tutorial accept fp16 and bf16 inputs alike.  P is at
+ * most 2^8 here (the lazy rescale threshold) and P o tS at most 2^8 |tS|,
+ * so fp16 holds them for |tS| below ~256. */
+attn_status attn_fwd_jvp_f16(const attn_shape* shape,
+                             const void* q, const void* k, const void* v,
+                             const void* tq, const void* tk, const void* tv,
+                             const int32_t* offsets, const attn_bias* bias,
+                             int causal, float sm_scale,
+                             void* o, void* to, float* lse, void* stream);
+attn_status attn_fwd_f16(const attn_shape* shape,
+                         const void* q, const void* k, const void* v,
+                         const int32_t* offsets, const attn_bias* bias,
+                         int causal, float sm_scale,
+                         void* o, float* lse, void* stream);
 
 /* attn_fwd_jvp for callers that may not allocate device memory: a framework
  * that owns every device allocation, a runtime that forbids cudaMalloc

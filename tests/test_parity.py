@@ -252,6 +252,42 @@ def test_outputs_16_byte_but_not_32_byte_aligned(Dv):
                  *oracle_dense(inp), what=f"16-byte aligned outputs Dv={Dv}")
 
 
+# ------------------------------------------------------------- fp16 storage
+def _to_f16(inp):
+    """The same draws rounded to fp16; the oracle reads these fp16 values."""
+    out = dict(inp)
+    for n in ("q", "k", "v", "tq", "tk", "tv"):
+        out[n] = inp[n].to(torch.float16)
+    return out
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("dense", dict(B=2, H=3, M=300, N=260, Dqk=128, Dv=64)),
+    ("causal", dict(B=1, H=2, M=640, N=640, Dqk=128, Dv=128, causal=True)),
+    ("d64", dict(B=2, H=2, M=400, N=700, Dqk=64, Dv=64)),
+    ("bias", dict(B=2, H=2, M=256, N=512, Dqk=128, Dv=64, bias=True, mask_keep=400)),
+    ("small", dict(B=1, H=2, M=515, N=999, Dqk=16, Dv=32)),
+])
+def test_fp16_storage(name, kw):
+    inp = _to_f16(make_inputs(Workload("f16", **kw), seed=31))
+    O, tO, L = run_gpu(inp)
+    assert_close(O, tO, L, *oracle_dense(inp), what=f"fp16 {name}")
+
+
+def test_fp16_jagged_and_forward_only():
+    lens = [3, 64, 130, 257, 1]
+    w = Workload("jf16", B=len(lens), H=2, Dqk=64, Dv=64, jagged=True, max_seq_len=300,
+                 max_len_draw=1, sm_scale=0.125)
+    inp = _to_f16(make_inputs(w, seed=32, lengths=lens))
+    O, tO, L = run_gpu(inp)
+    Or, tOr, Lr = oracle.attention_fwd_jvp_jagged(
+        inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"], inp["offsets"], 300,
+        sm_scale=0.125)
+    assert_close(O, tO, L, Or, tOr, Lr, what="fp16 jagged")
+    O2, L2 = run_gpu(inp, jvp=False)
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)
+
+
 # -------------------------------------------------------- kernel invariants
 @pytest.mark.parametrize("name", ["tiny", "edge_causal", "edge_bias"])
 def test_forward_only_matches_jvp_primal_bitwise(name):
