@@ -70,12 +70,19 @@ extern template cudaError_t launch_attn<128, 128, false, kBiasRing, false>(const
 extern template cudaError_t launch_attn<128, 128, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<128, 128, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<128, 128, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<256, 256, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<256, 256, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<256, 256, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<256, 256, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
 }
 
 namespace {
 
-// The kernel instantiation for (Dqk, Dv) = key (bit 1: Dqk = 128, bit 0:
-// Dv = 128), tangents, bias / mask.
+// The kernel instantiation for (Dqk, Dv) = key (0..3: bit 1 set for
+// Dqk = 128, bit 0 for Dv = 128, else 64; 4: 256 x 256, forward only),
+// tangents, bias / mask mode and element type.
 template <bool JVP, int BMODE, bool F16>
 cudaError_t dispatch_dims(int key, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
   switch (key) {
@@ -83,6 +90,9 @@ cudaError_t dispatch_dims(int key, const attn::KernelParams& kp, int grid, cudaS
     case 1: return attn::launch_attn<64, 128, JVP, BMODE, F16>(kp, grid, cs);
     case 2: return attn::launch_attn<128, 64, JVP, BMODE, F16>(kp, grid, cs);
     case 3: return attn::launch_attn<128, 128, JVP, BMODE, F16>(kp, grid, cs);
+    case 4:  // head dims 256 x 256, forward only
+      if constexpr (!JVP) return attn::launch_attn<256, 256, false, BMODE, F16>(kp, grid, cs);
+      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -232,7 +242,10 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   const bool jagged = offsets != nullptr;
   if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0) return ATTN_ERR_INVALID_ARG;
   auto dim_ok = [](int d) { return d == 16 || d == 32 || d == 64 || d == 128; };
-  if (!dim_ok(s->Dqk) || !dim_ok(s->Dv)) return ATTN_ERR_UNSUPPORTED;
+  // 256 x 256 only without tangents: O and tO of 256 columns each would take
+  // all 512 tensor-memory columns, leaving none for the scores
+  const bool d256 = s->Dqk == 256 && s->Dv == 256;
+  if (!(d256 && !jvp) && (!dim_ok(s->Dqk) || !dim_ok(s->Dv))) return ATTN_ERR_UNSUPPORTED;
   if (!std::isnan(sm_scale) && !(sm_scale > 0.f && std::isfinite(sm_scale)))
     return ATTN_ERR_INVALID_ARG;
   const bool has_bias = bias != nullptr && (bias->bias != nullptr || bias->mask != nullptr);
@@ -370,7 +383,7 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   cudaError_t e = cudaErrorInvalidValue;
   // head dims 16 and 32 run the 64-wide kernels: the tensor maps keep the
   // true dims and their 64-column boxes read zeros past them
-  const int key = (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
+  const int key = d256 ? 4 : (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
   // bias through the shared-memory ring when a tensor map describes it,
   // else per-thread loads; a mask alone also takes the ring mode
   const int mode = (kp.bias == nullptr && kp.mask == nullptr) ? attn::kNoBias

@@ -67,6 +67,8 @@ def test_rejects_unsupported_head_dims(L):
     assert _call(L, _shape(Dv=256)) == 2
     assert _call(L, _shape(Dqk=96)) == 2
     assert _call(L, _shape(Dv=48)) == 2
+    assert _call(L, _shape(Dqk=256, Dv=256)) == 2   # 256 only without tangents
+    assert _call(L, _shape(Dqk=256, Dv=128)) == 2
 
 
 def test_rejects_causal_cross_attention(L):

@@ -252,6 +252,28 @@ def test_outputs_16_byte_but_not_32_byte_aligned(Dv):
                  *oracle_dense(inp), what=f"16-byte aligned outputs Dv={Dv}")
 
 
+# ------------------------------------------------------ head dim 256 (forward)
+@pytest.mark.parametrize("name,kw", [
+    ("dense", dict(B=2, H=2, M=300, N=333, Dqk=256, Dv=256)),
+    ("causal", dict(B=1, H=3, M=400, N=400, Dqk=256, Dv=256, causal=True)),
+    ("bias", dict(B=2, H=2, M=200, N=260, Dqk=256, Dv=256, bias=True, mask_keep=200)),
+])
+def test_head_dim_256_forward(name, kw):
+    inp = make_inputs(Workload("d256", input_std=0.5, **kw), seed=41)
+    O, L = run_gpu(inp, jvp=False)
+    Or, _, Lr = oracle_dense(inp)
+    assert_close(O, np.zeros_like(O), L, Or, np.zeros_like(Or), Lr, what=f"D256 {name}")
+
+
+def test_head_dim_256_fp16_forward():
+    inp = make_inputs(Workload("d256h", B=1, H=2, M=260, N=300, Dqk=256, Dv=256, input_std=0.5), seed=42)
+    for n in ("q", "k", "v", "tq", "tk", "tv"):
+        inp[n] = inp[n].to(torch.float16)
+    O, L = run_gpu(inp, jvp=False)
+    Or, _, Lr = oracle_dense(inp)
+    assert_close(O, np.zeros_like(O), L, Or, np.zeros_like(Or), Lr, what="D256 fp16")
+
+
 # ------------------------------------------------------------- fp16 storage
 def _to_f16(inp):
     """The same draws rounded to fp16; the oracle reads these fp16 values."""
