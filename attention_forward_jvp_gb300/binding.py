@@ -26,6 +26,8 @@ EXPORTS = (
     "attn_fwd_jvp_f16",
     "attn_fwd_f16",
     "attn_fwd_jvp_noalloc",
+    "attn_bwd",
+    "attn_bwd_f16",
     "attn_sync_check",
     "attn_status_string",
     "attn_launch_count",
@@ -79,6 +81,11 @@ def lib() -> ctypes.CDLL:
                            ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp]
     L.attn_fwd_f16.restype = i32
     L.attn_fwd_f16.argtypes = L.attn_fwd.argtypes
+    L.attn_bwd.restype = i32
+    L.attn_bwd.argtypes = [ctypes.POINTER(AttnShape), vp, vp, vp, vp, vp, vp, vp,
+                           ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp, vp, vp]
+    L.attn_bwd_f16.restype = i32
+    L.attn_bwd_f16.argtypes = L.attn_bwd.argtypes
     L.attn_sync_check.restype = i32
     L.attn_sync_check.argtypes = [vp]
     L.attn_status_string.restype = ctypes.c_char_p
@@ -263,6 +270,37 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: Optional[float] = None,
     del keep
     _check(st)
     return o, lse
+
+
+def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float] = None,
+             out=None):
+    """Attention backward (dense, no bias / mask, Dqk == Dv).  Takes the
+    forward's inputs, its output ``o`` and log-sum-exp ``lse`` and the
+    gradient ``do`` of O; returns (dq, dk, dv, delta), delta = rowsum(do o o)
+    in float32."""
+    if q.device.type == "cpu":
+        return _host_call(attn_bwd, (q, k, v, o, lse, do), dict(causal=causal, sm_scale=sm_scale),
+                          n_out=4)
+    dev = q.device
+    dt = _elem_type(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _need(t, name, dt, dev)
+    _need(lse, "lse", torch.float32, dev)
+    sh, _, out_shape, _ = _describe(q, k, v, None, None, None, None)
+    if tuple(o.shape) != out_shape or tuple(do.shape) != out_shape or tuple(lse.shape) != out_shape[:-1]:
+        raise ValueError("o and do must be [B, H, M, Dv] and lse [B, H, M]")
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        delta = torch.empty(out_shape[:-1], dtype=torch.float32, device=dev)
+    else:
+        dq, dk, dv, delta = out
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    fn = lib().attn_bwd_f16 if dt == torch.float16 else lib().attn_bwd
+    st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), None, None,
+            1 if causal else 0, _scale(sm_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
+            ctypes.c_void_p(stream))
+    _check(st)
+    return dq, dk, dv, delta
 
 
 def _host_call(fn, tensors, kw, n_out):

@@ -1,0 +1,512 @@
+// Attention backward for sm_103a: gradients dQ, dK, dV of a loss through
+// O = softmax(s Q K^T) V, given dO and the forward's log-sum-exp.
+//
+// Method (the Triton fused-attention tutorial's backward, "_attn_bwd_dkdv"
+// and "_attn_bwd_dq"; "flash_attention.py" "_attn_bwd_dkdv_inner" /
+// "_attn_bwd_dq_inner"): P is recomputed from the stored LSE, no running
+// maximum, and
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - Delta),  dQ = s dS K,  dK = s dS^T Q
+// with Delta = rowsum(dO o O) from a preprocessing pass.  Two passes, each
+// a persistent kernel of this template:
+//   dQ pass (KV = false): a unit is 128 query rows; key tiles of 64 stream
+//     by.  Row operands Q, dO; streamed K, V.  Scores S = Q K^T, dP = dO V^T;
+//     dQ += dS K.
+//   dK / dV pass (KV = true): a unit is 128 key rows; query tiles of 64
+//     stream by.  Row operands K, V; streamed Q, dO.  S^T = K Q^T,
+//     dP^T = V dO^T; dV += P^T dO, dK += dS^T Q.
+// Neither pass needs atomics: each owns its output rows.
+//
+// GB300 mapping (one CTA per SM, 12 warps, as the forward kernel):
+//   warp 0  bulk-tensor producer: the unit's two row operands, then the
+//           two streamed operands of each tile into a ring of NS stages.
+//   warp 1  tcgen05 issuer (whole warp, one elected lane): per tile the two
+//           score chains (N = 64 each) into a double-buffered TMEM pair,
+//           then the previous tile's output chain(s) from TMEM operands.
+//           A commit after a unit's last score chain frees the row operands
+//           (a commit completes its barrier exactly once, when the MMAs
+//           before it are done, so no waiter can mistake one phase for
+//           another).
+//   warps 4..11  elementwise warps, two per TMEM lane quadrant, 32 of the 64
+//           columns each: P = exp2(S s log2e - LSE log2e), dS = P (dP - Delta),
+//           written as 16-bit operands over the thread's own dP columns;
+//           the epilogue scales and stores the accumulators.
+#pragma once
+#include "attn_kernel.cuh"
+
+namespace attn {
+
+struct BwdParams {
+  CUtensorMap tm_r1, tm_r2;  // row operands, box 64 x 128 (dQ: Q, dO; KV: K, V)
+  CUtensorMap tm_t1, tm_t2;  // streamed operands, box 64 x 64 (dQ: K, V; KV: Q, dO)
+  int B, H, M, N;
+  int causal;
+  int n_rt;       // row tiles of 128 per (b, h)
+  int num_units;  // B * H * n_rt
+  float scale_log2;  // sm_scale * log2(e)
+  float sm_scale;
+  const float* lse;    // [B, H, M], natural log
+  const float* delta;  // [B, H, M]
+  uint16_t* out1;      // dQ pass: dQ [B,H,M,D]; KV pass: dK [B,H,N,D]
+  uint16_t* out2;      // KV pass: dV [B,H,N,D]
+  int d_out;           // head dim of the tensors (D, or 16 / 32 padded to D = 64)
+  int* err;
+  unsigned long long timeout_ns;
+};
+
+template <int D, bool KV>
+struct BwdPlan {
+  static constexpr int TN = 64;                      // streamed rows per tile
+  static constexpr int R_SUB = kBM * 128;            // 64-column chunk of a row operand
+  static constexpr int T_SUB = TN * 128;             // 64-column chunk of a streamed tile
+  static constexpr int R_TILE = (D / 64) * R_SUB;
+  static constexpr int T_TILE = (D / 64) * T_SUB;
+  static constexpr int RSET = 2 * R_TILE;            // R1 then R2
+  static constexpr int T_STAGE = 2 * T_TILE;         // T1 then T2
+  static constexpr int BUDGET = 227 * 1024 - 1024;
+  static constexpr int NS = (RSET + 4 * T_STAGE <= BUDGET) ? 4 : (RSET + 3 * T_STAGE <= BUDGET) ? 3 : 2;
+  static constexpr int OFF_R = 0;
+  static constexpr int OFF_T = RSET;
+  static constexpr int OFF_BAR = OFF_T + NS * T_STAGE;
+  // barriers: r_full, r_empty, t_full[NS], t_empty[NS], s_full[2], p_full[2], drain
+  static constexpr int B_RF = 0, B_RE = 1, B_TF = 2, B_TE = B_TF + NS, B_SF = B_TE + NS,
+                       B_PF = B_SF + 2, B_DRAIN = B_PF + 2, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16;
+  static constexpr int SMEM_LAUNCH = SMEM_BYTES > 120 * 1024 ? SMEM_BYTES : 120 * 1024;
+  // TMEM: buffer b = [X (64 fp32: S or S^T) | Y (64 fp32: dP or dP^T)] at
+  // b * 128; accumulators after them: dQ pass dQ (D); KV pass dV (D), dK (D)
+  static constexpr int SBUF = 2 * TN;
+  static constexpr int COL_A = 2 * SBUF;
+  static constexpr int COLS_USED = COL_A + (KV ? 2 : 1) * D;
+  static constexpr int TMEM_COLS = COLS_USED <= 256 ? 256 : 512;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
+  static_assert(COLS_USED <= 512, "tensor memory plan exceeds 512 columns");
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+};
+
+struct BwdUnit {
+  int z;        // b * H + h
+  int rt;       // row tile
+  int t0;       // first streamed tile index (KV causal: the diagonal)
+  int nt;       // streamed tiles
+  int rows;     // valid rows of this (b, h): M (dQ) or N (KV)
+};
+
+// Unit u: causal dQ units go longest-first (descending query tile), causal
+// KV units too (ascending key tile: more query tiles above the diagonal).
+template <bool KV>
+__device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
+  const int BH = p.B * p.H;
+  BwdUnit w;
+  if (p.causal) {
+    w.rt = KV ? u / BH : p.n_rt - 1 - u / BH;
+    w.z = u % BH;
+  } else {
+    w.z = u / p.n_rt;
+    w.rt = u % p.n_rt;
+  }
+  if (!KV) {
+    w.rows = p.M;
+    int hi = p.N;
+    if (p.causal) hi = min(hi, (w.rt + 1) * kBM);
+    w.t0 = 0;
+    w.nt = (hi + 63) / 64;
+  } else {
+    w.rows = p.N;
+    const int nq = (p.M + 63) / 64;
+    w.t0 = p.causal ? (w.rt * kBM) / 64 : 0;
+    w.nt = max(0, nq - w.t0);
+  }
+  return w;
+}
+
+template <int D, bool KV, bool F16>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using P = BwdPlan<D, KV>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, ERR_SMEM_ALIGN);
+    return;
+  }
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + P::OFF_BAR;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(P::B_RF), 1);
+    mbar_init(bar(P::B_RE), 1);
+    for (int i = 0; i < P::NS; ++i) {
+      mbar_init(bar(P::B_TF + i), 1);
+      mbar_init(bar(P::B_TE + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(P::B_SF + i), 1);
+      mbar_init(bar(P::B_PF + i), 8);  // one arrival per elementwise warp
+    }
+    mbar_init(bar(P::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tm_r1);
+    prefetch_tmap(&p.tm_r2);
+    prefetch_tmap(&p.tm_t1);
+    prefetch_tmap(&p.tm_t2);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), P::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter W{abort_flag, p.err, p.timeout_ns};
+  auto unit_at = [&](int rnd) { return unit_of_round(rnd); };
+
+  if (warp < 4) {
+    setmaxnreg_dec<kLowRegs>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        uint32_t rfill = 0, tfill = 0;
+        bool ok = true;
+        for (int rnd = 0; ok; ++rnd) {
+          const int u = unit_at(rnd);
+          if (u >= p.num_units) break;
+          const BwdUnit w = bwd_unit<KV>(p, u);
+          if (w.nt == 0) continue;
+          ok = wait_bar(bar(P::B_RE), (rfill & 1u) ^ 1u, W);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(P::B_RF), P::RSET);
+          const int r = w.rt * kBM;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d(sbase + P::OFF_R + c * P::R_SUB, &p.tm_r1, bar(P::B_RF), c * 64, r, w.z);
+            tma_load_3d(sbase + P::OFF_R + P::R_TILE + c * P::R_SUB, &p.tm_r2, bar(P::B_RF), c * 64, r,
+                        w.z);
+          }
+          ++rfill;
+          for (int j = 0; j < w.nt; ++j) {
+            const int tr = (w.t0 + j) * P::TN;
+            const uint32_t ts = tfill % P::NS;
+            ok = wait_bar(bar(P::B_TE + ts), ((tfill / P::NS) & 1u) ^ 1u, W);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(P::B_TF + ts), P::T_STAGE);
+            const uint32_t dst = sbase + P::OFF_T + ts * P::T_STAGE;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              tma_load_3d(dst + c * P::T_SUB, &p.tm_t1, bar(P::B_TF + ts), c * 64, tr, w.z);
+              tma_load_3d(dst + P::T_TILE + c * P::T_SUB, &p.tm_t2, bar(P::B_TF + ts), c * 64, tr, w.z);
+            }
+            ++tfill;
+          }
+        }
+        for (uint32_t s = 0; s < P::NS && s < tfill; ++s) {
+          const uint32_t nf = (tfill - s + P::NS - 1) / P::NS;
+          drain_bar(bar(P::B_TF + s), (nf - 1) & 1u, p.timeout_ns);
+        }
+        if (rfill > 0) drain_bar(bar(P::B_RF), (rfill - 1) & 1u, p.timeout_ns);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      const bool leader = elect_one();
+      constexpr uint32_t idesc_s = idesc_16(kBM, P::TN, false, F16);  // score chains, N = 64
+      constexpr uint32_t idesc_a = idesc_16(kBM, D, true, F16);       // output chains, N = D
+      auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait_bar(b, parity, W));
+      };
+      // output chain(s) of tile t (ring stage ts), first tile of a unit: zero-init
+      auto issue_out = [&](uint32_t t, uint32_t ts, bool first) -> bool {
+        const uint32_t sb = t & 1u;
+        if (!wait_all(bar(P::B_PF + sb), (t >> 1) & 1u)) return false;
+        tc_fence_after();
+        const uint32_t sT = sbase + P::OFF_T + ts * P::T_STAGE;
+        // 16-bit operands over the Y columns: half h at Y + 32 h holds
+        // P^T (KV pass) at +0 and dS at +16 (KV) / +0 (dQ pass), 8 packed
+        // columns per 16 streamed rows
+        const uint32_t aY = tmem + sb * P::SBUF + P::TN;
+        if (KV) {
+          // dV += P^T dO
+#pragma unroll
+          for (int kk = 0; kk < P::TN / 16; ++kk) {
+            const uint64_t db = sdesc_sw128(sT + P::T_TILE + kk * 2048, P::T_SUB, 1024);
+            if (leader)
+              mma_ts(tmem + P::COL_A, aY + 32 * (kk >> 1) + 8 * (kk & 1), db, idesc_a,
+                     (first && kk == 0) ? 0u : 1u);
+            __syncwarp();
+          }
+        }
+        // dQ += dS K   /   dK += dS^T Q
+        const uint32_t acc = tmem + P::COL_A + (KV ? D : 0);
+        const uint32_t ds_off = KV ? 16u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < P::TN / 16; ++kk) {
+          const uint64_t db = sdesc_sw128(sT + kk * 2048, P::T_SUB, 1024);
+          if (leader)
+            mma_ts(acc, aY + 32 * (kk >> 1) + ds_off + 8 * (kk & 1), db, idesc_a,
+                   (first && kk == 0) ? 0u : 1u);
+          __syncwarp();
+        }
+        if (leader) tc_commit(bar(P::B_TE + ts));  // also: this tile's output MMAs done
+        __syncwarp();
+        return true;
+      };
+      uint32_t ruse = 0, tuse = 0, g = 0;
+      bool ok = true;
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_at(rnd);
+        if (u >= p.num_units) break;
+        const BwdUnit w = bwd_unit<KV>(p, u);
+        if (w.nt == 0) continue;
+        ok = wait_all(bar(P::B_RF), ruse & 1u);
+        if (!ok) break;
+        const uint32_t sR1 = sbase + P::OFF_R, sR2 = sbase + P::OFF_R + P::R_TILE;
+        for (int j = 0; j < w.nt; ++j, ++g) {
+          const uint32_t ts = tuse % P::NS;
+          ok = wait_all(bar(P::B_TF + ts), (tuse / P::NS) & 1u);
+          if (!ok) break;
+          const uint32_t sT = sbase + P::OFF_T + ts * P::T_STAGE;
+          const uint32_t dX = tmem + (g & 1u) * P::SBUF;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            const uint64_t da = sdesc_sw128(sR1 + (kk >> 2) * P::R_SUB + off, 16, 1024);
+            const uint64_t db = sdesc_sw128(sT + (kk >> 2) * P::T_SUB + off, 16, 1024);
+            if (leader) mma_ss(dX, da, db, idesc_s, kk > 0 ? 1u : 0u);
+            __syncwarp();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            const uint64_t da = sdesc_sw128(sR2 + (kk >> 2) * P::R_SUB + off, 16, 1024);
+            const uint64_t db = sdesc_sw128(sT + P::T_TILE + (kk >> 2) * P::T_SUB + off, 16, 1024);
+            if (leader) mma_ss(dX + P::TN, da, db, idesc_s, kk > 0 ? 1u : 0u);
+            __syncwarp();
+          }
+          if (leader) {
+            tc_commit(bar(P::B_SF + (g & 1u)));
+            // the unit's last score chain: the row operands are free once it
+            // is done (the output chains never read them)
+            if (j == w.nt - 1) tc_commit(bar(P::B_RE));
+          }
+          __syncwarp();
+          ++tuse;
+          if (j > 0) {
+            ok = issue_out(g - 1, (tuse - 2) % P::NS, j == 1);
+            if (!ok) break;
+          }
+        }
+        if (!ok) break;
+        ok = issue_out(g - 1, (tuse - 1) % P::NS, w.nt == 1);
+        ++ruse;
+      }
+      if (leader) {
+        tc_commit(bar(P::B_DRAIN));
+        drain_bar(bar(P::B_DRAIN), 0, p.timeout_ns);
+      }
+      __syncwarp();
+    }
+  } else {
+    setmaxnreg_inc<kHighRegs>();
+    // ---------------------------------------------- elementwise / epilogue
+    const int quad = warp & 3;
+    const int half = (warp - 4) >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    constexpr float kLog2eF = 1.4426950408889634f;
+    uint32_t g = 0, tuse = 0;
+    bool ok = true;
+    for (int rnd = 0; ok; ++rnd) {
+      const int u = unit_at(rnd);
+      if (u >= p.num_units) break;
+      const BwdUnit w = bwd_unit<KV>(p, u);
+      const int ri = w.rt * kBM + row;  // this thread's row (query for dQ, key for KV)
+      const bool row_ok = ri < w.rows;
+      const long long zrow = static_cast<long long>(w.z);
+      if (w.nt == 0) {
+        // no streamed tile touches these rows: zero gradients
+        if (row_ok) {
+          const int ncol = min(D / 2, p.d_out - half * (D / 2));  // a multiple of 8
+          const long long off = (zrow * w.rows + ri) * p.d_out + half * (D / 2);
+          for (int c = 0; c < ncol; c += 8) {
+            *reinterpret_cast<uint4*>(p.out1 + off + c) = make_uint4(0u, 0u, 0u, 0u);
+            if (KV) *reinterpret_cast<uint4*>(p.out2 + off + c) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
+      // dQ pass: the row's LSE (log2 units) and Delta
+      float lse2_r = INFINITY, delta_r = 0.f;
+      if (!KV && row_ok) {
+        const float l = __ldg(p.lse + zrow * p.M + ri);
+        lse2_r = l == -INFINITY ? INFINITY : l * kLog2eF;  // empty row: P = 0
+        delta_r = __ldg(p.delta + zrow * p.M + ri);
+      }
+      for (int j = 0; j < w.nt; ++j, ++g, ++tuse) {
+        const uint32_t sb = g & 1u;
+        const int col0 = (w.t0 + j) * 64 + half * 32;  // first column (key or query) of this thread
+        float lse2_c[32], delta_c[32];
+        if (KV) {
+          // the 32 query columns' LSE and Delta (the same for every lane)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int qi = col0 + c;
+            float l = INFINITY, dd = 0.f;
+            if (qi < p.M) {
+              const float v = __ldg(p.lse + zrow * p.M + qi);
+              l = v == -INFINITY ? INFINITY : v * kLog2eF;
+              dd = __ldg(p.delta + zrow * p.M + qi);
+            }
+            lse2_c[c] = l;
+            delta_c[c] = dd;
+          }
+        }
+        ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t xr[32], yr[32];
+        tmem_ld_32x32b_x32(tl + sb * P::SBUF + half * 32, xr);
+        tmem_ld_32x32b_x32(tl + sb * P::SBUF + P::TN + half * 32, yr);
+        tmem_wait_ld_regs(xr);
+        tmem_regs_ready(yr);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int cc = c + e;
+            const int col = col0 + cc;
+            bool keep;
+            float l2, dl;
+            if (!KV) {  // row = query ri, column = key col
+              keep = col < p.N && (!p.causal || col <= ri);
+              l2 = lse2_r;
+              dl = delta_r;
+            } else {    // row = key ri, column = query col
+              keep = col < p.M && (!p.causal || ri <= col);
+              l2 = lse2_c[cc];
+              dl = delta_c[cc];
+            }
+            const float pe = keep ? ex2(fmaf(__uint_as_float(xr[cc]), p.scale_log2, -l2)) : 0.f;
+            pv[e] = pe;
+            dv[e] = pe * (__uint_as_float(yr[cc]) - dl);
+          }
+          pk[c / 2] = pack2<F16>(pv[0], pv[1]);
+          dk[c / 2] = pack2<F16>(dv[0], dv[1]);
+        }
+        const uint32_t yb = tl + sb * P::SBUF + P::TN + half * 32;
+        if (KV) {
+          tmem_st_32x32b_x16(yb, pk);
+          tmem_st_32x32b_x16(yb + 16, dk);
+        } else {
+          tmem_st_32x32b_x16(yb, dk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(P::B_PF + sb));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      // every MMA of the unit is done once the last tile's output MMAs are
+      // (their commit is the last tile's ring-stage release; the phase after
+      // it needs a tile this thread has not processed yet)
+      const uint32_t tl_last = tuse - 1;
+      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_TE + tl_last % P::NS), (tl_last / P::NS) & 1u, W));
+      if (!ok) break;
+      tc_fence_after();
+      constexpr int DH = D / 2;     // columns per thread
+      constexpr int NW = DH / 2;    // packed words
+      constexpr int CW = NW / 4;
+      const int q = lane & 3;
+      for (int which = 0; which < (KV ? 2 : 1); ++which) {
+        // dQ pass: dQ (scaled).  KV pass: which 0 = dV (unscaled), 1 = dK (scaled)
+        const uint32_t colA = P::COL_A + (KV ? (which == 0 ? 0 : D) : 0);
+        const float f = (KV && which == 0) ? 1.f : p.sm_scale;
+        uint32_t pw[NW];
+#pragma unroll
+        for (int c0 = 0; c0 < DH; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tl + colA + half * DH + c0, v);
+          tmem_wait_ld_regs(v);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            pw[c0 / 2 + i / 2] = pack2<F16>(__uint_as_float(v[i]) * f, __uint_as_float(v[i + 1]) * f);
+        }
+        quad_transpose<CW>(pw, q);
+        uint16_t* out = (KV && which == 0) ? p.out2 : p.out1;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rk = w.rt * kBM + quad * 32 + (lane & ~3) + k;
+          const int col = half * DH + q * 2 * CW;
+          if (rk < w.rows && col < p.d_out) {
+            const long long off = (zrow * w.rows + rk) * p.d_out + col;
+            store_chunk<CW>(out + off, pw + k * CW, false);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, P::TMEM_COLS);
+}
+
+template <int D, bool KV, bool F16>
+cudaError_t launch_attn_bwd(const BwdParams& bp, int grid, cudaStream_t stream) {
+  using P = BwdPlan<D, KV>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_done[dev]) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D, KV, F16>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(attn_bwd_kernel<D, KV, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             P::SMEM_LAUNCH);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  attn_bwd_kernel<D, KV, F16><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(bp);
+  return cudaGetLastError();
+}
+
+// Delta = rowsum(dO o O) over [rows, d] (one warp per row, fp32 sums).
+template <bool F16>
+__global__ void attn_bwd_delta_kernel(const uint16_t* o, const uint16_t* dout, float* delta,
+                                      long long rows, int d) {
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long r = wid; r < rows; r += nw) {
+    float acc = 0.f;
+    for (int c = lane; c < d; c += 32) {
+      const uint16_t a = o[r * d + c], b = dout[r * d + c];
+      float fa, fb;
+      if constexpr (F16) {
+        fa = __half2float(__ushort_as_half(a));
+        fb = __half2float(__ushort_as_half(b));
+      } else {
+        fa = __uint_as_float(static_cast<uint32_t>(a) << 16);
+        fb = __uint_as_float(static_cast<uint32_t>(b) << 16);
+      }
+      acc = fmaf(fa, fb, acc);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) delta[r] = acc;
+  }
+}
+
+}  // namespace attn

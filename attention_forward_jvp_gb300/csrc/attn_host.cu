@@ -13,7 +13,7 @@
 #include <mutex>
 
 #include "attn_jvp.h"
-#include "attn_kernel.cuh"
+#include "attn_bwd_kernel.cuh"
 #include "attn_plan.h"
 
 static_assert(attn::kPlanBM == attn::kBM && attn::kPlanBN == attn::kBN,
@@ -76,6 +76,14 @@ extern template cudaError_t launch_attn<256, 256, false, kBiasRing, false>(const
 extern template cudaError_t launch_attn<256, 256, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, true, true>(const BwdParams&, int, cudaStream_t);
 }
 
 namespace {
@@ -395,6 +403,118 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   return ATTN_OK;
 }
 
+// ------------------------------------------------------------- backward
+// One pass of the dQ kernel (kv = false) or of the dK / dV kernel.
+cudaError_t dispatch_bwd(int d, bool kv, bool f16, const attn::BwdParams& bp, int grid, cudaStream_t cs) {
+  if (d == 64) {
+    if (f16) return kv ? attn::launch_attn_bwd<64, true, true>(bp, grid, cs)
+                       : attn::launch_attn_bwd<64, false, true>(bp, grid, cs);
+    return kv ? attn::launch_attn_bwd<64, true, false>(bp, grid, cs)
+              : attn::launch_attn_bwd<64, false, false>(bp, grid, cs);
+  }
+  if (d == 128) {
+    if (f16) return kv ? attn::launch_attn_bwd<128, true, true>(bp, grid, cs)
+                       : attn::launch_attn_bwd<128, false, true>(bp, grid, cs);
+    return kv ? attn::launch_attn_bwd<128, true, false>(bp, grid, cs)
+              : attn::launch_attn_bwd<128, false, false>(bp, grid, cs);
+  }
+  return cudaErrorInvalidValue;
+}
+
+attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const void* v, const void* o,
+                    const void* dout, const float* lse, const int32_t* offsets, const attn_bias* bias,
+                    int causal, float sm_scale, void* dq, void* dk, void* dv, float* delta,
+                    void* stream, bool f16) {
+  if (s == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0 || s->M < 0 || s->N < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (offsets != nullptr) return ATTN_ERR_UNSUPPORTED;  // dense layouts only
+  if (bias != nullptr && (bias->bias != nullptr || bias->mask != nullptr)) return ATTN_ERR_UNSUPPORTED;
+  auto dim_ok = [](int d) { return d == 16 || d == 32 || d == 64 || d == 128; };
+  if (!dim_ok(s->Dqk) || s->Dv != s->Dqk) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isnan(sm_scale) && !(sm_scale > 0.f && std::isfinite(sm_scale)))
+    return ATTN_ERR_INVALID_ARG;
+  if (causal && s->M != s->N) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s->B) * s->H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  const int64_t BH = static_cast<int64_t>(s->B) * s->H;
+  if (BH == 0 || (s->M == 0 && s->N == 0)) return ATTN_OK;  // nothing to write
+  const bool rows_q = s->M > 0, rows_k = s->N > 0;
+  if (rows_q && (q == nullptr || o == nullptr || dout == nullptr || lse == nullptr || dq == nullptr ||
+                 delta == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  if (rows_k && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  for (const void* p : {q, o, dout, static_cast<const void*>(lse), static_cast<const void*>(dq),
+                        static_cast<const void*>(delta)})
+    if (rows_q && !aligned16(p)) return ATTN_ERR_MISALIGNED;
+  for (const void* p : {k, v, static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if (rows_k && !aligned16(p)) return ATTN_ERR_MISALIGNED;
+
+  DeviceState* ds = nullptr;
+  attn_status st = device_state(&ds);
+  if (st != ATTN_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const float scale = std::isnan(sm_scale) ? 1.0f / std::sqrt(static_cast<float>(s->Dqk)) : sm_scale;
+  const int D = s->Dqk <= 64 ? 64 : 128;  // 16 and 32 run zero-padded in the 64-wide kernels
+  const uint64_t d = static_cast<uint64_t>(s->Dqk), M = s->M, N = s->N, Z = static_cast<uint64_t>(BH);
+
+  // Delta = rowsum(dO o O)
+  if (rows_q) {
+    const long long rows = static_cast<long long>(BH) * s->M;
+    const long long want = (rows + 7) / 8;  // 8 warps (rows) per 256-thread block
+    const int blocks = static_cast<int>(want < 16LL * ds->num_sms ? want : 16LL * ds->num_sms);
+    if (f16)
+      attn::attn_bwd_delta_kernel<true><<<blocks, 256, 0, cs>>>(
+          static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows, s->Dv);
+    else
+      attn::attn_bwd_delta_kernel<false><<<blocks, 256, 0, cs>>>(
+          static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows, s->Dv);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1);
+  }
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool kv = pass == 1;
+    const int rows = kv ? s->N : s->M;
+    if (rows == 0) continue;
+    attn::BwdParams bp;
+    std::memset(&bp, 0, sizeof(bp));
+    bp.B = s->B;
+    bp.H = s->H;
+    bp.M = s->M;
+    bp.N = s->N;
+    bp.causal = causal ? 1 : 0;
+    bp.n_rt = (rows + attn::kBM - 1) / attn::kBM;
+    bp.scale_log2 = scale * attn::kLog2e;
+    bp.sm_scale = scale;
+    bp.lse = lse;
+    bp.delta = delta;
+    bp.out1 = static_cast<uint16_t*>(kv ? dk : dq);
+    bp.out2 = static_cast<uint16_t*>(kv ? dv : nullptr);
+    bp.d_out = s->Dqk;
+    bp.err = ds->scratch;
+    bp.timeout_ns = g_timeout_ns.load();
+    // the streamed side has no rows: its maps are never used, only valid
+    const bool other = kv ? rows_q : rows_k;
+    const uint64_t Ro = other ? (kv ? M : N) : static_cast<uint64_t>(rows);
+    const void* r1 = kv ? k : q;
+    const void* r2 = kv ? v : dout;
+    const void* t1 = other ? (kv ? q : k) : r1;
+    const void* t2 = other ? (kv ? dout : v) : r2;
+    bool ok = encode_map(&bp.tm_r1, r1, d, rows, Z, attn::kBM, f16);
+    ok = ok && encode_map(&bp.tm_r2, r2, d, rows, Z, attn::kBM, f16);
+    ok = ok && encode_map(&bp.tm_t1, t1, d, Ro, Z, 64, f16);
+    ok = ok && encode_map(&bp.tm_t2, t2, d, Ro, Z, 64, f16);
+    if (!ok) return ATTN_ERR_CUDA;
+    const int64_t units = BH * bp.n_rt;
+    if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    bp.num_units = static_cast<int>(units);
+    const int grid = static_cast<int>(units < ds->num_sms ? units : ds->num_sms);
+    if (dispatch_bwd(D, kv, f16, bp, grid, cs) != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1);
+  }
+  return ATTN_OK;
+}
+
 // ------------------------------------------------ allocation-free variant
 // Callers that may not allocate device memory (an embedding framework
 // that owns every allocation, a graph-building runtime that forbids
@@ -479,6 +599,22 @@ attn_status attn_fwd_f16(const attn_shape* shape, const void* q, const void* k, 
                          void* o, float* lse, void* stream) {
   return run(shape, q, k, v, nullptr, nullptr, nullptr, offsets, bias, causal, sm_scale, o,
              nullptr, lse, stream, false, nullptr, true);
+}
+
+attn_status attn_bwd(const attn_shape* shape, const void* q, const void* k, const void* v,
+                     const void* o, const void* dout, const float* lse, const int32_t* offsets,
+                     const attn_bias* bias, int causal, float sm_scale, void* dq, void* dk, void* dv,
+                     float* delta, void* stream) {
+  return run_bwd(shape, q, k, v, o, dout, lse, offsets, bias, causal, sm_scale, dq, dk, dv, delta,
+                 stream, false);
+}
+
+attn_status attn_bwd_f16(const attn_shape* shape, const void* q, const void* k, const void* v,
+                         const void* o, const void* dout, const float* lse, const int32_t* offsets,
+                         const attn_bias* bias, int causal, float sm_scale, void* dq, void* dk,
+                         void* dv, float* delta, void* stream) {
+  return run_bwd(shape, q, k, v, o, dout, lse, offsets, bias, causal, sm_scale, dq, dk, dv, delta,
+                 stream, true);
 }
 
 attn_status attn_sync_check(void* stream) {

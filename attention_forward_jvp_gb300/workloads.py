@@ -160,3 +160,43 @@ def min_hbm_bytes(w: Workload, inputs: dict, jvp: bool = True) -> int:
     if inputs.get("mask") is not None:
         n += inputs["mask"].numel()
     return n
+
+
+def make_bwd_inputs(w: Workload, seed: int = 0) -> dict:
+    """Inputs of the backward for dense workload ``w``: bf16 ``q, k, v``
+    and the output gradient ``do`` ``[B, H, M, Dv]``, drawn in that order
+    (``randn`` times ``input_std``; ``do`` at std 1), plus ``sm_scale`` and
+    ``causal``.  The forward's O and LSE are not drawn: each side computes
+    its own."""
+    assert not w.jagged, "the backward inputs are dense"
+    g = torch.Generator().manual_seed(seed)
+    return {
+        "workload": w, "sm_scale": w.scale, "causal": w.causal,
+        "q": _randn(g, (w.B, w.H, w.M, w.Dqk), w.input_std),
+        "k": _randn(g, (w.B, w.H, w.N, w.Dqk), w.input_std),
+        "v": _randn(g, (w.B, w.H, w.N, w.Dv), w.input_std),
+        "do": _randn(g, (w.B, w.H, w.M, w.Dv), 1.0),
+    }
+
+
+def flops_bwd(w: Workload) -> float:
+    """Algorithmic FLOPs of the backward: five matmuls per score element
+    (S = Q K^T, dP = dO V^T, dV = P^T dO, dQ = dS K, dK = dS^T Q), halved
+    for causal attention -- 2.5 times the forward, the rule of the
+    fused-attention tutorial's benchmark.  Kernels that recompute a product
+    do not get credit for it."""
+    f = 2.0 * (3 * w.Dqk + 2 * w.Dv) * float(w.B * w.H * w.M * w.N)
+    if w.causal:
+        f *= 0.5
+    return f
+
+
+def min_hbm_bytes_bwd(w: Workload) -> int:
+    """Bytes the backward must move at least once: q, k, v, o, do, lse read;
+    dq, dk, dv written (all 16-bit but lse); Delta written and read (fp32)."""
+    rows_q, rows_k = w.B * w.H * w.M, w.B * w.H * w.N
+    n = 2 * (rows_q * w.Dqk + rows_k * (w.Dqk + w.Dv) + 2 * rows_q * w.Dv)
+    n += 4 * rows_q                          # lse
+    n += 2 * (rows_q * w.Dqk + rows_k * (w.Dqk + w.Dv))
+    n += 2 * 4 * rows_q                      # Delta out + in
+    return n

@@ -172,6 +172,46 @@ attn_status attn_fwd_jvp_noalloc(const attn_shape* shape,
                                  int causal, float sm_scale,
                                  void* o, void* to, float* lse, void* stream);
 
+/* Backward of softmax attention: given the forward's inputs q, k, v, its
+ * output o and log-sum-exp lse (as attn_fwd writes them) and the gradient
+ * dout = dL/dO of a loss L, writes
+ *
+ *   Delta = rowsum(dout o O)             delta [B, H, M] fp32
+ *   dV    = P^T dout                     dv    [B, H, N, D]
+ *   dS    = P o (dout V^T - Delta)
+ *   dQ    = sm_scale dS K                dq    [B, H, M, D]
+ *   dK    = sm_scale dS^T Q              dk    [B, H, N, D]
+ *
+ * with P = exp(sm_scale Q K^T - LSE) over the valid set (0 elsewhere and
+ * on rows with LSE = -inf).  Sources: the Triton fused-attention tutorial's
+ * backward (_attn_bwd_preprocess for Delta, _attn_bwd_dkdv and _attn_bwd_dq
+ * recomputing P from the stored log-sum-exp); "flash_attention.py"
+ * (triton_flashattn) _attn_bwd_dkdv_inner / _attn_bwd_dq_inner.
+ *
+ * This version: dense layouts only (offsets must be NULL), no bias or mask
+ * (bias must be NULL or hold two NULL pointers), Dqk == Dv = D in
+ * {16, 32, 64, 128}; otherwise ATTN_ERR_UNSUPPORTED.  Causal requires
+ * M == N.  Layouts, element types (bf16; fp16 for attn_bwd_f16), pointer
+ * ownership and alignment, sm_scale and stream semantics are those of
+ * attn_fwd.  lse must be the forward's (natural log); a row's lse decides
+ * its P, so a stale or mismatched lse gives wrong gradients, not an error.
+ * delta is a caller-owned output that the two gradient kernels also read.
+ * Launches three kernels on `stream` (Delta, then dQ, then dK / dV); no
+ * atomics, each output element is written once.  M == 0 writes zero dK and
+ * dV; N == 0 writes zero dQ (and delta). */
+attn_status attn_bwd(const attn_shape* shape,
+                     const void* q, const void* k, const void* v,
+                     const void* o, const void* dout, const float* lse,
+                     const int32_t* offsets, const attn_bias* bias,
+                     int causal, float sm_scale,
+                     void* dq, void* dk, void* dv, float* delta, void* stream);
+attn_status attn_bwd_f16(const attn_shape* shape,
+                         const void* q, const void* k, const void* v,
+                         const void* o, const void* dout, const float* lse,
+                         const int32_t* offsets, const attn_bias* bias,
+                         int causal, float sm_scale,
+                         void* dq, void* dk, void* dv, float* delta, void* stream);
+
 /* Synchronises `stream`, then reads and clears the error word of the
  * current device.  Returns ATTN_ERR_TIMEOUT if a launch since the last
  * check reported a timed-out wait, ATTN_ERR_CUDA on a CUDA error, else

@@ -122,3 +122,33 @@ def test_timeout_setter_and_debug_hook_are_callable(L):
     L.attn_set_wait_timeout_ns(2_000_000_000)
     L.attn_debug_skip_first_load(0)
     assert L.attn_launch_count() >= 0
+
+
+def _bwd(L, shape, q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, offsets=None, bias=None,
+         causal=0, scale=float("nan"), dq=FAKE, dk=FAKE, dv=FAKE, delta=FAKE, f16=False):
+    fn = L.attn_bwd_f16 if f16 else L.attn_bwd
+    return fn(ctypes.byref(shape) if shape is not None else None, q, k, v, o, do, lse, offsets,
+              bias, causal, scale, dq, dk, dv, delta, None)
+
+
+def test_bwd_validation(L):
+    assert _bwd(L, None) == 1
+    assert _bwd(L, _shape(Dqk=64, Dv=128)) == 2          # Dqk != Dv
+    assert _bwd(L, _shape(Dqk=256, Dv=256)) == 2
+    assert _bwd(L, _shape(Dqk=8, Dv=8), f16=True) == 2
+    assert _bwd(L, _shape(T=100, msl=64), offsets=ctypes.c_void_p(0x20000)) == 2  # jagged
+    b = binding.AttnBias()
+    b.mask = 0x10000
+    assert _bwd(L, _shape(), bias=ctypes.byref(b)) == 2  # mask / bias
+    assert _bwd(L, _shape(M=128, N=256), causal=1) == 1
+    assert _bwd(L, _shape(), scale=-1.0) == 1
+    assert _bwd(L, _shape(M=-3)) == 1
+    assert _bwd(L, _shape(), lse=None) == 1
+    assert _bwd(L, _shape(), dv=None) == 1
+    assert _bwd(L, _shape(), delta=None) == 1
+    bad = ctypes.c_void_p(0x10008)
+    assert _bwd(L, _shape(), do=bad) == 3
+    assert _bwd(L, _shape(), dk=bad) == 3
+    # nothing to write: OK without touching a pointer or the GPU
+    assert _bwd(L, _shape(B=0)) == 0
+    assert _bwd(L, _shape(M=0, N=0), q=None, k=None, v=None) == 0

@@ -1,0 +1,142 @@
+"""GPU parity of the attention backward (dQ, dK, dV, Delta) through the C
+ABI against the float64 oracle (oracle.attention_bwd / head_bwd).
+
+The chain under test is the one a user runs: the library's forward writes
+O and LSE, the library's backward takes them with dO.  The oracle takes
+only q, k, v, dO from the seeded generator and recomputes everything.
+
+Tolerance (derived from the arithmetic; no published one covers the
+backward): P and dS enter the tensor-core products as 16-bit values
+(relative rounding 2^-9 for bf16) and O comes from the forward in bf16, the
+same error sources as the forward's tangent output, so each gradient G
+must satisfy max|G - G_oracle| <= 2e-2 * max(1, ||G_oracle||_inf) and
+Delta max|err| <= 1e-2 * max(1, ||Delta_oracle||_inf).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_forward_jvp_gb300 import binding, build
+from attention_forward_jvp_gb300.workloads import WORKLOADS, Workload, make_bwd_inputs
+
+pytestmark = pytest.mark.gpu
+
+G_TOL = 2e-2
+D_TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    binding.lib()
+
+
+def run_gpu_bwd(inp, f16=False):
+    cast = (lambda t: t.float().half()) if f16 else (lambda t: t)
+    q, k, v, do = (cast(inp[n]).cuda() for n in ("q", "k", "v", "do"))
+    kw = dict(causal=inp["causal"], sm_scale=inp["sm_scale"])
+    o, lse = binding.attn_fwd(q, k, v, **kw)
+    dq, dk, dv, delta = binding.attn_bwd(q, k, v, o, lse, do, **kw)
+    assert binding.sync_check() == 0
+    return tuple(t.float().cpu().numpy() for t in (dq, dk, dv, delta))
+
+
+def oracle_bwd(inp, f16=False):
+    cast = (lambda t: t.float().half()) if f16 else (lambda t: t)
+    return oracle.attention_bwd(*(cast(inp[n]) for n in ("q", "k", "v", "do")),
+                                causal=inp["causal"], sm_scale=inp["sm_scale"])
+
+
+def assert_grads_close(got, ref, what=""):
+    errs = []
+    for name, g, r in zip(("dQ", "dK", "dV"), got[:3], ref[:3]):
+        assert g.shape == r.shape, f"{what}: {name} shape {g.shape} vs {r.shape}"
+        assert np.isfinite(g).all(), f"{what}: non-finite {name}"
+        e = float(np.abs(g - r).max()) if g.size else 0.0
+        scale = max(1.0, float(np.abs(r).max()) if r.size else 0.0)
+        assert e <= G_TOL * scale, f"{what}: {name} err {e:.3e} (scale {scale:.2f})"
+        errs.append(e / scale)
+    g, r = got[3], ref[3]
+    e = float(np.abs(g - r).max()) if g.size else 0.0
+    scale = max(1.0, float(np.abs(r).max()) if r.size else 0.0)
+    assert e <= D_TOL * scale, f"{what}: Delta err {e:.3e} (scale {scale:.2f})"
+    return errs
+
+
+def _w(**kw):
+    base = dict(name="bwd", B=1, H=2, M=256, N=256, Dqk=64, Dv=64)
+    base.update(kw)
+    return Workload(**base)
+
+
+CASES = [
+    # name, workload
+    ("nc_d64", _w(M=384, N=384)),
+    ("causal_d64", _w(M=320, N=320, causal=True)),
+    ("nc_d128", _w(M=256, N=320, Dqk=128, Dv=128)),
+    ("causal_d128", _w(M=448, N=448, Dqk=128, Dv=128, causal=True)),
+    ("cross_ragged", _w(B=2, H=1, M=200, N=333)),
+    ("short_q", _w(M=1, N=515)),
+    ("short_k", _w(M=300, N=1)),
+    ("tiny_causal", _w(M=5, N=5, causal=True)),
+    ("d16", _w(M=200, N=260, Dqk=16, Dv=16)),
+    ("d32_causal", _w(M=257, N=257, Dqk=32, Dv=32, causal=True)),
+    ("scale_std2", _w(M=256, N=384, input_std=2.0, sm_scale=0.2)),
+]
+
+
+@pytest.mark.parametrize("name,w", CASES, ids=[c[0] for c in CASES])
+def test_bwd_parity(name, w):
+    inp = make_bwd_inputs(w, seed=7)
+    assert_grads_close(run_gpu_bwd(inp), oracle_bwd(inp), what=name)
+
+
+@pytest.mark.parametrize("name,w", [CASES[1], CASES[2]], ids=["causal_d64", "nc_d128"])
+def test_bwd_parity_f16(name, w):
+    inp = make_bwd_inputs(w, seed=8)
+    assert_grads_close(run_gpu_bwd(inp, f16=True), oracle_bwd(inp, f16=True), what=name + "_f16")
+
+
+def test_bwd_empty_sides():
+    # no queries: dK = dV = 0; no keys: dQ = 0
+    for M, N in ((0, 200), (130, 0)):
+        w = _w(M=M, N=N)
+        inp = make_bwd_inputs(w, seed=3)
+        q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+        o = torch.zeros_like(do)
+        lse = torch.full((w.B, w.H, w.M), float("-inf"), device="cuda")
+        dq, dk, dv, delta = (torch.full_like(t, 7.0) for t in (q, k, v, lse))
+        binding.attn_bwd(q, k, v, o, lse, do, out=(dq, dk, dv, delta))
+        assert binding.sync_check() == 0
+        assert torch.all(dq == 0) and torch.all(dk == 0) and torch.all(dv == 0)
+        assert torch.all(delta == 0)
+
+
+def test_bwd_unsupported_configs():
+    inp = make_bwd_inputs(_w(M=128, N=128, Dqk=64, Dv=128), seed=1)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    lse = torch.zeros(1, 2, 128, device="cuda")
+    with pytest.raises(binding.AttnError) as e:
+        binding.attn_bwd(q, k, v, do, lse, do)
+    assert e.value.status == 2  # Dqk != Dv
+
+
+def test_bwd_full_size_sampled_heads():
+    # the benchmark's shape (B2 H16 N4096 D128 causal); two heads checked
+    # whole against the oracle, and at every head the identity
+    # sum_j dK_j = 0 (adding one vector to every key leaves each row's
+    # softmax unchanged)
+    w = WORKLOADS["causal"]
+    inp = make_bwd_inputs(w, seed=0)
+    dq, dk, dv, delta = run_gpu_bwd(inp)
+    s = inp["sm_scale"]
+    for b, h in ((0, 0), (1, 15)):
+        r = oracle.head_bwd(*(inp[n][b, h].double().numpy() for n in ("q", "k", "v", "do")), s,
+                            causal=True)
+        assert_grads_close((dq[b, h], dk[b, h], dv[b, h], delta[b, h]), r, what=f"head {b},{h}")
+    col = np.abs(dk.astype(np.float64).sum(axis=2))
+    scale = np.abs(dk).max()
+    assert col.max() <= 2e-2 * max(1.0, scale) * 8, f"sum_j dK_j = {col.max():.3e}"
