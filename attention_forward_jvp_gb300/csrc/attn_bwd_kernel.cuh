@@ -62,23 +62,29 @@ struct BwdPlan {
   static constexpr int T_TILE = (D / 64) * T_SUB;
   static constexpr int RSET = 2 * R_TILE;            // R1 then R2
   static constexpr int T_STAGE = 2 * T_TILE;         // T1 then T2
-  static constexpr int BUDGET = 227 * 1024 - 1024;
+  static constexpr int BUDGET = 227 * 1024 - 4096;
   static constexpr int NS = (RSET + 4 * T_STAGE <= BUDGET) ? 4 : (RSET + 3 * T_STAGE <= BUDGET) ? 3 : 2;
+  // TMEM: score buffer b = [X (64 fp32: S or S^T) | Y (64 fp32: dP or dP^T)]
+  // at b * 128, three buffers where the accumulators leave room, else two;
+  // accumulators after them: dQ pass dQ (D); KV pass dV (D), dK (D)
+  static constexpr int SBUF = 2 * TN;
+  static constexpr int NACC = (KV ? 2 : 1) * D;
+  static constexpr int NSB = (3 * SBUF + NACC <= 512) ? 3 : 2;
+  static constexpr int COL_A = NSB * SBUF;
+  static constexpr int COLS_USED = COL_A + NACC;
+  static constexpr int TMEM_COLS = COLS_USED <= 256 ? 256 : 512;
   static constexpr int OFF_R = 0;
   static constexpr int OFF_T = RSET;
   static constexpr int OFF_BAR = OFF_T + NS * T_STAGE;
-  // barriers: r_full, r_empty, t_full[NS], t_empty[NS], s_full[2], p_full[2], drain
+  // barriers: r_full, r_empty, t_full[NS], t_empty[NS], s_full[NSB], p_full[NSB], drain
   static constexpr int B_RF = 0, B_RE = 1, B_TF = 2, B_TE = B_TF + NS, B_SF = B_TE + NS,
-                       B_PF = B_SF + 2, B_DRAIN = B_PF + 2, NBAR = B_DRAIN + 1;
+                       B_PF = B_SF + NSB, B_DRAIN = B_PF + NSB, NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16;
+  // KV pass: per elementwise warp, the current query tile's 32 column
+  // values of -LSE log2(e) then -Delta
+  static constexpr int OFF_COLV = (OFF_MISC + 16 + 15) / 16 * 16;
+  static constexpr int SMEM_BYTES = OFF_COLV + (KV ? 8 * 64 * 4 : 0);
   static constexpr int SMEM_LAUNCH = SMEM_BYTES > 120 * 1024 ? SMEM_BYTES : 120 * 1024;
-  // TMEM: buffer b = [X (64 fp32: S or S^T) | Y (64 fp32: dP or dP^T)] at
-  // b * 128; accumulators after them: dQ pass dQ (D); KV pass dV (D), dK (D)
-  static constexpr int SBUF = 2 * TN;
-  static constexpr int COL_A = 2 * SBUF;
-  static constexpr int COLS_USED = COL_A + (KV ? 2 : 1) * D;
-  static constexpr int TMEM_COLS = COLS_USED <= 256 ? 256 : 512;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
   static_assert(COLS_USED <= 512, "tensor memory plan exceeds 512 columns");
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       mbar_init(bar(P::B_TF + i), 1);
       mbar_init(bar(P::B_TE + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < P::NSB; ++i) {
       mbar_init(bar(P::B_SF + i), 1);
       mbar_init(bar(P::B_PF + i), 8);  // one arrival per elementwise warp
     }
@@ -221,12 +227,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, wait_bar(b, parity, W));
       };
-      // output chain(s) of tile t (ring stage ts), first tile of a unit: zero-init
-      auto issue_out = [&](uint32_t t, uint32_t ts, bool first) -> bool {
-        const uint32_t sb = t & 1u;
-        if (!wait_all(bar(P::B_PF + sb), (t >> 1) & 1u)) return false;
+      // Descriptor low words (the issue loop is instruction-bound: a score
+      // MMA lasts ~48 cycles, so each MMA gets one 32-bit add per operand):
+      // row operands and ring stage 0, K-major; ring stage 0 MN-major (the
+      // output chains' B, 64-column chunks T_SUB apart).
+      constexpr uint32_t kHi = sdesc_hi_sw128(1024);
+      const uint32_t lo_r1 = sdesc_lo(sbase + P::OFF_R, 16);
+      const uint32_t lo_r2 = lo_r1 + (P::R_TILE >> 4);
+      const uint32_t lo_t = sdesc_lo(sbase + P::OFF_T, 16);
+      const uint32_t lo_tmn = sdesc_lo(sbase + P::OFF_T, P::T_SUB);
+      // output chain(s) of tile t (its ring stage is t % NS); the first
+      // tile of a unit zero-initialises the accumulators
+      auto issue_out = [&](uint32_t t, bool first) -> bool {
+        const uint32_t sb = t % P::NSB;
+        if (!wait_all(bar(P::B_PF + sb), (t / P::NSB) & 1u)) return false;
         tc_fence_after();
-        const uint32_t sT = sbase + P::OFF_T + ts * P::T_STAGE;
+        const uint32_t ts = t % P::NS;
+        const uint32_t lm = lo_tmn + ts * (P::T_STAGE >> 4);
         // 16-bit operands over the Y columns: half h at Y + 32 h holds
         // P^T (KV pass) at +0 and dS at +16 (KV) / +0 (dQ pass), 8 packed
         // columns per 16 streamed rows
@@ -235,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           // dV += P^T dO
 #pragma unroll
           for (int kk = 0; kk < P::TN / 16; ++kk) {
-            const uint64_t db = sdesc_sw128(sT + P::T_TILE + kk * 2048, P::T_SUB, 1024);
+            const uint64_t db = sdesc_join(lm + ((P::T_TILE + kk * 2048) >> 4), kHi);
             if (leader)
               mma_ts(tmem + P::COL_A, aY + 32 * (kk >> 1) + 8 * (kk & 1), db, idesc_a,
                      (first && kk == 0) ? 0u : 1u);
@@ -247,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         const uint32_t ds_off = KV ? 16u : 0u;
 #pragma unroll
         for (int kk = 0; kk < P::TN / 16; ++kk) {
-          const uint64_t db = sdesc_sw128(sT + kk * 2048, P::T_SUB, 1024);
+          const uint64_t db = sdesc_join(lm + ((kk * 2048) >> 4), kHi);
           if (leader)
             mma_ts(acc, aY + 32 * (kk >> 1) + ds_off + 8 * (kk & 1), db, idesc_a,
                    (first && kk == 0) ? 0u : 1u);
@@ -257,7 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         __syncwarp();
         return true;
       };
-      uint32_t ruse = 0, tuse = 0, g = 0;
+      // Score chains run up to NSB - 1 tiles ahead of the output chains, so
+      // the tensor pipe has them queued while the elementwise warps work.
+      constexpr int kAhead = P::NSB - 1;
+      uint32_t ruse = 0, g = 0;
       bool ok = true;
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_at(rnd);
@@ -266,44 +286,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         if (w.nt == 0) continue;
         ok = wait_all(bar(P::B_RF), ruse & 1u);
         if (!ok) break;
-        const uint32_t sR1 = sbase + P::OFF_R, sR2 = sbase + P::OFF_R + P::R_TILE;
+        const uint32_t g0 = g;
         for (int j = 0; j < w.nt; ++j, ++g) {
-          const uint32_t ts = tuse % P::NS;
-          ok = wait_all(bar(P::B_TF + ts), (tuse / P::NS) & 1u);
+          const uint32_t ts = g % P::NS;
+          ok = wait_all(bar(P::B_TF + ts), (g / P::NS) & 1u);
           if (!ok) break;
-          const uint32_t sT = sbase + P::OFF_T + ts * P::T_STAGE;
-          const uint32_t dX = tmem + (g & 1u) * P::SBUF;
+          const uint32_t lt = lo_t + ts * (P::T_STAGE >> 4);
+          const uint32_t dX = tmem + (g % P::NSB) * P::SBUF;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk & 3) * 32;
-            const uint64_t da = sdesc_sw128(sR1 + (kk >> 2) * P::R_SUB + off, 16, 1024);
-            const uint64_t db = sdesc_sw128(sT + (kk >> 2) * P::T_SUB + off, 16, 1024);
-            if (leader) mma_ss(dX, da, db, idesc_s, kk > 0 ? 1u : 0u);
+            const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
+            const uint32_t ob = ((kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
+            if (leader) mma_ss(dX, sdesc_join(lo_r1 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
             __syncwarp();
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk & 3) * 32;
-            const uint64_t da = sdesc_sw128(sR2 + (kk >> 2) * P::R_SUB + off, 16, 1024);
-            const uint64_t db = sdesc_sw128(sT + P::T_TILE + (kk >> 2) * P::T_SUB + off, 16, 1024);
-            if (leader) mma_ss(dX + P::TN, da, db, idesc_s, kk > 0 ? 1u : 0u);
+            const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
+            const uint32_t ob = (P::T_TILE + (kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
+            if (leader)
+              mma_ss(dX + P::TN, sdesc_join(lo_r2 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
             __syncwarp();
           }
           if (leader) {
-            tc_commit(bar(P::B_SF + (g & 1u)));
+            tc_commit(bar(P::B_SF + g % P::NSB));
             // the unit's last score chain: the row operands are free once it
             // is done (the output chains never read them)
             if (j == w.nt - 1) tc_commit(bar(P::B_RE));
           }
           __syncwarp();
-          ++tuse;
-          if (j > 0) {
-            ok = issue_out(g - 1, (tuse - 2) % P::NS, j == 1);
+          if (j >= kAhead) {
+            ok = issue_out(g - kAhead, j == kAhead);
             if (!ok) break;
           }
         }
         if (!ok) break;
-        ok = issue_out(g - 1, (tuse - 1) % P::NS, w.nt == 1);
+        // the unit's remaining output chains
+        for (uint32_t t = (w.nt > kAhead ? g - kAhead : g0); ok && t < g; ++t) ok = issue_out(t, t == g0);
         ++ruse;
       }
       if (leader) {
@@ -320,6 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const int row = quad * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     constexpr float kLog2eF = 1.4426950408889634f;
+    // KV pass: this warp's 64-float slot of column terms
+    float* colv = reinterpret_cast<float*>(smem + P::OFF_COLV) + (KV ? (warp - 4) * 64 : 0);
     uint32_t g = 0, tuse = 0;
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
@@ -341,33 +362,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         }
         continue;
       }
-      // dQ pass: the row's LSE (log2 units) and Delta
-      float lse2_r = INFINITY, delta_r = 0.f;
-      if (!KV && row_ok) {
-        const float l = __ldg(p.lse + zrow * p.M + ri);
-        lse2_r = l == -INFINITY ? INFINITY : l * kLog2eF;  // empty row: P = 0
-        delta_r = __ldg(p.delta + zrow * p.M + ri);
-      }
-      for (int j = 0; j < w.nt; ++j, ++g, ++tuse) {
-        const uint32_t sb = g & 1u;
-        const int col0 = (w.t0 + j) * 64 + half * 32;  // first column (key or query) of this thread
-        float lse2_c[32], delta_c[32];
-        if (KV) {
-          // the 32 query columns' LSE and Delta (the same for every lane)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int qi = col0 + c;
-            float l = INFINITY, dd = 0.f;
-            if (qi < p.M) {
-              const float v = __ldg(p.lse + zrow * p.M + qi);
-              l = v == -INFINITY ? INFINITY : v * kLog2eF;
-              dd = __ldg(p.delta + zrow * p.M + qi);
-            }
-            lse2_c[c] = l;
-            delta_c[c] = dd;
-          }
+      // Per-row (dQ pass) or per-column (KV pass) terms of the exponent and
+      // of dS, pre-negated: nl = -LSE log2(e) and nd = -Delta, with
+      // nl = -inf for empty rows and padding rows / columns so that their P
+      // is exactly 0 without a test.
+      auto neg_terms = [&](int i, float& nl, float& nd) {
+        nl = -INFINITY;
+        nd = 0.f;
+        if (i < p.M) {
+          const float l = __ldg(p.lse + zrow * p.M + i);
+          nl = l == -INFINITY ? -INFINITY : -l * kLog2eF;
+          nd = -__ldg(p.delta + zrow * p.M + i);
         }
-        ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
+      };
+      float nl_r = -INFINITY, nd_r = 0.f;   // dQ pass: this row's terms
+      float nl_c = -INFINITY, nd_c = 0.f;   // KV pass: this lane's column of the next tile
+      if (!KV) neg_terms(ri, nl_r, nd_r);
+      else neg_terms((w.t0) * 64 + half * 32 + lane, nl_c, nd_c);
+      const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
+      for (int j = 0; j < w.nt; ++j, ++g, ++tuse) {
+        const uint32_t sb = g % P::NSB;
+        const int col0 = (w.t0 + j) * 64 + half * 32;  // first column (key or query) of this thread
+        if (KV) {
+          // publish this tile's column terms to the warp's slot, then fetch
+          // the next tile's (their latency hides behind this tile)
+          __syncwarp();
+          colv[lane] = nl_c;
+          colv[32 + lane] = nd_c;
+          __syncwarp();
+          if (j + 1 < w.nt) neg_terms(col0 + 64 + lane, nl_c, nd_c);
+        }
+        // valid columns [lo, hi) of this thread's 32 (the others get P = 0):
+        // dQ pass keys < N and, causal, <= the query; KV pass, causal,
+        // queries >= the key (queries >= M already have nl = -inf)
+        int lo = 0, hi = 32;
+        if (!KV) hi = (p.causal ? min(p.N, ri + 1) : p.N) - col0;
+        else if (p.causal) lo = ri - col0;
+        const bool full = lo <= 0 && hi >= 32;
+        // a sleeping wait: a spinning one would take issue slots from the
+        // MMA issuer on the same sub-partition
+        ok = __all_sync(0xffffffffu, wait_bar_sleep(bar(P::B_SF + sb), (g / P::NSB) & 1u, W));
         if (!ok) break;
         tc_fence_after();
         uint32_t xr[32], yr[32];
@@ -377,29 +411,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tmem_regs_ready(yr);
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cc = c + e;
-            const int col = col0 + cc;
-            bool keep;
-            float l2, dl;
-            if (!KV) {  // row = query ri, column = key col
-              keep = col < p.N && (!p.causal || col <= ri);
-              l2 = lse2_r;
-              dl = delta_r;
-            } else {    // row = key ri, column = query col
-              keep = col < p.M && (!p.causal || ri <= col);
-              l2 = lse2_c[cc];
-              dl = delta_c[cc];
-            }
-            const float pe = keep ? ex2(fmaf(__uint_as_float(xr[cc]), p.scale_log2, -l2)) : 0.f;
-            pv[e] = pe;
-            dv[e] = pe * (__uint_as_float(yr[cc]) - dl);
+        for (int c = 0; c < 32; c += 4) {
+          float4 nl4, nd4;
+          if (KV) {
+            nl4 = *reinterpret_cast<const float4*>(colv + c);
+            nd4 = *reinterpret_cast<const float4*>(colv + 32 + c);
+          } else {
+            nl4 = make_float4(nl_r, nl_r, nl_r, nl_r);
+            nd4 = make_float4(nd_r, nd_r, nd_r, nd_r);
           }
-          pk[c / 2] = pack2<F16>(pv[0], pv[1]);
-          dk[c / 2] = pack2<F16>(dv[0], dv[1]);
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int cc = c + e;
+            const float nla = e == 0 ? nl4.x : nl4.z, nlb = e == 0 ? nl4.y : nl4.w;
+            const float nda = e == 0 ? nd4.x : nd4.z, ndb = e == 0 ? nd4.y : nd4.w;
+            // x = S s log2(e) - LSE log2(e);  P = 2^x;  dS = P (dP - Delta)
+            const uint64_t x = f2_fma(f2_make(__uint_as_float(xr[cc]), __uint_as_float(xr[cc + 1])), sc2,
+                                      f2_make(nla, nlb));
+            float x0, x1;
+            f2_split(x, x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if (!full) {
+              p0 = (cc >= lo && cc < hi) ? p0 : 0.f;
+              p1 = (cc + 1 >= lo && cc + 1 < hi) ? p1 : 0.f;
+            }
+            const uint64_t d = f2_add(f2_make(__uint_as_float(yr[cc]), __uint_as_float(yr[cc + 1])),
+                                      f2_make(nda, ndb));
+            float d0, d1;
+            f2_split(f2_mul(f2_make(p0, p1), d), d0, d1);
+            pk[cc / 2] = pack2<F16>(p0, p1);
+            dk[cc / 2] = pack2<F16>(d0, d1);
+          }
         }
         const uint32_t yb = tl + sb * P::SBUF + P::TN + half * 32;
         if (KV) {
@@ -419,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       // (their commit is the last tile's ring-stage release; the phase after
       // it needs a tile this thread has not processed yet)
       const uint32_t tl_last = tuse - 1;
-      ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_TE + tl_last % P::NS), (tl_last / P::NS) & 1u, W));
+      ok = __all_sync(0xffffffffu, wait_bar_sleep(bar(P::B_TE + tl_last % P::NS), (tl_last / P::NS) & 1u, W));
       if (!ok) break;
       tc_fence_after();
       constexpr int DH = D / 2;     // columns per thread

@@ -166,6 +166,23 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor as two 32-bit halves.  The low word holds the start
+// address / 16 (bits 0-13) and the leading byte offset / 16 (bits 16-29);
+// the high word the stride byte offset / 16, the version bit and the
+// swizzle mode.  For operands a few KB apart only the low word differs, by
+// (address difference) / 16 -- no carry leaves the address field while the
+// address stays below 256 KB -- so an issue loop can keep one low word per
+// buffer and add a constant per MMA instead of rebuilding 64-bit values.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // Instruction descriptor, kind::f16: A and B both bf16 (f16 = false) or
 // both fp16, fp32 D, dense.  A is K-major; B is K-major or MN-major.
 __host__ __device__ constexpr uint32_t idesc_16(int m, int n, bool b_mn_major, bool f16) {
