@@ -719,29 +719,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       return v_seen == t || wait_all(bar(P::B_VF + t % P::NV), (t / P::NV) & 1u);
     };
 
+    // Descriptor low words of Q buffer 0, K stage 0 (K-major) and V stage 0
+    // (MN-major, 64-column chunks V_SUB apart); a buffer / stage / K step is
+    // a constant added to the low word (see sdesc_lo), which keeps the issue
+    // loop to one add per operand per MMA.
+    constexpr uint32_t kHi = sdesc_hi_sw128(1024);
+    const uint32_t lo_q = sdesc_lo(sbase + P::OFF_Q, 16);
+    const uint32_t lo_k = sdesc_lo(sbase + P::OFF_K, 16);
+    const uint32_t lo_v = sdesc_lo(sbase + P::OFF_V, P::V_SUB);
+
     // [S | Q tK^T] = Q [K ; tK]^T, tS += tQ K^T for tile t; `mid` runs after
     // the first half of the first chain.
     auto issue_s = [&](uint32_t t, uint32_t qb, auto&& mid) -> bool {
       if (!wait_k(t)) return false;
-      const uint32_t sQ = sbase + qb * P::QSET + P::OFF_Q, sTQ = sbase + qb * P::QSET + P::OFF_TQ;
+      const uint32_t lq = lo_q + qb * (P::QSET >> 4);
       const uint32_t dS = tmem + (t & 1u) * P::SBUF;
-      const uint32_t sK = sbase + P::OFF_K + (t % P::NK) * P::K_STAGE;
+      const uint32_t lk = lo_k + (t % P::NK) * (P::K_STAGE >> 4);
 #pragma unroll
       for (int kk = 0; kk < DQK / 16; ++kk) {
-        const uint32_t off = (kk & 3) * 32;
-        const uint64_t dq = sdesc_sw128(sQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
-        const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
-        if (leader) mma_ss(dS, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
+        const uint32_t oq = ((kk >> 2) * P::Q_SUB + (kk & 3) * 32) >> 4;
+        const uint32_t ok_ = ((kk >> 2) * P::K_GROUP + (kk & 3) * 32) >> 4;
+        if (leader) mma_ss(dS, sdesc_join(lq + oq, kHi), sdesc_join(lk + ok_, kHi), idesc_s, kk > 0 ? 1u : 0u);
         __syncwarp();
         if (kk == DQK / 32 - 1) mid();
       }
       if (JVP) {
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          const uint64_t dtq = sdesc_sw128(sTQ + (kk >> 2) * P::Q_SUB + off, 16, 1024);
-          const uint64_t dk = sdesc_sw128(sK + (kk >> 2) * P::K_GROUP + off, 16, 1024);
-          if (leader) mma_ss(dS + kBN, dtq, dk, idesc_t, 1u);
+          const uint32_t oq = (P::OFF_TQ - P::OFF_Q + (kk >> 2) * P::Q_SUB + (kk & 3) * 32) >> 4;
+          const uint32_t ok_ = ((kk >> 2) * P::K_GROUP + (kk & 3) * 32) >> 4;
+          if (leader) mma_ss(dS + kBN, sdesc_join(lq + oq, kHi), sdesc_join(lk + ok_, kHi), idesc_t, 1u);
           __syncwarp();
         }
       }
@@ -762,13 +769,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         return false;
       tc_fence_after();
       const uint32_t colo = P::COL_O + (un % P::NOB) * P::OBUF;
-      const uint32_t sV = sbase + P::OFF_V + (t % P::NV) * P::V_STAGE;
+      const uint32_t lv = lo_v + (t % P::NV) * (P::V_STAGE >> 4);
       // keys [16 kk, 16 kk + 16): P at column base + 32 (kk / 2) + 8 (kk % 2),
       // H 16 columns further (the layout the softmax halves write)
       const uint32_t aP = tmem + sb * P::SBUF + kBN;
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk) {
-        const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
+        const uint64_t dv = sdesc_join(lv + ((kk * 2048) >> 4), kHi);
         if (leader)
           mma_ts(tmem + colo, aP + 32 * (kk >> 1) + 8 * (kk & 1), dv, idesc_o,
                  (first && kk == 0) ? 0u : 1u);
@@ -778,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (JVP) {
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t dv = sdesc_sw128(sV + kk * 2048, P::V_SUB, 1024);
+          const uint64_t dv = sdesc_join(lv + ((kk * 2048) >> 4), kHi);
           if (leader) mma_ts(tmem + colo + DV, aP + 32 * (kk >> 1) + 16 + 8 * (kk & 1), dv, idesc_h, 1u);
           __syncwarp();
         }
