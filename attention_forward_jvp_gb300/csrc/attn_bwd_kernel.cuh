@@ -238,10 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const uint32_t lo_tmn = sdesc_lo(sbase + P::OFF_T, P::T_SUB);
       // output chain(s) of tile t (its ring stage is t % NS); the first
       // tile of a unit zero-initialises the accumulators
-      auto issue_out = [&](uint32_t t, bool first) -> bool {
+      // (`waited`: the caller has already waited for its P / dS)
+      auto issue_out = [&](uint32_t t, bool first, bool waited) -> bool {
         const uint32_t sb = t % P::NSB;
-        if (!wait_all(bar(P::B_PF + sb), (t / P::NSB) & 1u)) return false;
-        tc_fence_after();
+        if (!waited) {
+          if (!wait_all(bar(P::B_PF + sb), (t / P::NSB) & 1u)) return false;
+          tc_fence_after();
+        }
         const uint32_t ts = t % P::NS;
         const uint32_t lm = lo_tmn + ts * (P::T_STAGE >> 4);
         // 16-bit operands over the Y columns: half h at Y + 32 h holds
@@ -276,7 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       };
       // Score chains run up to NSB - 1 tiles ahead of the output chains, so
       // the tensor pipe has them queued while the elementwise warps work.
+      // With two tiles of lookahead the issuer waits once per tile -- for the
+      // tile's operands and for the P / dS of the output chain it issues
+      // next (long since written) -- then issues the score chains and that
+      // output chain as one batch: the tensor pipe's instruction queue is
+      // short, and every pause of the issuer between MMAs leaves it idle.
+      // With one tile of lookahead that P / dS is still being computed when
+      // the next score chains can go, so those go first.
       constexpr int kAhead = P::NSB - 1;
+      constexpr bool kHoist = kAhead >= 2;
       uint32_t ruse = 0, g = 0;
       bool ok = true;
       for (int rnd = 0; ok; ++rnd) {
@@ -290,6 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         for (int j = 0; j < w.nt; ++j, ++g) {
           const uint32_t ts = g % P::NS;
           ok = wait_all(bar(P::B_TF + ts), (g / P::NS) & 1u);
+          if (kHoist && ok && j >= kAhead) {
+            const uint32_t t = g - kAhead;
+            ok = wait_all(bar(P::B_PF + t % P::NSB), (t / P::NSB) & 1u);
+            tc_fence_after();
+          }
           if (!ok) break;
           const uint32_t lt = lo_t + ts * (P::T_STAGE >> 4);
           const uint32_t dX = tmem + (g % P::NSB) * P::SBUF;
@@ -316,13 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           }
           __syncwarp();
           if (j >= kAhead) {
-            ok = issue_out(g - kAhead, j == kAhead);
+            ok = issue_out(g - kAhead, j == kAhead, kHoist);
             if (!ok) break;
           }
         }
         if (!ok) break;
         // the unit's remaining output chains
-        for (uint32_t t = (w.nt > kAhead ? g - kAhead : g0); ok && t < g; ++t) ok = issue_out(t, t == g0);
+        for (uint32_t t = (w.nt > kAhead ? g - kAhead : g0); ok && t < g; ++t) ok = issue_out(t, t == g0, false);
         ++ruse;
       }
       if (leader) {
