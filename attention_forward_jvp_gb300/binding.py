@@ -28,6 +28,7 @@ EXPORTS = (
     "attn_fwd_jvp_noalloc",
     "attn_bwd",
     "attn_bwd_f16",
+    "attn_bwd_stages",
     "attn_sync_check",
     "attn_status_string",
     "attn_launch_count",
@@ -86,6 +87,10 @@ def lib() -> ctypes.CDLL:
                            ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp, vp, vp]
     L.attn_bwd_f16.restype = i32
     L.attn_bwd_f16.argtypes = L.attn_bwd.argtypes
+    L.attn_bwd_stages.restype = i32
+    L.attn_bwd_stages.argtypes = [ctypes.POINTER(AttnShape), vp, vp, vp, vp, vp, vp, vp,
+                                  ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp, vp, i32,
+                                  ctypes.c_uint, vp]
     L.attn_sync_check.restype = i32
     L.attn_sync_check.argtypes = [vp]
     L.attn_status_string.restype = ctypes.c_char_p
@@ -272,12 +277,16 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: Optional[float] = None,
     return o, lse
 
 
+BWD_DELTA, BWD_DQ, BWD_DKDV, BWD_ALL = 1, 2, 4, 7
+
+
 def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float] = None,
-             out=None):
+             out=None, stages: int = BWD_ALL):
     """Attention backward (dense, no bias / mask, Dqk == Dv).  Takes the
     forward's inputs, its output ``o`` and log-sum-exp ``lse`` and the
     gradient ``do`` of O; returns (dq, dk, dv, delta), delta = rowsum(do o o)
-    in float32."""
+    in float32.  ``stages`` (an OR of BWD_DELTA, BWD_DQ, BWD_DKDV) runs a
+    subset of the three launches; the others leave their outputs as given."""
     if q.device.type == "cpu":
         return _host_call(attn_bwd, (q, k, v, o, lse, do), dict(causal=causal, sm_scale=sm_scale),
                           n_out=4)
@@ -295,10 +304,16 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float
     else:
         dq, dk, dv, delta = out
     stream = torch.cuda.current_stream(dev).cuda_stream
-    fn = lib().attn_bwd_f16 if dt == torch.float16 else lib().attn_bwd
-    st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), None, None,
-            1 if causal else 0, _scale(sm_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
-            ctypes.c_void_p(stream))
+    if stages == BWD_ALL:
+        fn = lib().attn_bwd_f16 if dt == torch.float16 else lib().attn_bwd
+        st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), None, None,
+                1 if causal else 0, _scale(sm_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
+                ctypes.c_void_p(stream))
+    else:
+        st = lib().attn_bwd_stages(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do),
+                                   _ptr(lse), None, None, 1 if causal else 0, _scale(sm_scale),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
+                                   1 if dt == torch.float16 else 0, int(stages), ctypes.c_void_p(stream))
     _check(st)
     return dq, dk, dv, delta
 

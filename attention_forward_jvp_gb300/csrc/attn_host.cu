@@ -424,8 +424,9 @@ cudaError_t dispatch_bwd(int d, bool kv, bool f16, const attn::BwdParams& bp, in
 attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const void* v, const void* o,
                     const void* dout, const float* lse, const int32_t* offsets, const attn_bias* bias,
                     int causal, float sm_scale, void* dq, void* dk, void* dv, float* delta,
-                    void* stream, bool f16) {
+                    void* stream, bool f16, unsigned stages) {
   if (s == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (stages == 0 || (stages & ~static_cast<unsigned>(ATTN_BWD_ALL)) != 0) return ATTN_ERR_INVALID_ARG;
   if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0 || s->M < 0 || s->N < 0)
     return ATTN_ERR_INVALID_ARG;
   if (offsets != nullptr) return ATTN_ERR_UNSUPPORTED;  // dense layouts only
@@ -459,7 +460,7 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
   const uint64_t d = static_cast<uint64_t>(s->Dqk), M = s->M, N = s->N, Z = static_cast<uint64_t>(BH);
 
   // Delta = rowsum(dO o O)
-  if (rows_q) {
+  if (rows_q && (stages & ATTN_BWD_DELTA)) {
     const long long rows = static_cast<long long>(BH) * s->M;
     const long long want = (rows + 7) / 8;  // 8 warps (rows) per 256-thread block
     const int blocks = static_cast<int>(want < 16LL * ds->num_sms ? want : 16LL * ds->num_sms);
@@ -475,7 +476,7 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
   for (int pass = 0; pass < 2; ++pass) {
     const bool kv = pass == 1;
     const int rows = kv ? s->N : s->M;
-    if (rows == 0) continue;
+    if (rows == 0 || !(stages & (kv ? ATTN_BWD_DKDV : ATTN_BWD_DQ))) continue;
     attn::BwdParams bp;
     std::memset(&bp, 0, sizeof(bp));
     bp.B = s->B;
@@ -606,7 +607,15 @@ attn_status attn_bwd(const attn_shape* shape, const void* q, const void* k, cons
                      const attn_bias* bias, int causal, float sm_scale, void* dq, void* dk, void* dv,
                      float* delta, void* stream) {
   return run_bwd(shape, q, k, v, o, dout, lse, offsets, bias, causal, sm_scale, dq, dk, dv, delta,
-                 stream, false);
+                 stream, false, ATTN_BWD_ALL);
+}
+
+attn_status attn_bwd_stages(const attn_shape* shape, const void* q, const void* k, const void* v,
+                            const void* o, const void* dout, const float* lse, const int32_t* offsets,
+                            const attn_bias* bias, int causal, float sm_scale, void* dq, void* dk,
+                            void* dv, float* delta, int f16, unsigned stages, void* stream) {
+  return run_bwd(shape, q, k, v, o, dout, lse, offsets, bias, causal, sm_scale, dq, dk, dv, delta,
+                 stream, f16 != 0, stages);
 }
 
 attn_status attn_bwd_f16(const attn_shape* shape, const void* q, const void* k, const void* v,
@@ -614,7 +623,7 @@ attn_status attn_bwd_f16(const attn_shape* shape, const void* q, const void* k, 
                          const attn_bias* bias, int causal, float sm_scale, void* dq, void* dk,
                          void* dv, float* delta, void* stream) {
   return run_bwd(shape, q, k, v, o, dout, lse, offsets, bias, causal, sm_scale, dq, dk, dv, delta,
-                 stream, true);
+                 stream, true, ATTN_BWD_ALL);
 }
 
 attn_status attn_sync_check(void* stream) {

@@ -2,7 +2,7 @@
 """Benchmark: attention forward + JVP TFLOP/s on one GB300 (per rank).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload causal|noncausal|jagged|bias_mask|tiny]
+                  [--workload causal|noncausal|jagged|bias_mask|tiny] [--op fwd_jvp|bwd]
 
 A step is one fused forward + JVP pass (one launch of the library's kernel)
 over the workload's synthetic inputs, already resident in HBM.  FLOPs are
@@ -14,6 +14,13 @@ is bracketed by barriers and the slowest rank's time is used.
 
 --impl reference times the float64 CPU oracle on the host cores (rank 0
 only) on a bounded sample of the same workload: each step is one head.
+
+--op bwd measures the attention backward instead (dense workloads): a step
+is one backward -- the Delta launch, the dQ pass and the dK / dV pass --
+given the forward's O and LSE (computed before the timed region).  FLOPs
+are the standard five matmuls per score element (S, dP, dV, dQ, dK), halved
+for causal attention; the kernels recompute S and dP in both passes, which
+earns no credit.
 """
 from __future__ import annotations
 
@@ -32,9 +39,11 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from attention_forward_jvp_gb300.workloads import WORKLOADS, flops_fwd_jvp, make_inputs, min_hbm_bytes  # noqa: E402
+from attention_forward_jvp_gb300.workloads import (WORKLOADS, flops_bwd, flops_fwd_jvp, make_bwd_inputs,  # noqa: E402
+                                                   make_inputs, min_hbm_bytes, min_hbm_bytes_bwd)
 
 METRIC = "attn fwd+JVP TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 tensor peak"
+METRIC_BWD = "attn backward (dQ, dK, dV) TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 tensor peak"
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 10**6  # GB300 L2
 
@@ -412,6 +421,163 @@ def run_ours(args, w, world, rank, local):
     return 0
 
 
+# --------------------------------------------------------------- backward
+def oracle_sample_bwd(w, inp, n_units: int, start: int = 0):
+    """The backward oracle on ``n_units`` whole (b, h) heads.  Returns
+    (seconds, algorithmic flops of the sample)."""
+    import oracle
+    BH = w.B * w.H
+    t0 = time.perf_counter()
+    for i in range(n_units):
+        b, h = divmod((start + i) % BH, w.H)
+        oracle.head_bwd(*(oracle.to_f64(inp[n][b, h]) for n in ("q", "k", "v", "do")), inp["sm_scale"],
+                        causal=w.causal)
+    dt = time.perf_counter() - t0
+    return dt, flops_bwd(w) / BH * n_units
+
+
+def run_reference_bwd(args, w, world, rank):
+    if rank != 0:
+        return 0
+    inp = make_bwd_inputs(w, seed=0)
+    for i in range(args.warmup):
+        oracle_sample_bwd(w, inp, 1, start=i)
+    tot = fl = 0.0
+    for i in range(args.steps):
+        dt, f1 = oracle_sample_bwd(w, inp, 1, start=args.warmup + i)
+        tot += dt
+        fl = f1
+    value = fl * args.steps / tot / 1e12
+    desc = (f"each step: one of {w.B * w.H} (batch, head) pairs of the {w.name} workload, float64 NumPy "
+            "(the oracle forms the full score matrix even when causal)")
+    line = {
+        "impl": "reference", "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": describe(w).replace("fwd+JVP", "backward"),
+                                        "sample_per_step": "one head"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_bwd(args, w, world, rank, local):
+    from attention_forward_jvp_gb300 import binding
+    from attention_forward_jvp_gb300 import build as _b
+
+    if w.jagged or w.bias or w.mask_keep is not None or w.Dqk != w.Dv:
+        raise SystemExit(f"--op bwd runs dense workloads without bias / mask and Dqk == Dv ({w.name} is not)")
+    if not os.path.exists(_b.LIB_PATH):
+        _b.build()
+    binding.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = make_bwd_inputs(w, seed=0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    kw = dict(causal=w.causal, sm_scale=inp["sm_scale"])
+    o, lse = binding.attn_fwd(q, k, v, **kw)
+    out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(lse))
+    flops = flops_bwd(w)
+    elem = float(w.B * w.H * w.M * w.N) * (0.5 if w.causal else 1.0)
+    flops_dkdv = 4.0 * (w.Dqk + w.Dv) * elem   # S^T, dP^T, dV, dK
+    stream = torch.cuda.current_stream(dev)
+    stages = (binding.BWD_DELTA, binding.BWD_DQ, binding.BWD_DKDV)
+
+    flush = min_hbm_bytes_bwd(w) < 2 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            binding.attn_bwd(q, k, v, o, lse, do, out=out, **kw)
+        st = binding.sync_check(stream)
+        if st != 0:
+            raise RuntimeError(f"device error during warm-up: {binding.status_string(st)}")
+        barrier(world)
+        torch.cuda.synchronize()
+        n0 = binding.launch_count()
+        clk.mark("timed")
+        for i in range(args.steps):
+            if flush:
+                flush_buf.fill_(float(i))
+            ev[i][0].record(stream)
+            for j, sg in enumerate(stages):
+                binding.attn_bwd(q, k, v, o, lse, do, out=out, stages=sg, **kw)
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize()
+        clk.mark("after")
+        barrier(world)
+        launches = binding.launch_count() - n0
+    st = binding.sync_check(stream)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {binding.status_string(st)}")
+    per = [sum(e[j].elapsed_time(e[j + 1]) for e in ev) / args.steps for j in range(3)]
+    ms = sum(per)
+    ms_max = max_over_ranks(ms, world)
+    value = world * flops / (ms_max * 1e-3) / 1e12
+
+    # end to end through the public API with pinned host buffers
+    hin = [t.cpu().pin_memory() for t in (q, k, v, o, lse, do)]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    e2e_steps = max(1, min(args.steps, 10))
+    hout = binding.attn_bwd(*hin, **kw)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        hout = binding.attn_bwd(*hin, **kw)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+    e2e_val = world * flops / e2e_s / 1e12
+
+    if rank != 0:
+        return 0
+    pk, pk_kind = peaks()
+    peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    achieved = flops_dkdv / (per[2] * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None,
+            "kernel": "dK/dV pass (attn_bwd_kernel<D, KV=true>): S^T, dP^T, dV, dK",
+            "peak_kind": f"{pk_kind} bf16 burst (kernel timed alone)",
+            "stage_ms": {"delta": per[0], "dq": per[1], "dkdv": per[2]},
+            "stage_tflops": {"dq": 2.0 * (2 * w.Dqk + w.Dv) * elem / (per[1] * 1e-3) / 1e12,
+                             "dkdv": achieved},
+            "delta_gbs": 2.0 * 2 * w.B * w.H * w.M * w.Dv / (per[0] * 1e-3) / 1e9}
+    cpu = None
+    if world == 1 and not args.skip_cpu_baseline:
+        dt = fl = 0.0
+        n = 0
+        while n < w.B * w.H and (n == 0 or dt < args.cpu_seconds):
+            d1, f1 = oracle_sample_bwd(w, inp, 1, start=n)
+            dt += d1
+            fl += f1
+            n += 1
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n} of {w.B * w.H} (batch, head) pairs of the {w.name} workload, float64 NumPy",
+               "seconds": dt}
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": describe(w).replace("fwd+JVP", "backward"), "flops_per_step": flops,
+                   "l2": ("L2 flushed before each step (%d MB written)" % (2 * L2_BYTES // 10**6)
+                          if flush else "inputs larger than L2, no flush"),
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": value / world / peak,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "kernel_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,11 +588,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="approximate seconds of oracle work in the CPU-baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="fwd_jvp", choices=["fwd_jvp", "bwd"],
+                    help="fwd_jvp: the fused forward + JVP (default); bwd: the backward")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]
     world, rank, local = dist_setup(args.impl)
-    if args.impl == "reference":
+    if args.op == "bwd":
+        rc = (run_reference_bwd(args, w, world, rank) if args.impl == "reference"
+              else run_ours_bwd(args, w, world, rank, local))
+    elif args.impl == "reference":
         rc = run_reference(args, w, world, rank)
     else:
         rc = run_ours(args, w, world, rank, local)

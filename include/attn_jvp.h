@@ -212,6 +212,28 @@ attn_status attn_bwd_f16(const attn_shape* shape,
                          int causal, float sm_scale,
                          void* dq, void* dk, void* dv, float* delta, void* stream);
 
+/* The launches of attn_bwd / attn_bwd_f16, selected by `stages` (a nonzero
+ * OR of the flags below; other bits: ATTN_ERR_INVALID_ARG): Delta; the dQ
+ * pass (reads delta); the dK / dV pass (reads delta).  Given delta the two
+ * gradient passes are independent, so a caller may run them on different
+ * streams, or time them one by one.  f16 nonzero selects fp16 storage.
+ * Arguments, validation (every pointer of attn_bwd is still required),
+ * layouts and results are those of attn_bwd; a stage writes only its own
+ * outputs. */
+enum {
+  ATTN_BWD_DELTA = 1,
+  ATTN_BWD_DQ = 2,
+  ATTN_BWD_DKDV = 4,
+  ATTN_BWD_ALL = 7
+};
+attn_status attn_bwd_stages(const attn_shape* shape,
+                            const void* q, const void* k, const void* v,
+                            const void* o, const void* dout, const float* lse,
+                            const int32_t* offsets, const attn_bias* bias,
+                            int causal, float sm_scale,
+                            void* dq, void* dk, void* dv, float* delta,
+                            int f16, unsigned stages, void* stream);
+
 /* Synchronises `stream`, then reads and clears the error word of the
  * current device.  Returns ATTN_ERR_TIMEOUT if a launch since the last
  * check reported a timed-out wait, ATTN_ERR_CUDA on a CUDA error, else

@@ -152,3 +152,14 @@ def test_bwd_validation(L):
     # nothing to write: OK without touching a pointer or the GPU
     assert _bwd(L, _shape(B=0)) == 0
     assert _bwd(L, _shape(M=0, N=0), q=None, k=None, v=None) == 0
+
+
+def test_bwd_stages_validation(L):
+    def st(stages, shape=None):
+        s = shape or _shape()
+        return L.attn_bwd_stages(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 0,
+                                 float("nan"), FAKE, FAKE, FAKE, FAKE, 0, stages, None)
+    assert st(0) == 1            # no stage selected
+    assert st(8) == 1            # unknown stage bit
+    assert st(7, _shape(B=0)) == 0
+    assert st(2, _shape(Dqk=64, Dv=128)) == 2

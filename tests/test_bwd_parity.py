@@ -140,3 +140,19 @@ def test_bwd_full_size_sampled_heads():
     col = np.abs(dk.astype(np.float64).sum(axis=2))
     scale = np.abs(dk).max()
     assert col.max() <= 2e-2 * max(1.0, scale) * 8, f"sum_j dK_j = {col.max():.3e}"
+
+
+def test_bwd_stages_match_one_call():
+    # Delta, the dQ pass and the dK / dV pass launched one by one give
+    # bitwise the results of one attn_bwd call
+    inp = make_bwd_inputs(_w(M=300, N=300, causal=True), seed=11)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    kw = dict(causal=True, sm_scale=inp["sm_scale"])
+    o, lse = binding.attn_fwd(q, k, v, **kw)
+    ref = binding.attn_bwd(q, k, v, o, lse, do, **kw)
+    out = tuple(torch.full_like(t, 3.0) for t in ref)
+    for sg in (binding.BWD_DELTA, binding.BWD_DKDV, binding.BWD_DQ):
+        binding.attn_bwd(q, k, v, o, lse, do, out=out, stages=sg, **kw)
+    assert binding.sync_check() == 0
+    for a, b in zip(ref, out):
+        assert torch.equal(a, b)
