@@ -281,23 +281,29 @@ BWD_DELTA, BWD_DQ, BWD_DKDV, BWD_ALL = 1, 2, 4, 7
 
 
 def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float] = None,
+             offsets: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
              out=None, stages: int = BWD_ALL):
-    """Attention backward (dense, no bias / mask, Dqk == Dv).  Takes the
-    forward's inputs, its output ``o`` and log-sum-exp ``lse`` and the
-    gradient ``do`` of O; returns (dq, dk, dv, delta), delta = rowsum(do o o)
-    in float32.  ``stages`` (an OR of BWD_DELTA, BWD_DQ, BWD_DKDV) runs a
-    subset of the three launches; the others leave their outputs as given."""
+    """Attention backward (no bias / mask, Dqk == Dv).  Takes the forward's
+    inputs, its output ``o`` and log-sum-exp ``lse`` and the gradient ``do``
+    of O; returns (dq, dk, dv, delta), delta = rowsum(do o o) in float32.
+    Dense ``[B, H, M|N, D]`` or jagged ``[H, T, D]`` with int32 ``offsets``
+    and ``max_seq_len`` (tokens past a sequence's cap get zero gradients).
+    ``stages`` (an OR of BWD_DELTA, BWD_DQ, BWD_DKDV) runs a subset of the
+    launches; the others leave their outputs as given."""
     if q.device.type == "cpu":
-        return _host_call(attn_bwd, (q, k, v, o, lse, do), dict(causal=causal, sm_scale=sm_scale),
-                          n_out=4)
+        return _host_call(attn_bwd, (q, k, v, o, lse, do),
+                          dict(causal=causal, sm_scale=sm_scale, offsets=offsets,
+                               max_seq_len=max_seq_len), n_out=4)
     dev = q.device
     dt = _elem_type(q)
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _need(t, name, dt, dev)
     _need(lse, "lse", torch.float32, dev)
-    sh, _, out_shape, _ = _describe(q, k, v, None, None, None, None)
+    if offsets is not None:
+        _need(offsets, "offsets", torch.int32, dev)
+    sh, _, out_shape, _ = _describe(q, k, v, offsets, max_seq_len, None, None)
     if tuple(o.shape) != out_shape or tuple(do.shape) != out_shape or tuple(lse.shape) != out_shape[:-1]:
-        raise ValueError("o and do must be [B, H, M, Dv] and lse [B, H, M]")
+        raise ValueError("o and do must be shaped like the forward's output and lse like its log-sum-exp")
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         delta = torch.empty(out_shape[:-1], dtype=torch.float32, device=dev)
@@ -306,12 +312,12 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float
     stream = torch.cuda.current_stream(dev).cuda_stream
     if stages == BWD_ALL:
         fn = lib().attn_bwd_f16 if dt == torch.float16 else lib().attn_bwd
-        st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), None, None,
-                1 if causal else 0, _scale(sm_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
+        st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(offsets),
+                None, 1 if causal else 0, _scale(sm_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
                 ctypes.c_void_p(stream))
     else:
         st = lib().attn_bwd_stages(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do),
-                                   _ptr(lse), None, None, 1 if causal else 0, _scale(sm_scale),
+                                   _ptr(lse), _ptr(offsets), None, 1 if causal else 0, _scale(sm_scale),
                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
                                    1 if dt == torch.float16 else 0, int(stages), ctypes.c_void_p(stream))
     _check(st)

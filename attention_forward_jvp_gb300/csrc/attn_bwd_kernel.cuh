@@ -40,14 +40,18 @@ struct BwdParams {
   CUtensorMap tm_t1, tm_t2;  // streamed operands, box 64 x 64 (dQ: K, V; KV: Q, dO)
   int B, H, M, N;
   int causal;
-  int n_rt;       // row tiles of 128 per (b, h)
+  int jagged;          // [H, T, D] layout with offsets[B + 1]
+  const int* offsets;  // jagged: device offsets
+  long long T;         // jagged: total tokens
+  int max_seq_len;     // jagged: cap on a sequence's length
+  int n_rt;       // row tiles of 128 per (b, h) (jagged: per max_seq_len)
   int num_units;  // B * H * n_rt
   float scale_log2;  // sm_scale * log2(e)
   float sm_scale;
-  const float* lse;    // [B, H, M], natural log
-  const float* delta;  // [B, H, M]
-  uint16_t* out1;      // dQ pass: dQ [B,H,M,D]; KV pass: dK [B,H,N,D]
-  uint16_t* out2;      // KV pass: dV [B,H,N,D]
+  const float* lse;    // [B, H, M] (jagged [H, T]), natural log
+  const float* delta;  // same layout as lse
+  uint16_t* out1;      // dQ pass: dQ; KV pass: dK
+  uint16_t* out2;      // KV pass: dV
   int d_out;           // head dim of the tensors (D, or 16 / 32 padded to D = 64)
   int* err;
   unsigned long long timeout_ns;
@@ -91,37 +95,64 @@ struct BwdPlan {
 };
 
 struct BwdUnit {
-  int z;        // b * H + h
-  int rt;       // row tile
-  int t0;       // first streamed tile index (KV causal: the diagonal)
-  int nt;       // streamed tiles
-  int rows;     // valid rows of this (b, h): M (dQ) or N (KV)
+  int z;            // tensor-map z: b * H + h (dense) or h (jagged)
+  int rt;           // row tile
+  int t0;           // first streamed tile (KV causal: the diagonal)
+  int nt;           // streamed tiles (rows with none get zero gradients)
+  int rows;         // valid positions of this pass's rows (queries for dQ, keys for KV)
+  int cols;         // valid positions of the streamed dimension (keys for dQ, queries for KV)
+  int row0;         // tensor-map row of position 0 (jagged: the sequence's first token)
+  long long orow0;  // output row of position 0 of this pass's rows
+  long long qrow0;  // LSE / Delta index of query 0
 };
 
-// Unit u: causal dQ units go longest-first (descending query tile), causal
-// KV units too (ascending key tile: more query tiles above the diagonal).
+// Unit u, costliest first: dense causal dQ units by descending query tile,
+// causal KV units by ascending key tile (more query tiles above the
+// diagonal); jagged units by descending row tile (a high tile only exists
+// in a long sequence) except causal KV, ascending.  A jagged unit past its
+// sequence's length has no rows and nt = 0.
 template <bool KV>
 __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
   const int BH = p.B * p.H;
   BwdUnit w;
-  if (p.causal) {
-    w.rt = KV ? u / BH : p.n_rt - 1 - u / BH;
-    w.z = u % BH;
+  int q_len, k_len;
+  if (!p.jagged) {
+    if (p.causal) {
+      w.rt = KV ? u / BH : p.n_rt - 1 - u / BH;
+      w.z = u % BH;
+    } else {
+      w.z = u / p.n_rt;
+      w.rt = u % p.n_rt;
+    }
+    q_len = p.M;
+    k_len = p.N;
+    w.row0 = 0;
+    w.qrow0 = static_cast<long long>(w.z) * p.M;
+    w.orow0 = static_cast<long long>(w.z) * (KV ? p.N : p.M);
   } else {
-    w.z = u / p.n_rt;
-    w.rt = u % p.n_rt;
+    const int tile = u / BH, r = u % BH;
+    w.rt = (KV && p.causal) ? tile : p.n_rt - 1 - tile;
+    const int b = r / p.H, h = r % p.H;
+    const int begin = __ldg(p.offsets + b), end = __ldg(p.offsets + b + 1);
+    const int len = max(0, min(end - begin, p.max_seq_len));
+    q_len = k_len = len;
+    w.z = h;
+    w.row0 = begin;
+    w.qrow0 = static_cast<long long>(h) * p.T + begin;
+    w.orow0 = w.qrow0;
   }
+  w.rows = KV ? k_len : q_len;
+  w.cols = KV ? q_len : k_len;
+  const bool active = w.rt * kBM < w.rows;
   if (!KV) {
-    w.rows = p.M;
-    int hi = p.N;
+    int hi = k_len;
     if (p.causal) hi = min(hi, (w.rt + 1) * kBM);
     w.t0 = 0;
-    w.nt = (hi + 63) / 64;
+    w.nt = active ? (hi + 63) / 64 : 0;
   } else {
-    w.rows = p.N;
-    const int nq = (p.M + 63) / 64;
+    const int nq = (q_len + 63) / 64;
     w.t0 = p.causal ? (w.rt * kBM) / 64 : 0;
-    w.nt = max(0, nq - w.t0);
+    w.nt = active ? max(0, nq - w.t0) : 0;
   }
   return w;
 }
@@ -189,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           ok = wait_bar(bar(P::B_RE), (rfill & 1u) ^ 1u, W);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(P::B_RF), P::RSET);
-          const int r = w.rt * kBM;
+          const int r = w.row0 + w.rt * kBM;
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
             tma_load_3d(sbase + P::OFF_R + c * P::R_SUB, &p.tm_r1, bar(P::B_RF), c * 64, r, w.z);
@@ -198,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           }
           ++rfill;
           for (int j = 0; j < w.nt; ++j) {
-            const int tr = (w.t0 + j) * P::TN;
+            const int tr = w.row0 + (w.t0 + j) * P::TN;
             const uint32_t ts = tfill % P::NS;
             ok = wait_bar(bar(P::B_TE + ts), ((tfill / P::NS) & 1u) ^ 1u, W);
             if (!ok) break;
@@ -365,12 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const BwdUnit w = bwd_unit<KV>(p, u);
       const int ri = w.rt * kBM + row;  // this thread's row (query for dQ, key for KV)
       const bool row_ok = ri < w.rows;
-      const long long zrow = static_cast<long long>(w.z);
       if (w.nt == 0) {
         // no streamed tile touches these rows: zero gradients
         if (row_ok) {
           const int ncol = min(D / 2, p.d_out - half * (D / 2));  // a multiple of 8
-          const long long off = (zrow * w.rows + ri) * p.d_out + half * (D / 2);
+          const long long off = (w.orow0 + ri) * p.d_out + half * (D / 2);
           for (int c = 0; c < ncol; c += 8) {
             *reinterpret_cast<uint4*>(p.out1 + off + c) = make_uint4(0u, 0u, 0u, 0u);
             if (KV) *reinterpret_cast<uint4*>(p.out2 + off + c) = make_uint4(0u, 0u, 0u, 0u);
@@ -382,13 +412,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       // of dS, pre-negated: nl = -LSE log2(e) and nd = -Delta, with
       // nl = -inf for empty rows and padding rows / columns so that their P
       // is exactly 0 without a test.
+      const int q_len = KV ? w.cols : w.rows;
       auto neg_terms = [&](int i, float& nl, float& nd) {
         nl = -INFINITY;
         nd = 0.f;
-        if (i < p.M) {
-          const float l = __ldg(p.lse + zrow * p.M + i);
+        if (i < q_len) {
+          const float l = __ldg(p.lse + w.qrow0 + i);
           nl = l == -INFINITY ? -INFINITY : -l * kLog2eF;
-          nd = -__ldg(p.delta + zrow * p.M + i);
+          nd = -__ldg(p.delta + w.qrow0 + i);
         }
       };
       float nl_r = -INFINITY, nd_r = 0.f;   // dQ pass: this row's terms
@@ -412,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         // dQ pass keys < N and, causal, <= the query; KV pass, causal,
         // queries >= the key (queries >= M already have nl = -inf)
         int lo = 0, hi = 32;
-        if (!KV) hi = (p.causal ? min(p.N, ri + 1) : p.N) - col0;
+        if (!KV) hi = (p.causal ? min(w.cols, ri + 1) : w.cols) - col0;
         else if (p.causal) lo = ri - col0;
         const bool full = lo <= 0 && hi >= 32;
         // a sleeping wait: a spinning one would take issue slots from the
@@ -505,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           const int rk = w.rt * kBM + quad * 32 + (lane & ~3) + k;
           const int col = half * DH + q * 2 * CW;
           if (rk < w.rows && col < p.d_out) {
-            const long long off = (zrow * w.rows + rk) * p.d_out + col;
+            const long long off = (w.orow0 + rk) * p.d_out + col;
             store_chunk<CW>(out + off, pw + k * CW, false);
           }
         }

@@ -404,6 +404,28 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
 }
 
 // ------------------------------------------------------------- backward
+// Jagged backward: tokens of sequence b past its first min(len, max_seq_len)
+// attend nothing and are attended by nothing, so their dQ, dK, dV are zero.
+// One block per sequence; rows are d 16-bit elements (d a multiple of 8).
+// A NULL output is left alone (each gradient pass zeroes its own).
+__global__ void attn_bwd_zero_tail_kernel(const int* offsets, int H, long long T, int max_seq_len,
+                                          uint16_t* dq, uint16_t* dk, uint16_t* dv, int d) {
+  const int b = blockIdx.x;
+  const int begin = offsets[b], end = offsets[b + 1];
+  const int first = begin + max(0, min(end - begin, max_seq_len));
+  const int chunks = d / 8;  // 16-byte chunks per row
+  const long long per_head = static_cast<long long>(end - first) * chunks;
+  for (long long i = threadIdx.x; i < per_head * H; i += blockDim.x) {
+    const long long h = i / per_head, rem = i % per_head;
+    const long long row = h * T + first + rem / chunks;
+    const long long off = row * d + (rem % chunks) * 8;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    if (dq != nullptr) *reinterpret_cast<uint4*>(dq + off) = z;
+    if (dk != nullptr) *reinterpret_cast<uint4*>(dk + off) = z;
+    if (dv != nullptr) *reinterpret_cast<uint4*>(dv + off) = z;
+  }
+}
+
 // One pass of the dQ kernel (kv = false) or of the dK / dV kernel.
 cudaError_t dispatch_bwd(int d, bool kv, bool f16, const attn::BwdParams& bp, int grid, cudaStream_t cs) {
   if (d == 64) {
@@ -427,19 +449,22 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
                     void* stream, bool f16, unsigned stages) {
   if (s == nullptr) return ATTN_ERR_INVALID_ARG;
   if (stages == 0 || (stages & ~static_cast<unsigned>(ATTN_BWD_ALL)) != 0) return ATTN_ERR_INVALID_ARG;
-  if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0 || s->M < 0 || s->N < 0)
-    return ATTN_ERR_INVALID_ARG;
-  if (offsets != nullptr) return ATTN_ERR_UNSUPPORTED;  // dense layouts only
+  const bool jagged = offsets != nullptr;
+  if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0) return ATTN_ERR_INVALID_ARG;
+  if (!jagged && (s->M < 0 || s->N < 0)) return ATTN_ERR_INVALID_ARG;
+  if (jagged && (s->T < 0 || s->T > 0x7fffffffLL || s->max_seq_len < 0)) return ATTN_ERR_INVALID_ARG;
   if (bias != nullptr && (bias->bias != nullptr || bias->mask != nullptr)) return ATTN_ERR_UNSUPPORTED;
   auto dim_ok = [](int d) { return d == 16 || d == 32 || d == 64 || d == 128; };
   if (!dim_ok(s->Dqk) || s->Dv != s->Dqk) return ATTN_ERR_UNSUPPORTED;
   if (!std::isnan(sm_scale) && !(sm_scale > 0.f && std::isfinite(sm_scale)))
     return ATTN_ERR_INVALID_ARG;
-  if (causal && s->M != s->N) return ATTN_ERR_INVALID_ARG;
+  if (!jagged && causal && s->M != s->N) return ATTN_ERR_INVALID_ARG;
   if (static_cast<int64_t>(s->B) * s->H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   const int64_t BH = static_cast<int64_t>(s->B) * s->H;
-  if (BH == 0 || (s->M == 0 && s->N == 0)) return ATTN_OK;  // nothing to write
-  const bool rows_q = s->M > 0, rows_k = s->N > 0;
+  // rows of the query side and of the key side (jagged: the packed tokens)
+  const int64_t n_q = jagged ? s->T : s->M, n_k = jagged ? s->T : s->N;
+  if (BH == 0 || (n_q == 0 && n_k == 0)) return ATTN_OK;  // nothing to write
+  const bool rows_q = n_q > 0, rows_k = n_k > 0;
   if (rows_q && (q == nullptr || o == nullptr || dout == nullptr || lse == nullptr || dq == nullptr ||
                  delta == nullptr))
     return ATTN_ERR_INVALID_ARG;
@@ -457,11 +482,14 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const float scale = std::isnan(sm_scale) ? 1.0f / std::sqrt(static_cast<float>(s->Dqk)) : sm_scale;
   const int D = s->Dqk <= 64 ? 64 : 128;  // 16 and 32 run zero-padded in the 64-wide kernels
-  const uint64_t d = static_cast<uint64_t>(s->Dqk), M = s->M, N = s->N, Z = static_cast<uint64_t>(BH);
+  const uint64_t d = static_cast<uint64_t>(s->Dqk), M = static_cast<uint64_t>(n_q),
+                 N = static_cast<uint64_t>(n_k);
+  // tensor-map z: b * H + h dense, h jagged (rows are the packed tokens)
+  const uint64_t Z = jagged ? static_cast<uint64_t>(s->H) : static_cast<uint64_t>(BH);
 
   // Delta = rowsum(dO o O)
   if (rows_q && (stages & ATTN_BWD_DELTA)) {
-    const long long rows = static_cast<long long>(BH) * s->M;
+    const long long rows = (jagged ? static_cast<long long>(s->H) : static_cast<long long>(BH)) * n_q;
     const long long want = (rows + 7) / 8;  // 8 warps (rows) per 256-thread block
     const int blocks = static_cast<int>(want < 16LL * ds->num_sms ? want : 16LL * ds->num_sms);
     if (f16)
@@ -473,18 +501,31 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1);
   }
+  // jagged: gradients of the tokens past each sequence's max_seq_len
+  if (jagged && s->B > 0 && (stages & (ATTN_BWD_DQ | ATTN_BWD_DKDV))) {
+    const bool zq = (stages & ATTN_BWD_DQ) != 0, zkv = (stages & ATTN_BWD_DKDV) != 0;
+    attn_bwd_zero_tail_kernel<<<s->B, 256, 0, cs>>>(
+        offsets, s->H, s->T, s->max_seq_len, zq ? static_cast<uint16_t*>(dq) : nullptr,
+        zkv ? static_cast<uint16_t*>(dk) : nullptr, zkv ? static_cast<uint16_t*>(dv) : nullptr, s->Dqk);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1);
+  }
   for (int pass = 0; pass < 2; ++pass) {
     const bool kv = pass == 1;
-    const int rows = kv ? s->N : s->M;
+    const int64_t rows = kv ? n_k : n_q;
     if (rows == 0 || !(stages & (kv ? ATTN_BWD_DKDV : ATTN_BWD_DQ))) continue;
     attn::BwdParams bp;
     std::memset(&bp, 0, sizeof(bp));
     bp.B = s->B;
     bp.H = s->H;
-    bp.M = s->M;
-    bp.N = s->N;
+    bp.M = jagged ? s->max_seq_len : s->M;
+    bp.N = jagged ? s->max_seq_len : s->N;
     bp.causal = causal ? 1 : 0;
-    bp.n_rt = (rows + attn::kBM - 1) / attn::kBM;
+    bp.jagged = jagged ? 1 : 0;
+    bp.offsets = offsets;
+    bp.T = jagged ? s->T : 0;
+    bp.max_seq_len = s->max_seq_len;
+    bp.n_rt = static_cast<int>(((jagged ? s->max_seq_len : rows) + attn::kBM - 1) / attn::kBM);
     bp.scale_log2 = scale * attn::kLog2e;
     bp.sm_scale = scale;
     bp.lse = lse;
@@ -497,6 +538,7 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     // the streamed side has no rows: its maps are never used, only valid
     const bool other = kv ? rows_q : rows_k;
     const uint64_t Ro = other ? (kv ? M : N) : static_cast<uint64_t>(rows);
+    if (bp.n_rt == 0) continue;  // jagged with max_seq_len = 0: nothing attends
     const void* r1 = kv ? k : q;
     const void* r2 = kv ? v : dout;
     const void* t1 = other ? (kv ? q : k) : r1;

@@ -162,21 +162,34 @@ def min_hbm_bytes(w: Workload, inputs: dict, jvp: bool = True) -> int:
     return n
 
 
-def make_bwd_inputs(w: Workload, seed: int = 0) -> dict:
-    """Inputs of the backward for dense workload ``w``: bf16 ``q, k, v``
-    and the output gradient ``do`` ``[B, H, M, Dv]``, drawn in that order
-    (``randn`` times ``input_std``; ``do`` at std 1), plus ``sm_scale`` and
-    ``causal``.  The forward's O and LSE are not drawn: each side computes
-    its own."""
-    assert not w.jagged, "the backward inputs are dense"
+def make_bwd_inputs(w: Workload, seed: int = 0, lengths: Optional[list] = None) -> dict:
+    """Inputs of the backward for workload ``w``: bf16 ``q, k, v`` and the
+    output gradient ``do`` (dense ``[B, H, M|N, D]``, jagged ``[H, T, D]``),
+    drawn in that order (``randn`` times ``input_std``; ``do`` at std 1),
+    after the jagged lengths (``lengths`` overrides them), plus
+    ``sm_scale``, ``causal``, ``offsets``, ``max_seq_len``.  The forward's O
+    and LSE are not drawn: each side computes its own."""
     g = torch.Generator().manual_seed(seed)
-    return {
-        "workload": w, "sm_scale": w.scale, "causal": w.causal,
-        "q": _randn(g, (w.B, w.H, w.M, w.Dqk), w.input_std),
-        "k": _randn(g, (w.B, w.H, w.N, w.Dqk), w.input_std),
-        "v": _randn(g, (w.B, w.H, w.N, w.Dv), w.input_std),
-        "do": _randn(g, (w.B, w.H, w.M, w.Dv), 1.0),
-    }
+    out = {"workload": w, "sm_scale": w.scale, "causal": w.causal, "offsets": None, "max_seq_len": None}
+    if w.jagged:
+        if lengths is None:
+            lens = torch.randint(1, w.max_len_draw + 1, (w.B,), generator=g, dtype=torch.int64)
+        else:
+            lens = torch.tensor(lengths, dtype=torch.int64)
+            assert lens.numel() == w.B
+        offsets = torch.zeros(w.B + 1, dtype=torch.int64)
+        offsets[1:] = torch.cumsum(lens, 0)
+        T = int(offsets[-1])
+        qs, ks, vs = (w.H, T, w.Dqk), (w.H, T, w.Dqk), (w.H, T, w.Dv)
+        out["offsets"] = offsets.to(torch.int32)
+        out["max_seq_len"] = w.max_seq_len
+    else:
+        qs, ks, vs = (w.B, w.H, w.M, w.Dqk), (w.B, w.H, w.N, w.Dqk), (w.B, w.H, w.N, w.Dv)
+    out["q"] = _randn(g, qs, w.input_std)
+    out["k"] = _randn(g, ks, w.input_std)
+    out["v"] = _randn(g, vs, w.input_std)
+    out["do"] = _randn(g, qs[:-1] + (w.Dv,), 1.0)
+    return out
 
 
 def flops_bwd(w: Workload) -> float:

@@ -188,17 +188,21 @@ attn_status attn_fwd_jvp_noalloc(const attn_shape* shape,
  * recomputing P from the stored log-sum-exp); "flash_attention.py"
  * (triton_flashattn) _attn_bwd_dkdv_inner / _attn_bwd_dq_inner.
  *
- * This version: dense layouts only (offsets must be NULL), no bias or mask
- * (bias must be NULL or hold two NULL pointers), Dqk == Dv = D in
- * {16, 32, 64, 128}; otherwise ATTN_ERR_UNSUPPORTED.  Causal requires
- * M == N.  Layouts, element types (bf16; fp16 for attn_bwd_f16), pointer
- * ownership and alignment, sm_scale and stream semantics are those of
- * attn_fwd.  lse must be the forward's (natural log); a row's lse decides
- * its P, so a stale or mismatched lse gives wrong gradients, not an error.
- * delta is a caller-owned output that the two gradient kernels also read.
- * Launches three kernels on `stream` (Delta, then dQ, then dK / dV); no
- * atomics, each output element is written once.  M == 0 writes zero dK and
- * dV; N == 0 writes zero dQ (and delta). */
+ * This version: no bias or mask (bias must be NULL or hold two NULL
+ * pointers) and Dqk == Dv = D in {16, 32, 64, 128}; otherwise
+ * ATTN_ERR_UNSUPPORTED.  Dense (offsets NULL; causal requires M == N) or
+ * jagged (offsets != NULL, the FBGEMM jagged backward's layout:
+ * q, k, v, o, dout, dq, dk, dv [H, T, D], lse and delta [H, T]); a jagged
+ * token past its sequence's min(length, max_seq_len) gets dq = dk = dv = 0,
+ * tokens >= offsets[B] are not written.  Layouts, element types (bf16; fp16
+ * for attn_bwd_f16), pointer ownership and alignment, sm_scale and stream
+ * semantics are those of attn_fwd.  lse must be the forward's (natural log);
+ * a row's lse decides its P, so a stale or mismatched lse gives wrong
+ * gradients, not an error.  delta is a caller-owned output that the two
+ * gradient kernels also read.  Launches on `stream`: Delta, (jagged) a
+ * one-block-per-sequence zero fill of the capped tokens, the dQ pass, the
+ * dK / dV pass; no atomics, each output element is written once.  Dense
+ * M == 0 writes zero dK and dV; N == 0 writes zero dQ (and delta). */
 attn_status attn_bwd(const attn_shape* shape,
                      const void* q, const void* k, const void* v,
                      const void* o, const void* dout, const float* lse,

@@ -136,7 +136,11 @@ def test_bwd_validation(L):
     assert _bwd(L, _shape(Dqk=64, Dv=128)) == 2          # Dqk != Dv
     assert _bwd(L, _shape(Dqk=256, Dv=256)) == 2
     assert _bwd(L, _shape(Dqk=8, Dv=8), f16=True) == 2
-    assert _bwd(L, _shape(T=100, msl=64), offsets=ctypes.c_void_p(0x20000)) == 2  # jagged
+    off = ctypes.c_void_p(0x20000)
+    assert _bwd(L, _shape(T=-1, msl=64), offsets=off) == 1          # jagged, bad T
+    assert _bwd(L, _shape(T=100, msl=-2), offsets=off) == 1         # jagged, bad cap
+    assert _bwd(L, _shape(T=100, msl=64, Dqk=64, Dv=128), offsets=off) == 2
+    assert _bwd(L, _shape(T=0, msl=64), offsets=off) == 0           # no tokens: no-op
     b = binding.AttnBias()
     b.mask = 0x10000
     assert _bwd(L, _shape(), bias=ctypes.byref(b)) == 2  # mask / bias

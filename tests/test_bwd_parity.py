@@ -156,3 +156,32 @@ def test_bwd_stages_match_one_call():
     assert binding.sync_check() == 0
     for a, b in zip(ref, out):
         assert torch.equal(a, b)
+
+
+JAGGED_LENS = [3, 64, 130, 257, 1, 0, 300, 128]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128, 32])
+def test_bwd_jagged(causal, D):
+    # lengths around the tile sizes, an empty sequence and two sequences
+    # past max_seq_len = 256 (their capped tokens get zero gradients)
+    w = Workload("jb", B=len(JAGGED_LENS), H=2, Dqk=D, Dv=D, jagged=True, max_seq_len=256,
+                 max_len_draw=1, causal=causal)
+    inp = make_bwd_inputs(w, seed=21, lengths=JAGGED_LENS)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    off = inp["offsets"].cuda()
+    kw = dict(causal=causal, sm_scale=inp["sm_scale"], offsets=off, max_seq_len=256)
+    o, lse = binding.attn_fwd(q, k, v, **kw)
+    dq, dk, dv, delta = binding.attn_bwd(q, k, v, o, lse, do, **kw)
+    assert binding.sync_check() == 0
+    got = tuple(t.float().cpu().numpy() for t in (dq, dk, dv, delta))
+    ref = oracle.attention_bwd_jagged(inp["q"], inp["k"], inp["v"], inp["do"], inp["offsets"], 256,
+                                      causal=causal, sm_scale=inp["sm_scale"])
+    assert_grads_close(got, ref, what=f"jagged D{D} causal={causal}")
+    # capped tokens: exactly zero
+    offs = inp["offsets"].numpy()
+    for b, L in enumerate(JAGGED_LENS):
+        if L > 256:
+            for g in got[:3]:
+                assert np.all(g[:, offs[b] + 256:offs[b + 1]] == 0)
