@@ -25,6 +25,7 @@ EXPORTS = (
     "attn_fwd",
     "attn_fwd_jvp_f16",
     "attn_fwd_f16",
+    "attn_fwd_f8",
     "attn_fwd_jvp_noalloc",
     "attn_bwd",
     "attn_bwd_f16",
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd_stages.argtypes = [ctypes.POINTER(AttnShape), vp, vp, vp, vp, vp, vp, vp,
                                   ctypes.POINTER(AttnBias), i32, f32, vp, vp, vp, vp, i32,
                                   ctypes.c_uint, vp]
+    L.attn_fwd_f8.restype = i32
+    L.attn_fwd_f8.argtypes = [ctypes.POINTER(AttnShape), vp, vp, vp, i32, f32, vp, vp, vp]
     L.attn_sync_check.restype = i32
     L.attn_sync_check.argtypes = [vp]
     L.attn_status_string.restype = ctypes.c_char_p
@@ -322,6 +325,36 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float
                                    1 if dt == torch.float16 else 0, int(stages), ctypes.c_void_p(stream))
     _check(st)
     return dq, dk, dv, delta
+
+
+def attn_fwd_f8(q, k, vt, causal: bool = False, sm_scale: Optional[float] = None, out=None):
+    """FP8 (e5m2) forward: q [B, H, M, D], k [B, H, N, D] and the transposed
+    value vt [B, H, D, N], all torch.float8_e5m2.  Returns (o, lse): o e5m2
+    [B, H, M, D], lse float32 [B, H, M]."""
+    if q.device.type == "cpu":
+        return _host_call(attn_fwd_f8, (q, k, vt), dict(causal=causal, sm_scale=sm_scale), n_out=2)
+    dev = q.device
+    dt = torch.float8_e5m2
+    for name, t in (("q", q), ("k", k), ("vt", vt)):
+        _need(t, name, dt, dev)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, M, D]")
+    B, H, M, D = q.shape
+    N = k.shape[2]
+    if tuple(k.shape) != (B, H, N, D) or tuple(vt.shape) != (B, H, D, N):
+        raise ValueError("k must be [B, H, N, D] and vt [B, H, D, N]")
+    sh = AttnShape()
+    sh.B, sh.H, sh.M, sh.N, sh.Dqk, sh.Dv, sh.T, sh.max_seq_len = B, H, M, N, D, D, 0, 0
+    if out is None:
+        o = torch.empty((B, H, M, D), dtype=dt, device=dev)
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=dev)
+    else:
+        o, lse = out
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    st = lib().attn_fwd_f8(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(vt), 1 if causal else 0,
+                           _scale(sm_scale), _ptr(o), _ptr(lse), ctypes.c_void_p(stream))
+    _check(st)
+    return o, lse
 
 
 def _host_call(fn, tensors, kw, n_out):

@@ -76,6 +76,8 @@ extern template cudaError_t launch_attn<256, 256, false, kBiasRing, false>(const
 extern template cudaError_t launch_attn<256, 256, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<128, 128, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn_bwd<64, false, false>(const BwdParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn_bwd<64, true, false>(const BwdParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn_bwd<64, false, true>(const BwdParams&, int, cudaStream_t);
@@ -211,6 +213,20 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t d, uint64_t rows, uin
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D view [z][rows][inner] of bytes (e5m2 elements), box box_inner x
+// box_rows x 1 with the given swizzle; out-of-range elements read as zeros.
+bool encode_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t z,
+                   uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  cuuint64_t dims[3] = {inner, rows, z};
+  cuuint64_t strides[2] = {inner, inner * rows};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 // 4-D fp32 view of the bias [b][h][m][n] (n innermost), box 32 x 128 x 1 x
 // 1, 128-byte swizzle, keys / rows past the end read as zeros.  A broadcast
@@ -398,6 +414,68 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
                    : (kp.bias != nullptr && kp.bias_tma == 0) ? attn::kBiasGlobal
                                                                : attn::kBiasRing;
   e = dispatch_attn(key, jvp, mode, f16, kp, grid, cs);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------------ e5m2 forward
+attn_status run_f8(const attn_shape* s, const void* q, const void* k, const void* vt, int causal,
+                   float sm_scale, void* o, float* lse, void* stream) {
+  if (s == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (s->B < 0 || s->H < 0 || s->M < 0 || s->N < 0 || s->Dqk < 0 || s->Dv < 0) return ATTN_ERR_INVALID_ARG;
+  if (!((s->Dqk == 64 && s->Dv == 64) || (s->Dqk == 128 && s->Dv == 128))) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isnan(sm_scale) && !(sm_scale > 0.f && std::isfinite(sm_scale))) return ATTN_ERR_INVALID_ARG;
+  if (causal && s->M != s->N) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s->B) * s->H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  const int64_t BH = static_cast<int64_t>(s->B) * s->H;
+  if (BH == 0 || s->M == 0) return ATTN_OK;  // nothing to write
+  // V^T rows are N bytes apart: bulk tensor copies need a multiple of 16
+  if (s->N % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (s->N > 0 && (k == nullptr || vt == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+  if (s->N > 0 && (!aligned16(k) || !aligned16(vt))) return ATTN_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  attn_status st = device_state(&ds);
+  if (st != ATTN_OK) return st;
+
+  attn::KernelParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  const float scale = std::isnan(sm_scale) ? 1.0f / std::sqrt(static_cast<float>(s->Dqk)) : sm_scale;
+  kp.B = s->B;
+  kp.H = s->H;
+  kp.M = s->M;
+  kp.N = s->N;
+  kp.causal = causal ? 1 : 0;
+  kp.sm_scale = scale;
+  kp.scale_log2 = scale * attn::kLog2e;
+  kp.o = static_cast<uint16_t*>(o);  // e5m2 bytes; the kernel addresses them as such
+  kp.lse = lse;
+  kp.dv_out = s->Dv;
+  kp.err = ds->scratch;
+  kp.timeout_ns = g_timeout_ns.load();
+  kp.n_mt = (s->M + attn::kBM - 1) / attn::kBM;
+  const uint64_t D = static_cast<uint64_t>(s->Dqk), Z = static_cast<uint64_t>(BH);
+  const uint64_t M = s->M;
+  const uint64_t N = s->N > 0 ? static_cast<uint64_t>(s->N) : 16;  // no keys: valid, never read
+  const void* kb = s->N > 0 ? k : q;
+  const void* vb = s->N > 0 ? vt : q;
+  // Q, K: one 128-byte swizzled chunk per row (zeros past D); V^T: rows of
+  // 64 keys with 64-byte swizzle, Dv rows per box
+  bool ok = encode_map_u8(&kp.tm_q, q, D, M, Z, 128, attn::kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_map_u8(&kp.tm_k, kb, D, s->N > 0 ? N : M, Z, 128, attn::kBN, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_map_u8(&kp.tm_v, vb, s->N > 0 ? N : D, s->N > 0 ? D : M, Z, 64,
+                           static_cast<uint32_t>(s->Dv), CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!ok) return ATTN_ERR_CUDA;
+  const int64_t units = BH * kp.n_mt;
+  if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  kp.num_units = static_cast<int>(units);
+  const int grid = static_cast<int>(units < ds->num_sms ? units : ds->num_sms);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = s->Dqk == 64
+                            ? attn::launch_attn<64, 64, false, attn::kNoBias, false, true>(kp, grid, cs)
+                            : attn::launch_attn<128, 128, false, attn::kNoBias, false, true>(kp, grid, cs);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   g_launches.fetch_add(1);
   return ATTN_OK;
@@ -666,6 +744,11 @@ attn_status attn_bwd_f16(const attn_shape* shape, const void* q, const void* k, 
                          void* dv, float* delta, void* stream) {
   return run_bwd(shape, q, k, v, o, dout, lse, offsets, bias, causal, sm_scale, dq, dk, dv, delta,
                  stream, true, ATTN_BWD_ALL);
+}
+
+attn_status attn_fwd_f8(const attn_shape* shape, const void* q, const void* k, const void* vt,
+                        int causal, float sm_scale, void* o, float* lse, void* stream) {
+  return run_f8(shape, q, k, vt, causal, sm_scale, o, lse, stream);
 }
 
 attn_status attn_sync_check(void* stream) {

@@ -117,9 +117,14 @@ struct KernelParams {
 constexpr int kNoBias = 0, kBiasRing = 1, kBiasGlobal = 2;
 
 // Shared-memory and tensor-memory plan for one instantiation.
-template <int DQK, int DV, bool JVP, int BMODE>
+// F8: e5m2 operands (forward only): a row of Q or K (D <= 128 bytes) is
+// one 128-byte swizzled chunk, and V arrives transposed, a tile being Dv
+// rows of 64 keys (64-byte rows, 64-byte swizzle).
+template <int DQK, int DV, bool JVP, int BMODE, bool F8 = false>
 struct Plan {
+  static_assert(!F8 || (!JVP && BMODE == 0 && DQK <= 128 && DV <= 128), "e5m2: forward only, no bias");
   static constexpr int NQ = JVP ? 2 : 1;   // primal (+ tangent) operands
+  static constexpr int CH = F8 ? 1 : DQK / 64;  // 128-byte chunks per Q / K row
   // Bias stage: the fp32 bias of one key tile, two 128-row x 32-key boxes
   // (one per softmax half), 128-byte swizzled rows.
   static constexpr int BIAS_BOX = kBM * 32 * 4;
@@ -127,12 +132,12 @@ struct Plan {
   static constexpr int Q_SUB = kBM * 128;  // one 64-column swizzled sub-tile
   static constexpr int K_SUB = kBN * 128;
   static constexpr int V_SUB = kBN * 128;
-  static constexpr int Q_TILE = (DQK / 64) * Q_SUB;
-  static constexpr int V_TILE = (DV / 64) * V_SUB;
+  static constexpr int Q_TILE = CH * Q_SUB;
+  static constexpr int V_TILE = F8 ? DV * 64 : (DV / 64) * V_SUB;
   // K stage: for each 64-column chunk c, [K rows | tK rows] side by side so
   // that Q [K ; tK]^T is one N = 128 operand.
   static constexpr int K_GROUP = NQ * K_SUB;
-  static constexpr int K_STAGE = (DQK / 64) * K_GROUP;
+  static constexpr int K_STAGE = CH * K_GROUP;
   // V stage: [V chunks | tV chunks], uniform 64-column stride, so that
   // [V | tV] is one N = 2 Dv operand.
   static constexpr int V_STAGE = NQ * V_TILE;
@@ -200,6 +205,7 @@ struct Plan {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
   static_assert(COLS_USED <= 512, "tensor memory plan exceeds 512 columns");
   static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims are multiples of 64");
+  static_assert(V_TILE % 1024 == 0, "V tiles keep 1024-byte alignment");
   static_assert(NQ * DV <= 256, "[O | tO] MMA needs N <= 256");
 };
 
@@ -375,9 +381,14 @@ __device__ __forceinline__ void quad_transpose(uint32_t (&a)[4 * C], int q) {
 }
 
 // C packed words to global memory: one 32-byte store when C == 8 and the
-// address is 32-byte aligned, else 16-byte stores.
+// address is 32-byte aligned, one 8-byte store when C == 2, else 16-byte
+// stores.
 template <int C>
 __device__ __forceinline__ void store_chunk(uint16_t* dst, const uint32_t* w, bool aligned32) {
+  if constexpr (C == 2) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    return;
+  }
   if (C == 8 && aligned32) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
                  "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
@@ -448,9 +459,9 @@ __device__ __forceinline__ float rowmax32(const float* x) {
 // BMODE: kNoBias, kBiasRing or kBiasGlobal (see Plan).  Each mode compiles
 // only its own bias / mask code, which keeps the per-tile loop small.
 // F16: fp16 inputs, MMA operands and outputs instead of bf16.
-template <int DQK, int DV, bool JVP, int BMODE, bool F16>
+template <int DQK, int DV, bool JVP, int BMODE, bool F16, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KernelParams p) {
-  using P = Plan<DQK, DV, JVP, BMODE>;
+  using P = Plan<DQK, DV, JVP, BMODE, F8>;
   constexpr bool BM = BMODE != kNoBias;
   constexpr bool RING = BMODE == kBiasRing;
   constexpr bool GLOB = BMODE == kBiasGlobal;
@@ -551,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int r = w.row0 + w.mt * kBM;
           const uint32_t qdst = sbase + qb * P::QSET;
 #pragma unroll
-          for (int c = 0; c < DQK / 64; ++c) {
+          for (int c = 0; c < P::CH; ++c) {
             tma_load_3d(qdst + P::OFF_Q + c * P::Q_SUB, &p.tm_q, bar(P::B_QF + qb), c * 64, r, w.z);
             if (JVP)
               tma_load_3d(qdst + P::OFF_TQ + c * P::Q_SUB, &p.tm_tq, bar(P::B_QF + qb), c * 64, r,
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           mbar_arrive_expect_tx(bar(P::B_KF + ks), P::K_STAGE);
           const uint32_t kdst = sbase + P::OFF_K + ks * P::K_STAGE;
 #pragma unroll
-          for (int c = 0; c < DQK / 64; ++c) {
+          for (int c = 0; c < P::CH; ++c) {
             tma_load_3d(kdst + c * P::K_GROUP, &p.tm_k, bar(P::B_KF + ks), c * 64, r, w.z);
             if (JVP)
               tma_load_3d(kdst + c * P::K_GROUP + P::K_SUB, &p.tm_tk, bar(P::B_KF + ks), c * 64, r,
@@ -610,12 +621,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           if (!ok) break;
           mbar_arrive_expect_tx(bar(P::B_VF + vs), P::V_STAGE);
           const uint32_t vdst = sbase + P::OFF_V + vs * P::V_STAGE;
+          if constexpr (F8) {
+            // V^T: Dv rows of this tile's 64 keys (x = key, y = row of V^T)
+            tma_load_3d(vdst, &p.tm_v, bar(P::B_VF + vs), r, 0, w.z);
+          } else {
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c) {
             tma_load_3d(vdst + c * P::V_SUB, &p.tm_v, bar(P::B_VF + vs), c * 64, r, w.z);
             if (JVP)
               tma_load_3d(vdst + P::V_TILE + c * P::V_SUB, &p.tm_tv, bar(P::B_VF + vs), c * 64, r,
                           w.z);
+          }
           }
           if constexpr (P::NB > 0) {
             if (bias_ring) {
@@ -691,9 +707,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // the waits for the K / V tiles of the next batches are placed in the
     // middle of a batch, while the tensor pipe still holds queued MMAs.
     const bool leader = elect_one();
-    constexpr uint32_t idesc_s = idesc_16(kBM, JVP ? 2 * kBN : kBN, false, F16);  // [S | Q tK^T]
+    constexpr uint32_t idesc_s = F8 ? idesc_e5m2(kBM, kBN)
+                                    : idesc_16(kBM, JVP ? 2 * kBN : kBN, false, F16);  // [S | Q tK^T]
     constexpr uint32_t idesc_t = idesc_16(kBM, kBN, false, F16);                   // tQ K^T
-    constexpr uint32_t idesc_o = idesc_16(kBM, P::NQ * DV, true, F16);             // [O | tO]
+    constexpr uint32_t idesc_o = F8 ? idesc_e5m2(kBM, DV)                         // O (V^T K-major)
+                                    : idesc_16(kBM, P::NQ * DV, true, F16);       // [O | tO]
     constexpr uint32_t idesc_h = idesc_16(kBM, DV, true, F16);                     // H V
     auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, wait_bar(b, parity, W));
@@ -726,7 +744,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     constexpr uint32_t kHi = sdesc_hi_sw128(1024);
     const uint32_t lo_q = sdesc_lo(sbase + P::OFF_Q, 16);
     const uint32_t lo_k = sdesc_lo(sbase + P::OFF_K, 16);
-    const uint32_t lo_v = sdesc_lo(sbase + P::OFF_V, P::V_SUB);
+    const uint32_t lo_v = sdesc_lo(sbase + P::OFF_V, F8 ? 16 : P::V_SUB);
+    constexpr uint32_t kHi64 = sdesc_hi_sw64(512);  // e5m2 V^T tiles: 64-byte rows
+    // K steps of one score chain: 16 elements (32 bytes) for 16-bit types,
+    // 32 elements (32 bytes) for e5m2
+    constexpr int KS = F8 ? DQK / 32 : DQK / 16;
 
     // [S | Q tK^T] = Q [K ; tK]^T, tS += tQ K^T for tile t; `mid` runs after
     // the first half of the first chain.
@@ -736,12 +758,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint32_t dS = tmem + (t & 1u) * P::SBUF;
       const uint32_t lk = lo_k + (t % P::NK) * (P::K_STAGE >> 4);
 #pragma unroll
-      for (int kk = 0; kk < DQK / 16; ++kk) {
+      for (int kk = 0; kk < KS; ++kk) {
         const uint32_t oq = ((kk >> 2) * P::Q_SUB + (kk & 3) * 32) >> 4;
         const uint32_t ok_ = ((kk >> 2) * P::K_GROUP + (kk & 3) * 32) >> 4;
-        if (leader) mma_ss(dS, sdesc_join(lq + oq, kHi), sdesc_join(lk + ok_, kHi), idesc_s, kk > 0 ? 1u : 0u);
+        if (leader) {
+          if constexpr (F8)
+            mma_ss_f8(dS, sdesc_join(lq + oq, kHi), sdesc_join(lk + ok_, kHi), idesc_s, kk > 0 ? 1u : 0u);
+          else
+            mma_ss(dS, sdesc_join(lq + oq, kHi), sdesc_join(lk + ok_, kHi), idesc_s, kk > 0 ? 1u : 0u);
+        }
         __syncwarp();
-        if (kk == DQK / 32 - 1) mid();
+        if (kk == KS / 2 - 1) mid();
       }
       if (JVP) {
 #pragma unroll
@@ -773,6 +800,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // keys [16 kk, 16 kk + 16): P at column base + 32 (kk / 2) + 8 (kk % 2),
       // H 16 columns further (the layout the softmax halves write)
       const uint32_t aP = tmem + sb * P::SBUF + kBN;
+      if constexpr (F8) {
+        // keys [32 kk, 32 kk + 32): e5m2 P in the 8 columns of softmax half
+        // kk; V^T rows of 64 keys, the K step 32 bytes along the row
+#pragma unroll
+        for (int kk = 0; kk < kBN / 32; ++kk) {
+          const uint64_t dv = sdesc_join(lv + ((kk * 32) >> 4), kHi64);
+          if (leader) mma_ts_f8(tmem + colo, aP + 8 * kk, dv, idesc_o, (first && kk == 0) ? 0u : 1u);
+          __syncwarp();
+          if (kk == 0) mid();
+        }
+      } else {
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk) {
         const uint64_t dv = sdesc_join(lv + ((kk * 2048) >> 4), kHi);
@@ -781,6 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                  (first && kk == 0) ? 0u : 1u);
         __syncwarp();
         if (kk == kBN / 32 - 1) mid();
+      }
       }
       if (JVP) {
 #pragma unroll
@@ -944,8 +983,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // at least 1 because the reference max trails the row max by < 8)
       const bool empty = !(lt_sum > 0.f);
       const float inv_l = empty ? 0.f : 1.f / lt_sum;
-      constexpr int NW = DVH / 2;  // packed words per half row
-      constexpr int CW = NW / 4;   // words per chunk (four chunks per half row)
+      constexpr int EPW = F8 ? 4 : 2;  // output elements per packed word
+      constexpr int NW = DVH / EPW;    // packed words per half row
+      constexpr int CW = NW / 4;       // words per chunk (four chunks per half row)
       uint32_t po[NW], pt[NW];
 #pragma unroll
       for (int c0 = 0; c0 < DVH; c0 += 32) {
@@ -955,6 +995,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if constexpr (JVP) tmem_ld_32x32b_x32(tl + colo + DV + half * DVH + c0, tv);
         tmem_wait_ld_regs(ov);
         if constexpr (JVP) tmem_regs_ready(tv);
+        if constexpr (F8) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            po[c0 / 4 + i / 4] = pack_e5m2x4(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l,
+                                             __uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
+          continue;
+        }
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const float o0 = __uint_as_float(ov[i]) * inv_l;
@@ -984,10 +1031,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int qk = e.mt * kBM + quad * 32 + (lane & ~3) + k;  // row of slot k
-        const int col = half * DVH + q * 2 * CW;                   // first column of the chunk
+        const int col = half * DVH + q * EPW * CW;                 // first column of the chunk
         if (qk < e.q_len && col < p.dv_out) {
           const long long off = (e.out0 + qk) * p.dv_out + col;
-          store_chunk<CW>(p.o + off, po + k * CW, out32);
+          if constexpr (F8)
+            store_chunk<CW>(reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(p.o) + off), po + k * CW, false);
+          else
+            store_chunk<CW>(p.o + off, po + k * CW, out32);
           if constexpr (JVP) store_chunk<CW>(p.to + off, pt + k * CW, out32);
         }
       }
@@ -1010,13 +1060,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // this half's output columns: [half * DVH, min((half + 1) * DVH, dv_out))
         const int ncol = min(DVH, p.dv_out - half * DVH);
         if (row_ok && ncol > 0) {
-          uint16_t* orow = p.o + (w.out0 + qi) * p.dv_out + half * DVH;
-          uint16_t* torow = JVP ? p.to + (w.out0 + qi) * p.dv_out + half * DVH : nullptr;
           uint32_t z[DVH / 2];
 #pragma unroll
           for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
-          store_row_bf16(orow, z, ncol / 2);
-          if (JVP) store_row_bf16(torow, z, ncol / 2);
+          if constexpr (F8) {
+            // e5m2 output: one byte per element
+            uint8_t* orow8 = reinterpret_cast<uint8_t*>(p.o) + (w.out0 + qi) * p.dv_out + half * DVH;
+            store_row_bf16(reinterpret_cast<uint16_t*>(orow8), z, ncol / 4);
+          } else {
+            uint16_t* orow = p.o + (w.out0 + qi) * p.dv_out + half * DVH;
+            uint16_t* torow = JVP ? p.to + (w.out0 + qi) * p.dv_out + half * DVH : nullptr;
+            store_row_bf16(orow, z, ncol / 2);
+            if (JVP) store_row_bf16(torow, z, ncol / 2);
+          }
         }
         if (row_ok && half == 0) p.lse[w.out0 + qi] = -INFINITY;
         continue;
@@ -1222,8 +1278,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint64_t sc2 = f2_make(sc, sc), nm2 = f2_make(neg_m, neg_m);
         uint64_t ls = 0;
         float lt0 = 0.f, lt1 = 0.f, rt0 = 0.f, rt1 = 0.f;
-        uint32_t pk[kHalf / 2];
         uint64_t pv[kHalf / 2];
+        if constexpr (F8) {
+          // four e5m2 weights per column, half h in the 8 columns at 8 h
+          uint32_t pk8[kHalf / 4];
+#pragma unroll
+          for (int c = 0; c < kHalf; c += 4) {
+            float a0, a1, a2, a3;
+            f2_split(f2_fma(f2_make(x[c], x[c + 1]), sc2, nm2), a0, a1);
+            f2_split(f2_fma(f2_make(x[c + 2], x[c + 3]), sc2, nm2), a2, a3);
+            const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
+            ls = f2_add(ls, f2_add(f2_make(p0, p1), f2_make(p2, p3)));
+            const uint32_t pw = pack_e5m2x4(p0, p1, p2, p3);
+            pk8[c / 4] = pw;
+            add_e5m2x4_f32(pw, lt0, lt1);
+          }
+          tmem_st_32x32b_x8(tl + sb * P::SBUF + kBN + half * (kHalf / 4), pk8);
+        } else {
+        uint32_t pk[kHalf / 2];
 #pragma unroll
         for (int c = 0; c < kHalf; c += 2) {
           float a0, a1;
@@ -1237,6 +1309,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           add2_f32<F16>(pw, lt0, lt1);
         }
         tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, pk);
+        }
         if constexpr (JVP) {
           uint32_t hk[kHalf / 2];
           tmem_wait_ld_regs(tr);
@@ -1316,8 +1389,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     if (ok && has_pend) ok = epilogue(pend);
 
-    // Jagged rows past max_seq_len inside their sequence: empty rows.
-    if (ok && p.jagged) {
+    // Jagged rows past max_seq_len inside their sequence: empty rows.  (The
+    // e5m2 kernel is dense only.)
+    if (!F8 && ok && p.jagged) {
       const int t256 = threadIdx.x - 128;
       for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         const int begin = __ldg(p.offsets + b), end = __ldg(p.offsets + b + 1);
@@ -1343,9 +1417,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, P::TMEM_COLS);
 }
 
-template <int DQK, int DV, bool JVP, int BMODE, bool F16>
+template <int DQK, int DV, bool JVP, int BMODE, bool F16, bool F8 = false>
 cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
-  using P = Plan<DQK, DV, JVP, BMODE>;
+  using P = Plan<DQK, DV, JVP, BMODE, F8>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1355,16 +1429,16 @@ cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
     // computed for; a build that compiled to another count is refused
     // (setmaxnreg.inc would otherwise wait for registers that never free).
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP, BMODE, F16>);
+    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP, BMODE, F16>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  attn_fwd_kernel<DQK, DV, JVP, BMODE, F16><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
+  attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
   return cudaGetLastError();
 }
 

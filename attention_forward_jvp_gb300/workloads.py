@@ -192,22 +192,36 @@ def make_bwd_inputs(w: Workload, seed: int = 0, lengths: Optional[list] = None) 
     return out
 
 
-def flops_bwd(w: Workload) -> float:
+def score_elements(w: Workload, offsets: Optional[torch.Tensor] = None) -> float:
+    """Score elements of the workload before the causal halving: B H M N
+    dense, H sum_b min(L_b, max_seq_len)^2 jagged."""
+    if w.jagged:
+        assert offsets is not None
+        lens = (offsets[1:] - offsets[:-1]).clamp(max=w.max_seq_len).to(torch.float64)
+        return float((lens * lens).sum()) * w.H
+    return float(w.B * w.H * w.M * w.N)
+
+
+def flops_bwd(w: Workload, offsets: Optional[torch.Tensor] = None) -> float:
     """Algorithmic FLOPs of the backward: five matmuls per score element
     (S = Q K^T, dP = dO V^T, dV = P^T dO, dQ = dS K, dK = dS^T Q), halved
     for causal attention -- 2.5 times the forward, the rule of the
     fused-attention tutorial's benchmark.  Kernels that recompute a product
     do not get credit for it."""
-    f = 2.0 * (3 * w.Dqk + 2 * w.Dv) * float(w.B * w.H * w.M * w.N)
+    f = 2.0 * (3 * w.Dqk + 2 * w.Dv) * score_elements(w, offsets)
     if w.causal:
         f *= 0.5
     return f
 
 
-def min_hbm_bytes_bwd(w: Workload) -> int:
+def min_hbm_bytes_bwd(w: Workload, rows: Optional[int] = None) -> int:
     """Bytes the backward must move at least once: q, k, v, o, do, lse read;
-    dq, dk, dv written (all 16-bit but lse); Delta written and read (fp32)."""
-    rows_q, rows_k = w.B * w.H * w.M, w.B * w.H * w.N
+    dq, dk, dv written (all 16-bit but lse); Delta written and read (fp32).
+    ``rows``: jagged H T (query rows = key rows)."""
+    if rows is not None:
+        rows_q = rows_k = rows
+    else:
+        rows_q, rows_k = w.B * w.H * w.M, w.B * w.H * w.N
     n = 2 * (rows_q * w.Dqk + rows_k * (w.Dqk + w.Dv) + 2 * rows_q * w.Dv)
     n += 4 * rows_q                          # lse
     n += 2 * (rows_q * w.Dqk + rows_k * (w.Dqk + w.Dv))

@@ -40,7 +40,8 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from attention_forward_jvp_gb300.workloads import (WORKLOADS, flops_bwd, flops_fwd_jvp, make_bwd_inputs,  # noqa: E402
-                                                   make_inputs, min_hbm_bytes, min_hbm_bytes_bwd)
+                                                   make_inputs, min_hbm_bytes, min_hbm_bytes_bwd,
+                                                   score_elements)
 
 METRIC = "attn fwd+JVP TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 tensor peak"
 METRIC_BWD = "attn backward (dQ, dK, dV) TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 tensor peak"
@@ -468,8 +469,8 @@ def run_ours_bwd(args, w, world, rank, local):
     from attention_forward_jvp_gb300 import binding
     from attention_forward_jvp_gb300 import build as _b
 
-    if w.jagged or w.bias or w.mask_keep is not None or w.Dqk != w.Dv:
-        raise SystemExit(f"--op bwd runs dense workloads without bias / mask and Dqk == Dv ({w.name} is not)")
+    if w.bias or w.mask_keep is not None or w.Dqk != w.Dv:
+        raise SystemExit(f"--op bwd runs workloads without bias / mask and Dqk == Dv ({w.name} is not)")
     if not os.path.exists(_b.LIB_PATH):
         _b.build()
     binding.lib()
@@ -477,16 +478,18 @@ def run_ours_bwd(args, w, world, rank, local):
     dev = torch.device("cuda", local)
     inp = make_bwd_inputs(w, seed=0)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
-    kw = dict(causal=w.causal, sm_scale=inp["sm_scale"])
+    kw = dict(causal=w.causal, sm_scale=inp["sm_scale"],
+              offsets=None if inp["offsets"] is None else inp["offsets"].to(dev),
+              max_seq_len=inp["max_seq_len"])
     o, lse = binding.attn_fwd(q, k, v, **kw)
     out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(lse))
-    flops = flops_bwd(w)
-    elem = float(w.B * w.H * w.M * w.N) * (0.5 if w.causal else 1.0)
+    flops = flops_bwd(w, inp["offsets"])
+    elem = score_elements(w, inp["offsets"]) * (0.5 if w.causal else 1.0)
     flops_dkdv = 4.0 * (w.Dqk + w.Dv) * elem   # S^T, dP^T, dV, dK
     stream = torch.cuda.current_stream(dev)
     stages = (binding.BWD_DELTA, binding.BWD_DQ, binding.BWD_DKDV)
 
-    flush = min_hbm_bytes_bwd(w) < 2 * L2_BYTES
+    flush = min_hbm_bytes_bwd(w, q.numel() // w.Dqk if w.jagged else None) < 2 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     with ClockSampler(local) as clk:
@@ -520,15 +523,19 @@ def run_ours_bwd(args, w, world, rank, local):
 
     # end to end through the public API with pinned host buffers
     hin = [t.cpu().pin_memory() for t in (q, k, v, o, lse, do)]
+    hkw = dict(kw)
+    if inp["offsets"] is not None:
+        hkw["offsets"] = inp["offsets"].pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in hin)
+    h2d += 0 if inp["offsets"] is None else inp["offsets"].numel() * 4
     e2e_steps = max(1, min(args.steps, 10))
-    hout = binding.attn_bwd(*hin, **kw)
+    hout = binding.attn_bwd(*hin, **hkw)
     d2h = sum(t.numel() * t.element_size() for t in hout)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        hout = binding.attn_bwd(*hin, **kw)
+        hout = binding.attn_bwd(*hin, **hkw)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
     e2e_val = world * flops / e2e_s / 1e12
@@ -545,9 +552,9 @@ def run_ours_bwd(args, w, world, rank, local):
             "stage_ms": {"delta": per[0], "dq": per[1], "dkdv": per[2]},
             "stage_tflops": {"dq": 2.0 * (2 * w.Dqk + w.Dv) * elem / (per[1] * 1e-3) / 1e12,
                              "dkdv": achieved},
-            "delta_gbs": 2.0 * 2 * w.B * w.H * w.M * w.Dv / (per[0] * 1e-3) / 1e9}
+            "delta_gbs": 2.0 * 2 * (o.numel() // w.Dv) * w.Dv / (per[0] * 1e-3) / 1e9}
     cpu = None
-    if world == 1 and not args.skip_cpu_baseline:
+    if world == 1 and not args.skip_cpu_baseline and not w.jagged:
         dt = fl = 0.0
         n = 0
         while n < w.B * w.H and (n == 0 or dt < args.cpu_seconds):

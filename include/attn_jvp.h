@@ -143,6 +143,24 @@ attn_status attn_fwd_f16(const attn_shape* shape,
                          int causal, float sm_scale,
                          void* o, float* lse, void* stream);
 
+/* FP8 forward (no tangents): the FP8 path of the Triton fused-attention
+ * tutorial (q, k, v in float8 e5m2, V stored transposed, P cast to e5m2
+ * before the P V product, O written in e5m2).  Dense only.
+ *   q  [B, H, M, D] e5m2     k [B, H, N, D] e5m2
+ *   vt [B, H, D, N] e5m2     (V transposed: vt[b,h,d,j] = V[b,h,j,d])
+ *   o  [B, H, M, D] e5m2     lse [B, H, M] fp32 (natural log)
+ * D = Dqk = Dv in {64, 128} (else ATTN_ERR_UNSUPPORTED); N a multiple of
+ * 16 (the rows of vt are N bytes and bulk copies need 16-byte strides;
+ * else ATTN_ERR_UNSUPPORTED); causal requires M == N.  S is accumulated in
+ * fp32 from the e5m2 products, P is rounded to e5m2 for the P V product,
+ * and O is normalised by the sum of the rounded weights, then rounded to
+ * e5m2 (nearest even, saturating).  Other conventions as attn_fwd.
+ * Pointers, shape fields T / max_seq_len: as attn_fwd (T ignored). */
+attn_status attn_fwd_f8(const attn_shape* shape,
+                        const void* q, const void* k, const void* vt,
+                        int causal, float sm_scale,
+                        void* o, float* lse, void* stream);
+
 /* attn_fwd_jvp for callers that may not allocate device memory: a framework
  * that owns every device allocation, a runtime that forbids cudaMalloc
  * while it records work, a real-time path with a frozen memory budget.

@@ -1,0 +1,144 @@
+"""GPU parity of the FP8 (e5m2) forward (attn_fwd_f8) against the FP8
+oracle (oracle.attention_fwd_e5m2: the tutorial's steps in float64 on the
+e5m2 inputs).
+
+Tolerance, derived from the arithmetic (the pages' own test allows atol 3):
+  * LSE within 1e-3: S is the exact e5m2 products summed in fp32 on both
+    sides; only the exponent and the log differ;
+  * O elementwise.  Both sides round every weight w_j to e5m2 (|d_j| <=
+    2^-3), but the kernel rounds it relative to its running maximum, which
+    does not trail the row maximum by a power of two, so its rounding
+    decisions are independent of the oracle's.  With B = sum_j w_j |V_j| and
+    O_x the exact output (oracle.e5m2_bound_terms): the oracle (row sum of
+    the unrounded weights) moves by at most 2^-3 B, the kernel (row sum of
+    the rounded ones) by at most 0.143 (B + |O_x|), and each output rounding
+    by 2^-3 of its value:
+        |O - O_oracle| <= 0.27 B + 0.15 |O_x| + 2^-3 (|O| + |O_oracle|) + 2^-15
+    (2^-15: twice the subnormal spacing of e5m2);
+  * O in aggregate: ||O - O_oracle||_2 <= 0.2 ||O_oracle||_2.  Two
+    independent roundings to a grid of relative spacing <= 2^-2 differ by
+    at most 2^-2 / sqrt(6) = 0.10 relative RMS; the weights add less unless
+    a row has very few keys.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_forward_jvp_gb300 import binding, build
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    binding.lib()
+
+
+def make_f8(B, H, M, N, D, seed, std=1.0):
+    """q, k, v drawn like the other workloads (randn fp32 x std), rounded to
+    e5m2; v in its natural [B, H, N, D] orientation."""
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(B, H, M, D, generator=g) * std).to(torch.float8_e5m2)
+    k = (torch.randn(B, H, N, D, generator=g) * std).to(torch.float8_e5m2)
+    v = (torch.randn(B, H, N, D, generator=g) * std).to(torch.float8_e5m2)
+    return q, k, v
+
+
+def run_f8(q, k, v, causal, sm_scale):
+    vt = v.transpose(-1, -2).contiguous()
+    o, lse = binding.attn_fwd_f8(q.cuda(), k.cuda(), vt.cuda(), causal=causal, sm_scale=sm_scale)
+    assert binding.sync_check() == 0
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def assert_f8_close(O, L, Or, Lr, Bt, Ox, what):
+    assert np.isfinite(O).all(), what
+    inf_r = np.isneginf(Lr)
+    assert np.array_equal(np.isneginf(L), inf_r), f"{what}: empty-row LSE pattern"
+    if (~inf_r).any():
+        el = np.abs(L[~inf_r] - Lr[~inf_r]).max()
+        assert el <= 1e-3, f"{what}: LSE err {el:.3e}"
+    bound = 0.27 * Bt + 0.15 * np.abs(Ox) + 2.0 ** -3 * (np.abs(O) + np.abs(Or)) + 2.0 ** -15
+    bad = np.abs(O - Or) > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements outside the bound, e.g. {O[bad][:4]} vs {Or[bad][:4]}"
+    rel = np.linalg.norm(O - Or) / max(np.linalg.norm(Or), 1e-30)
+    assert rel <= 0.2, f"{what}: relative L2 {rel:.3f}"
+    return rel
+
+
+def bound_terms(q, k, v, causal, s):
+    B, H = q.shape[:2]
+    Bt = np.zeros(q.shape[:3] + (v.shape[3],))
+    Ox = np.zeros_like(Bt)
+    for b in range(B):
+        for h in range(H):
+            Bt[b, h], Ox[b, h] = oracle.e5m2_bound_terms(*(oracle.to_f64(t[b, h]) for t in (q, k, v)), s, causal)
+    return Bt, Ox
+
+
+CASES = [
+    ("causal_d128", dict(B=1, H=2, M=640, N=640, D=128, causal=True)),
+    ("nc_d64_ragged", dict(B=2, H=1, M=300, N=512, D=64, causal=False)),
+    ("nc_d128", dict(B=1, H=2, M=200, N=1024, D=128, causal=False)),
+    ("one_query", dict(B=1, H=2, M=1, N=256, D=128, causal=False)),
+    ("sixteen_keys", dict(B=1, H=2, M=130, N=16, D=64, causal=False)),
+    ("causal_d64", dict(B=1, H=3, M=384, N=384, D=64, causal=True)),
+]
+
+
+@pytest.mark.parametrize("name,c", CASES, ids=[c[0] for c in CASES])
+def test_fp8_parity(name, c):
+    q, k, v = make_f8(c["B"], c["H"], c["M"], c["N"], c["D"], seed=5)
+    s = c["D"] ** -0.5
+    O, L = run_f8(q, k, v, c["causal"], s)
+    Or, Lr = oracle.attention_fwd_e5m2(q, k, v, causal=c["causal"], sm_scale=s)
+    assert_f8_close(O, L, Or, Lr, *bound_terms(q, k, v, c["causal"], s), name)
+
+
+def test_fp8_full_size_sampled_heads():
+    # the benchmark's shape (B2 H16 N4096 D128 causal) in e5m2; two heads
+    # checked whole against the oracle
+    q, k, v = make_f8(2, 16, 4096, 4096, 128, seed=0)
+    s = 128 ** -0.5
+    O, L = run_f8(q, k, v, True, s)
+    for b, h in ((0, 3), (1, 12)):
+        args = [oracle.to_f64(t[b, h]) for t in (q, k, v)]
+        Or, Lr = oracle.head_fwd_e5m2(*args, s, causal=True)
+        Bt, Ox = oracle.e5m2_bound_terms(*args, s, causal=True)
+        assert_f8_close(O[b, h], L[b, h], Or, Lr, Bt, Ox, f"head {b},{h}")
+
+
+def test_fp8_no_keys_and_unsupported():
+    q, k, v = make_f8(1, 1, 70, 0, 64, seed=2)
+    O, L = run_f8(q, k, v, False, 0.125)
+    assert np.all(O == 0) and np.all(np.isneginf(L))
+    q, k, v = make_f8(1, 1, 64, 100, 64, seed=3)   # 100 keys: V^T rows not 16-byte multiples
+    with pytest.raises(binding.AttnError) as e:
+        binding.attn_fwd_f8(q.cuda(), k.cuda(), v.transpose(-1, -2).contiguous().cuda())
+    assert e.value.status == 2
+
+
+@pytest.mark.parametrize("N", [0, 256])
+def test_fp8_guard_bands(N):
+    # o and lse carved out of larger buffers filled with a pattern: the
+    # kernel writes exactly o's and lse's bytes (with and without keys)
+    B, H, M, D = 1, 2, 70, 64
+    q, k, v = make_f8(B, H, M, N, D, seed=9)
+    G = 4096
+    obuf = torch.full((G + B * H * M * D + G,), 0x5a, dtype=torch.uint8, device="cuda")
+    lbuf = torch.full((G // 4 + B * H * M + G // 4,), 7.0, dtype=torch.float32, device="cuda")
+    o = obuf[G:G + B * H * M * D].view(torch.float8_e5m2).view(B, H, M, D)
+    lse = lbuf[G // 4:G // 4 + B * H * M].view(B, H, M)
+    binding.attn_fwd_f8(q.cuda(), k.cuda(), v.transpose(-1, -2).contiguous().cuda(), sm_scale=0.125,
+                        out=(o, lse))
+    assert binding.sync_check() == 0
+    assert torch.all(obuf[:G] == 0x5a) and torch.all(obuf[G + B * H * M * D:] == 0x5a)
+    assert torch.all(lbuf[:G // 4] == 7.0) and torch.all(lbuf[G // 4 + B * H * M:] == 7.0)
+    if N == 0:
+        assert torch.all(o.view(torch.uint8) == 0) and torch.all(torch.isneginf(lse))
+    else:
+        assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
