@@ -227,3 +227,24 @@ def min_hbm_bytes_bwd(w: Workload, rows: Optional[int] = None) -> int:
     n += 2 * (rows_q * w.Dqk + rows_k * (w.Dqk + w.Dv))
     n += 2 * 4 * rows_q                      # Delta out + in
     return n
+
+
+def make_f8_inputs(w: Workload, seed: int = 0) -> dict:
+    """Inputs of the FP8 forward for dense workload ``w``: ``q, k, v`` drawn
+    as ``randn`` fp32 times ``input_std`` in that order, rounded to
+    float8_e5m2 (v in its natural [B, H, N, Dv] orientation), and ``vt``,
+    v transposed to [B, H, Dv, N] and made contiguous (the FP8 layout)."""
+    assert not w.jagged and w.Dqk == w.Dv
+    g = torch.Generator().manual_seed(seed)
+
+    def draw(shape):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if w.input_std != 1.0:
+            x = x * w.input_std
+        return x.to(torch.float8_e5m2)
+
+    q = draw((w.B, w.H, w.M, w.Dqk))
+    k = draw((w.B, w.H, w.N, w.Dqk))
+    v = draw((w.B, w.H, w.N, w.Dv))
+    return {"workload": w, "sm_scale": w.scale, "causal": w.causal, "q": q, "k": k, "v": v,
+            "vt": v.transpose(-1, -2).contiguous()}

@@ -15,6 +15,11 @@ is bracketed by barriers and the slowest rank's time is used.
 --impl reference times the float64 CPU oracle on the host cores (rank 0
 only) on a bounded sample of the same workload: each step is one head.
 
+--op fwd_f8 measures the FP8 (e5m2) forward (q, k, v in e5m2, V
+transposed, O in e5m2) on a dense workload: a step is one launch; FLOPs are
+the forward's two matmuls per score element; the roofline peak is the
+measured bf16 peak times the nominal fp8 / bf16 rate (2).
+
 --op bwd measures the attention backward instead (dense workloads): a step
 is one backward -- the Delta launch, the dQ pass and the dK / dV pass --
 given the forward's O and LSE (computed before the timed region).  FLOPs
@@ -39,12 +44,14 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from attention_forward_jvp_gb300.workloads import (WORKLOADS, flops_bwd, flops_fwd_jvp, make_bwd_inputs,  # noqa: E402
-                                                   make_inputs, min_hbm_bytes, min_hbm_bytes_bwd,
-                                                   score_elements)
+from attention_forward_jvp_gb300.workloads import (WORKLOADS, flops_bwd, flops_fwd, flops_fwd_jvp,  # noqa: E402
+                                                   make_bwd_inputs, make_f8_inputs, make_inputs,
+                                                   min_hbm_bytes, min_hbm_bytes_bwd, score_elements)
 
 METRIC = "attn fwd+JVP TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 tensor peak"
 METRIC_BWD = "attn backward (dQ, dK, dV) TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 tensor peak"
+METRIC_F8 = "attn FP8 (e5m2) forward TFLOP/s (1xGB300) and fraction of the fp8 tensor peak"
+FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense fp8 : bf16 tensor rate of a GB300
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 10**6  # GB300 L2
 
@@ -585,6 +592,145 @@ def run_ours_bwd(args, w, world, rank, local):
     return 0
 
 
+# -------------------------------------------------------------- fp8 forward
+def oracle_sample_f8(w, inp, n_units: int, start: int = 0):
+    import oracle
+    BH = w.B * w.H
+    t0 = time.perf_counter()
+    for i in range(n_units):
+        b, h = divmod((start + i) % BH, w.H)
+        oracle.head_fwd_e5m2(*(oracle.to_f64(inp[n][b, h]) for n in ("q", "k", "v")), inp["sm_scale"],
+                             causal=w.causal)
+    return time.perf_counter() - t0, flops_fwd(w) / BH * n_units
+
+
+def run_reference_f8(args, w, world, rank):
+    if rank != 0:
+        return 0
+    inp = make_f8_inputs(w, seed=0)
+    for i in range(args.warmup):
+        oracle_sample_f8(w, inp, 1, start=i)
+    tot = fl = 0.0
+    for i in range(args.steps):
+        dt, fl = oracle_sample_f8(w, inp, 1, start=args.warmup + i)
+        tot += dt
+    value = fl * args.steps / tot / 1e12
+    desc = f"each step: one of {w.B * w.H} (batch, head) pairs of the {w.name} workload in e5m2, float64 NumPy"
+    line = {
+        "impl": "reference", "metric": METRIC_F8, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w).replace("fwd+JVP", "FP8 forward"), "sample_per_step": "one head"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_f8(args, w, world, rank, local):
+    from attention_forward_jvp_gb300 import binding
+    from attention_forward_jvp_gb300 import build as _b
+
+    if w.jagged or w.bias or w.mask_keep is not None or w.Dqk != w.Dv or w.Dqk not in (64, 128):
+        raise SystemExit(f"--op fwd_f8 runs dense workloads without bias / mask, D in {{64, 128}} ({w.name} is not)")
+    if not os.path.exists(_b.LIB_PATH):
+        _b.build()
+    binding.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = make_f8_inputs(w, seed=0)
+    q, k, vt = (inp[n].to(dev) for n in ("q", "k", "vt"))
+    kw = dict(causal=w.causal, sm_scale=inp["sm_scale"])
+    out = binding.attn_fwd_f8(q, k, vt, **kw)
+    stream = torch.cuda.current_stream(dev)
+    flops = flops_fwd(w)
+    io_bytes = q.numel() + k.numel() + vt.numel() + out[0].numel() + out[1].numel() * 4
+    flush = io_bytes < 2 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            binding.attn_fwd_f8(q, k, vt, out=out, **kw)
+        st = binding.sync_check(stream)
+        if st != 0:
+            raise RuntimeError(f"device error during warm-up: {binding.status_string(st)}")
+        barrier(world)
+        torch.cuda.synchronize()
+        n0 = binding.launch_count()
+        clk.mark("timed")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            if flush:
+                flush_buf.fill_(float(i))
+            ev[i][0].record(stream)
+            binding.attn_fwd_f8(q, k, vt, out=out, **kw)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        clk.mark("after")
+        barrier(world)
+        launches = binding.launch_count() - n0
+    st = binding.sync_check(stream)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {binding.status_string(st)}")
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    hin = [inp[n].pin_memory() for n in ("q", "k", "vt")]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    hout = binding.attn_fwd_f8(*hin, **kw)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+    e2e_steps = max(1, min(args.steps, 10))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        hout = binding.attn_fwd_f8(*hin, **kw)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+    if rank != 0:
+        return 0
+    pk, pk_kind = peaks()
+    peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * FP8_OVER_BF16
+    achieved = flops / (ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": None, "kernel": "attn_fwd_kernel<D, D, no JVP, no bias, e5m2>",
+            "peak_kind": f"{pk_kind} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8 / bf16 dense rate)",
+            "algorithmic_bytes": io_bytes, "hbm_gbs": io_bytes / (ms * 1e-3) / 1e9}
+    cpu = None
+    if world == 1 and not args.skip_cpu_baseline:
+        dt = fl = 0.0
+        n = 0
+        while n < w.B * w.H and (n == 0 or dt < args.cpu_seconds):
+            d1, f1 = oracle_sample_f8(w, inp, 1, start=n)
+            dt += d1
+            fl += f1
+            n += 1
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n} of {w.B * w.H} (batch, head) pairs of the {w.name} workload in e5m2, float64 NumPy",
+               "seconds": dt}
+    line = {
+        "metric": METRIC_F8, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e5m2", "data": "synthetic",
+        "config": {"workload": describe(w).replace("fwd+JVP", "FP8 forward"), "flops_per_step": flops,
+                   "l2": ("L2 flushed before each step (%d MB written)" % (2 * L2_BYTES // 10**6)
+                          if flush else "inputs larger than L2, no flush"),
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": value / world / peak,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "kernel_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,8 +741,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="approximate seconds of oracle work in the CPU-baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="fwd_jvp", choices=["fwd_jvp", "bwd"],
-                    help="fwd_jvp: the fused forward + JVP (default); bwd: the backward")
+    ap.add_argument("--op", default="fwd_jvp", choices=["fwd_jvp", "bwd", "fwd_f8"],
+                    help="fwd_jvp: the fused forward + JVP (default); bwd: the backward; "
+                         "fwd_f8: the FP8 (e5m2) forward")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]
@@ -604,6 +751,9 @@ def main():
     if args.op == "bwd":
         rc = (run_reference_bwd(args, w, world, rank) if args.impl == "reference"
               else run_ours_bwd(args, w, world, rank, local))
+    elif args.op == "fwd_f8":
+        rc = (run_reference_f8(args, w, world, rank) if args.impl == "reference"
+              else run_ours_f8(args, w, world, rank, local))
     elif args.impl == "reference":
         rc = run_reference(args, w, world, rank)
     else:
