@@ -571,30 +571,68 @@ cudaError_t launch_attn_bwd(const BwdParams& bp, int grid, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
-// Delta = rowsum(dO o O) over [rows, d] (one warp per row, fp32 sums).
+// Delta = rowsum(dO o O) over [rows, d], fp32 sums.  A warp takes four rows
+// at a time, each lane d / 32 consecutive elements of each (one 8-, 4- or
+// 2-byte load per row and operand), so eight loads are in flight per lane
+// before the first reduction; d = 16 leaves half the lanes idle.
+template <bool F16>
+__device__ __forceinline__ float dot2(uint32_t a, uint32_t b) {
+  float a0, a1, b0, b1;
+  if constexpr (F16) {
+    a0 = __half2float(__ushort_as_half(static_cast<uint16_t>(a & 0xffffu)));
+    a1 = __half2float(__ushort_as_half(static_cast<uint16_t>(a >> 16)));
+    b0 = __half2float(__ushort_as_half(static_cast<uint16_t>(b & 0xffffu)));
+    b1 = __half2float(__ushort_as_half(static_cast<uint16_t>(b >> 16)));
+  } else {
+    a0 = __uint_as_float(a << 16);
+    a1 = __uint_as_float(a & 0xffff0000u);
+    b0 = __uint_as_float(b << 16);
+    b1 = __uint_as_float(b & 0xffff0000u);
+  }
+  return fmaf(a1, b1, a0 * b0);
+}
+
 template <bool F16>
 __global__ void attn_bwd_delta_kernel(const uint16_t* o, const uint16_t* dout, float* delta,
                                       long long rows, int d) {
   const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  for (long long r = wid; r < rows; r += nw) {
-    float acc = 0.f;
-    for (int c = lane; c < d; c += 32) {
-      const uint16_t a = o[r * d + c], b = dout[r * d + c];
-      float fa, fb;
-      if constexpr (F16) {
-        fa = __half2float(__ushort_as_half(a));
-        fb = __half2float(__ushort_as_half(b));
+  const int per = d >> 5;  // elements per lane: 4, 2, 1 (d = 128, 64, 32); 0 for d = 16
+  for (long long r0 = wid * 4; r0 < rows; r0 += nw * 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const long long r = r0 + k;
+      if (r >= rows) break;
+      const long long base = r * d;
+      if (per == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(o + base + lane * 4);
+        const uint2 b = *reinterpret_cast<const uint2*>(dout + base + lane * 4);
+        acc[k] = dot2<F16>(a.x, b.x) + dot2<F16>(a.y, b.y);
+      } else if (per == 2) {
+        acc[k] = dot2<F16>(*reinterpret_cast<const uint32_t*>(o + base + lane * 2),
+                           *reinterpret_cast<const uint32_t*>(dout + base + lane * 2));
       } else {
-        fa = __uint_as_float(static_cast<uint32_t>(a) << 16);
-        fb = __uint_as_float(static_cast<uint32_t>(b) << 16);
+        for (int c = lane; c < d; c += 32) {
+          const uint32_t a = o[base + c], b = dout[base + c];
+          acc[k] = fmaf(F16 ? __half2float(__ushort_as_half(static_cast<uint16_t>(a))) : __uint_as_float(a << 16),
+                        F16 ? __half2float(__ushort_as_half(static_cast<uint16_t>(b))) : __uint_as_float(b << 16),
+                        acc[k]);
+        }
       }
-      acc = fmaf(fa, fb, acc);
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) delta[r] = acc;
+    for (int s = 16; s > 0; s >>= 1)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], s);
+    if (lane < 4 && r0 + lane < rows) {
+      float v = acc[0];
+#pragma unroll
+      for (int k = 1; k < 4; ++k)
+        if (lane == k) v = acc[k];
+      delta[r0 + lane] = v;
+    }
   }
 }
 

@@ -568,7 +568,7 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
   // Delta = rowsum(dO o O)
   if (rows_q && (stages & ATTN_BWD_DELTA)) {
     const long long rows = (jagged ? static_cast<long long>(s->H) : static_cast<long long>(BH)) * n_q;
-    const long long want = (rows + 7) / 8;  // 8 warps (rows) per 256-thread block
+    const long long want = (rows + 31) / 32;  // 8 warps x 4 rows per 256-thread block
     const int blocks = static_cast<int>(want < 16LL * ds->num_sms ? want : 16LL * ds->num_sms);
     if (f16)
       attn::attn_bwd_delta_kernel<true><<<blocks, 256, 0, cs>>>(
