@@ -80,9 +80,12 @@ struct BwdPlan {
   static constexpr int OFF_R = 0;
   static constexpr int OFF_T = RSET;
   static constexpr int OFF_BAR = OFF_T + NS * T_STAGE;
-  // barriers: r_full, r_empty, t_full[NS], t_empty[NS], s_full[NSB], p_full[NSB], drain
+  // barriers: r_full, r_empty, t_full[NS], t_empty[NS], s_full[NSB],
+  // p_full[NSB], drain (score issuer), o_done[NSB] (the output chain that
+  // read score buffer b is done), drain (output issuer)
   static constexpr int B_RF = 0, B_RE = 1, B_TF = 2, B_TE = B_TF + NS, B_SF = B_TE + NS,
-                       B_PF = B_SF + NSB, B_DRAIN = B_PF + NSB, NBAR = B_DRAIN + 1;
+                       B_PF = B_SF + NSB, B_DRAIN = B_PF + NSB, B_OD = B_DRAIN + 1,
+                       B_DRAIN2 = B_OD + NSB, NBAR = B_DRAIN2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // KV pass: per elementwise warp, the current query tile's 32 column
   // values of -LSE log2(e) then -Delta
@@ -183,8 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     for (int i = 0; i < P::NSB; ++i) {
       mbar_init(bar(P::B_SF + i), 1);
       mbar_init(bar(P::B_PF + i), 8);  // one arrival per elementwise warp
+      mbar_init(bar(P::B_OD + i), 1);
     }
     mbar_init(bar(P::B_DRAIN), 1);
+    mbar_init(bar(P::B_DRAIN2), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -250,8 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         if (rfill > 0) drain_bar(bar(P::B_RF), (rfill - 1) & 1u, p.timeout_ns);
       }
       __syncwarp();
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 3) {
+      // ------------------------------------------------------- MMA issuers
+      // Two issuing warps on different sub-partitions: warp 1 the score
+      // chains, warp 3 the output chains.  An issuing warp's waits, commits
+      // and fences queue behind its own MMAs, so a single issuer stalls at
+      // every wait while the tensor pipe drains; with two, each one's waits
+      // overlap the other's MMAs.  Ordering between them runs through
+      // barriers completed by tcgen05.commit of the warp whose MMAs must
+      // finish first: s_full (scores of tile g ready) -> elementwise ->
+      // p_full -> output chain of g -> o_done (its score buffer may be
+      // overwritten) -> score chains of tile g + NSB.  Each wait is gated by
+      // a phase the waiter itself enables, so no parity wait can alias.
       const bool leader = elect_one();
       constexpr uint32_t idesc_s = idesc_16(kBM, P::TN, false, F16);  // score chains, N = 64
       constexpr uint32_t idesc_a = idesc_16(kBM, D, true, F16);       // output chains, N = D
@@ -267,114 +282,106 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const uint32_t lo_r2 = lo_r1 + (P::R_TILE >> 4);
       const uint32_t lo_t = sdesc_lo(sbase + P::OFF_T, 16);
       const uint32_t lo_tmn = sdesc_lo(sbase + P::OFF_T, P::T_SUB);
-      // output chain(s) of tile t (its ring stage is t % NS); the first
-      // tile of a unit zero-initialises the accumulators
-      // (`waited`: the caller has already waited for its P / dS)
-      auto issue_out = [&](uint32_t t, bool first, bool waited) -> bool {
-        const uint32_t sb = t % P::NSB;
-        if (!waited) {
-          if (!wait_all(bar(P::B_PF + sb), (t / P::NSB) & 1u)) return false;
-          tc_fence_after();
-        }
-        const uint32_t ts = t % P::NS;
-        const uint32_t lm = lo_tmn + ts * (P::T_STAGE >> 4);
-        // 16-bit operands over the Y columns: half h at Y + 32 h holds
-        // P^T (KV pass) at +0 and dS at +16 (KV) / +0 (dQ pass), 8 packed
-        // columns per 16 streamed rows
-        const uint32_t aY = tmem + sb * P::SBUF + P::TN;
-        if (KV) {
-          // dV += P^T dO
-#pragma unroll
-          for (int kk = 0; kk < P::TN / 16; ++kk) {
-            const uint64_t db = sdesc_join(lm + ((P::T_TILE + kk * 2048) >> 4), kHi);
-            if (leader)
-              mma_ts(tmem + P::COL_A, aY + 32 * (kk >> 1) + 8 * (kk & 1), db, idesc_a,
-                     (first && kk == 0) ? 0u : 1u);
-            __syncwarp();
-          }
-        }
-        // dQ += dS K   /   dK += dS^T Q
-        const uint32_t acc = tmem + P::COL_A + (KV ? D : 0);
-        const uint32_t ds_off = KV ? 16u : 0u;
-#pragma unroll
-        for (int kk = 0; kk < P::TN / 16; ++kk) {
-          const uint64_t db = sdesc_join(lm + ((kk * 2048) >> 4), kHi);
-          if (leader)
-            mma_ts(acc, aY + 32 * (kk >> 1) + ds_off + 8 * (kk & 1), db, idesc_a,
-                   (first && kk == 0) ? 0u : 1u);
-          __syncwarp();
-        }
-        if (leader) tc_commit(bar(P::B_TE + ts));  // also: this tile's output MMAs done
-        __syncwarp();
-        return true;
-      };
-      // Score chains run up to NSB - 1 tiles ahead of the output chains, so
-      // the tensor pipe has them queued while the elementwise warps work.
-      // With two tiles of lookahead the issuer waits once per tile -- for the
-      // tile's operands and for the P / dS of the output chain it issues
-      // next (long since written) -- then issues the score chains and that
-      // output chain as one batch: the tensor pipe's instruction queue is
-      // short, and every pause of the issuer between MMAs leaves it idle.
-      // With one tile of lookahead that P / dS is still being computed when
-      // the next score chains can go, so those go first.
-      constexpr int kAhead = P::NSB - 1;
-      constexpr bool kHoist = kAhead >= 2;
-      uint32_t ruse = 0, g = 0;
       bool ok = true;
-      for (int rnd = 0; ok; ++rnd) {
-        const int u = unit_at(rnd);
-        if (u >= p.num_units) break;
-        const BwdUnit w = bwd_unit<KV>(p, u);
-        if (w.nt == 0) continue;
-        ok = wait_all(bar(P::B_RF), ruse & 1u);
-        if (!ok) break;
-        const uint32_t g0 = g;
-        for (int j = 0; j < w.nt; ++j, ++g) {
-          const uint32_t ts = g % P::NS;
-          ok = wait_all(bar(P::B_TF + ts), (g / P::NS) & 1u);
-          if (kHoist && ok && j >= kAhead) {
-            const uint32_t t = g - kAhead;
-            ok = wait_all(bar(P::B_PF + t % P::NSB), (t / P::NSB) & 1u);
-            tc_fence_after();
-          }
+      uint32_t g = 0;  // tile counter over units with tiles (same in every role)
+      if (warp == 1) {
+        uint32_t ruse = 0;
+        for (int rnd = 0; ok; ++rnd) {
+          const int u = unit_at(rnd);
+          if (u >= p.num_units) break;
+          const BwdUnit w = bwd_unit<KV>(p, u);
+          if (w.nt == 0) continue;
+          ok = wait_all(bar(P::B_RF), ruse & 1u);
           if (!ok) break;
-          const uint32_t lt = lo_t + ts * (P::T_STAGE >> 4);
-          const uint32_t dX = tmem + (g % P::NSB) * P::SBUF;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
-            const uint32_t ob = ((kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
-            if (leader) mma_ss(dX, sdesc_join(lo_r1 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
-            __syncwarp();
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
-            const uint32_t ob = (P::T_TILE + (kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
-            if (leader)
-              mma_ss(dX + P::TN, sdesc_join(lo_r2 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
-            __syncwarp();
-          }
-          if (leader) {
-            tc_commit(bar(P::B_SF + g % P::NSB));
-            // the unit's last score chain: the row operands are free once it
-            // is done (the output chains never read them)
-            if (j == w.nt - 1) tc_commit(bar(P::B_RE));
-          }
-          __syncwarp();
-          if (j >= kAhead) {
-            ok = issue_out(g - kAhead, j == kAhead, kHoist);
+          for (int j = 0; j < w.nt; ++j, ++g) {
+            const uint32_t ts = g % P::NS, sb = g % P::NSB;
+            // the tile's operands, and the output chain that last read this
+            // score buffer (tile g - NSB; a fresh barrier passes)
+            ok = wait_all(bar(P::B_TF + ts), (g / P::NS) & 1u) &&
+                 wait_all(bar(P::B_OD + sb), ((g / P::NSB) & 1u) ^ 1u);
             if (!ok) break;
+            tc_fence_after();
+            const uint32_t lt = lo_t + ts * (P::T_STAGE >> 4);
+            const uint32_t dX = tmem + sb * P::SBUF;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
+              const uint32_t ob = ((kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
+              if (leader) mma_ss(dX, sdesc_join(lo_r1 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
+              __syncwarp();
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
+              const uint32_t ob = (P::T_TILE + (kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
+              if (leader)
+                mma_ss(dX + P::TN, sdesc_join(lo_r2 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
+              __syncwarp();
+            }
+            if (leader) {
+              tc_commit(bar(P::B_SF + sb));
+              // the unit's last score chain: the row operands are free once
+              // it is done (the output chains never read them)
+              if (j == w.nt - 1) tc_commit(bar(P::B_RE));
+            }
+            __syncwarp();
+          }
+          ++ruse;
+        }
+        if (leader) {
+          tc_commit(bar(P::B_DRAIN));
+          drain_bar(bar(P::B_DRAIN), 0, p.timeout_ns);
+        }
+      } else {
+        for (int rnd = 0; ok; ++rnd) {
+          const int u = unit_at(rnd);
+          if (u >= p.num_units) break;
+          const BwdUnit w = bwd_unit<KV>(p, u);
+          if (w.nt == 0) continue;
+          for (int j = 0; j < w.nt; ++j, ++g) {
+            const uint32_t sb = g % P::NSB, ts = g % P::NS;
+            ok = wait_all(bar(P::B_PF + sb), (g / P::NSB) & 1u);
+            if (!ok) break;
+            tc_fence_after();
+            const bool first = j == 0;  // zero-initialises the accumulators
+            const uint32_t lm = lo_tmn + ts * (P::T_STAGE >> 4);
+            // 16-bit operands over the Y columns: half h at Y + 32 h holds
+            // P^T (KV pass) at +0 and dS at +16 (KV) / +0 (dQ pass), 8
+            // packed columns per 16 streamed rows
+            const uint32_t aY = tmem + sb * P::SBUF + P::TN;
+            if (KV) {
+              // dV += P^T dO
+#pragma unroll
+              for (int kk = 0; kk < P::TN / 16; ++kk) {
+                const uint64_t db = sdesc_join(lm + ((P::T_TILE + kk * 2048) >> 4), kHi);
+                if (leader)
+                  mma_ts(tmem + P::COL_A, aY + 32 * (kk >> 1) + 8 * (kk & 1), db, idesc_a,
+                         (first && kk == 0) ? 0u : 1u);
+                __syncwarp();
+              }
+            }
+            // dQ += dS K   /   dK += dS^T Q
+            const uint32_t acc = tmem + P::COL_A + (KV ? D : 0);
+            const uint32_t ds_off = KV ? 16u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < P::TN / 16; ++kk) {
+              const uint64_t db = sdesc_join(lm + ((kk * 2048) >> 4), kHi);
+              if (leader)
+                mma_ts(acc, aY + 32 * (kk >> 1) + ds_off + 8 * (kk & 1), db, idesc_a,
+                       (first && kk == 0) ? 0u : 1u);
+              __syncwarp();
+            }
+            if (leader) {
+              tc_commit(bar(P::B_TE + ts));  // stage free (the tile's score chains finished first)
+              tc_commit(bar(P::B_OD + sb));  // score buffer free
+            }
+            __syncwarp();
           }
         }
-        if (!ok) break;
-        // the unit's remaining output chains
-        for (uint32_t t = (w.nt > kAhead ? g - kAhead : g0); ok && t < g; ++t) ok = issue_out(t, t == g0, false);
-        ++ruse;
-      }
-      if (leader) {
-        tc_commit(bar(P::B_DRAIN));
-        drain_bar(bar(P::B_DRAIN), 0, p.timeout_ns);
+        if (leader) {
+          tc_commit(bar(P::B_DRAIN2));
+          drain_bar(bar(P::B_DRAIN2), 0, p.timeout_ns);
+        }
       }
       __syncwarp();
     }
