@@ -286,7 +286,7 @@ BWD_DELTA, BWD_DQ, BWD_DKDV, BWD_ALL = 1, 2, 4, 7
 def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float] = None,
              offsets: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
              out=None, stages: int = BWD_ALL):
-    """Attention backward (no bias / mask, Dqk == Dv).  Takes the forward's
+    """Attention backward (no bias / mask).  Takes the forward's
     inputs, its output ``o`` and log-sum-exp ``lse`` and the gradient ``do``
     of O; returns (dq, dk, dv, delta), delta = rowsum(do o o) in float32.
     Dense ``[B, H, M|N, D]`` or jagged ``[H, T, D]`` with int32 ``offsets``

@@ -31,6 +31,8 @@
 //           written as 16-bit operands over the thread's own dP columns;
 //           the epilogue scales and stores the accumulators.
 #pragma once
+#include <type_traits>
+
 #include "attn_kernel.cuh"
 
 namespace attn {
@@ -52,27 +54,32 @@ struct BwdParams {
   const float* delta;  // same layout as lse
   uint16_t* out1;      // dQ pass: dQ; KV pass: dK
   uint16_t* out2;      // KV pass: dV
-  int d_out;           // head dim of the tensors (D, or 16 / 32 padded to D = 64)
+  int d_qk;            // row width of q, k, dq, dk (Dqk; 16 / 32 run padded to 64)
+  int d_v;             // row width of v, o, do, dv
   int* err;
   unsigned long long timeout_ns;
 };
 
-template <int D, bool KV>
+template <int DQK, int DV, bool KV>
 struct BwdPlan {
   static constexpr int TN = 64;                      // streamed rows per tile
   static constexpr int R_SUB = kBM * 128;            // 64-column chunk of a row operand
   static constexpr int T_SUB = TN * 128;             // 64-column chunk of a streamed tile
-  static constexpr int R_TILE = (D / 64) * R_SUB;
-  static constexpr int T_TILE = (D / 64) * T_SUB;
-  static constexpr int RSET = 2 * R_TILE;            // R1 then R2
-  static constexpr int T_STAGE = 2 * T_TILE;         // T1 then T2
+  // row operands R1 (Q / K, Dqk wide) then R2 (dO / V, Dv wide); streamed
+  // T1 (K / Q, Dqk) then T2 (V / dO, Dv)
+  static constexpr int R1_TILE = (DQK / 64) * R_SUB;
+  static constexpr int R2_TILE = (DV / 64) * R_SUB;
+  static constexpr int T1_TILE = (DQK / 64) * T_SUB;
+  static constexpr int T2_TILE = (DV / 64) * T_SUB;
+  static constexpr int RSET = R1_TILE + R2_TILE;
+  static constexpr int T_STAGE = T1_TILE + T2_TILE;
   static constexpr int BUDGET = 227 * 1024 - 4096;
   static constexpr int NS = (RSET + 4 * T_STAGE <= BUDGET) ? 4 : (RSET + 3 * T_STAGE <= BUDGET) ? 3 : 2;
   // TMEM: score buffer b = [X (64 fp32: S or S^T) | Y (64 fp32: dP or dP^T)]
   // at b * 128, three buffers where the accumulators leave room, else two;
-  // accumulators after them: dQ pass dQ (D); KV pass dV (D), dK (D)
+  // accumulators after them: dQ pass dQ (Dqk); KV pass dV (Dv), dK (Dqk)
   static constexpr int SBUF = 2 * TN;
-  static constexpr int NACC = (KV ? 2 : 1) * D;
+  static constexpr int NACC = KV ? DV + DQK : DQK;
   static constexpr int NSB = (3 * SBUF + NACC <= 512) ? 3 : 2;
   static constexpr int COL_A = NSB * SBUF;
   static constexpr int COLS_USED = COL_A + NACC;
@@ -94,7 +101,7 @@ struct BwdPlan {
   static constexpr int SMEM_LAUNCH = SMEM_BYTES > 120 * 1024 ? SMEM_BYTES : 120 * 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
   static_assert(COLS_USED <= 512, "tensor memory plan exceeds 512 columns");
-  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static_assert((DQK == 64 || DQK == 128) && (DV == 64 || DV == 128), "head dims 64 or 128");
 };
 
 struct BwdUnit {
@@ -160,9 +167,9 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
   return w;
 }
 
-template <int D, bool KV, bool F16>
+template <int DQK, int DV, bool KV, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
-  using P = BwdPlan<D, KV>;
+  using P = BwdPlan<DQK, DV, KV>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -227,11 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           mbar_arrive_expect_tx(bar(P::B_RF), P::RSET);
           const int r = w.row0 + w.rt * kBM;
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
+          for (int c = 0; c < DQK / 64; ++c)
             tma_load_3d(sbase + P::OFF_R + c * P::R_SUB, &p.tm_r1, bar(P::B_RF), c * 64, r, w.z);
-            tma_load_3d(sbase + P::OFF_R + P::R_TILE + c * P::R_SUB, &p.tm_r2, bar(P::B_RF), c * 64, r,
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_3d(sbase + P::OFF_R + P::R1_TILE + c * P::R_SUB, &p.tm_r2, bar(P::B_RF), c * 64, r,
                         w.z);
-          }
           ++rfill;
           for (int j = 0; j < w.nt; ++j) {
             const int tr = w.row0 + (w.t0 + j) * P::TN;
@@ -241,10 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             mbar_arrive_expect_tx(bar(P::B_TF + ts), P::T_STAGE);
             const uint32_t dst = sbase + P::OFF_T + ts * P::T_STAGE;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < DQK / 64; ++c)
               tma_load_3d(dst + c * P::T_SUB, &p.tm_t1, bar(P::B_TF + ts), c * 64, tr, w.z);
-              tma_load_3d(dst + P::T_TILE + c * P::T_SUB, &p.tm_t2, bar(P::B_TF + ts), c * 64, tr, w.z);
-            }
+#pragma unroll
+            for (int c = 0; c < DV / 64; ++c)
+              tma_load_3d(dst + P::T1_TILE + c * P::T_SUB, &p.tm_t2, bar(P::B_TF + ts), c * 64, tr, w.z);
             ++tfill;
           }
         }
@@ -269,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       // a phase the waiter itself enables, so no parity wait can alias.
       const bool leader = elect_one();
       constexpr uint32_t idesc_s = idesc_16(kBM, P::TN, false, F16);  // score chains, N = 64
-      constexpr uint32_t idesc_a = idesc_16(kBM, D, true, F16);       // output chains, N = D
+      constexpr uint32_t idesc_k = idesc_16(kBM, DQK, true, F16);     // dQ / dK chains, N = Dqk
+      constexpr uint32_t idesc_v = idesc_16(kBM, DV, true, F16);      // dV chain, N = Dv
       auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, wait_bar(b, parity, W));
       };
@@ -279,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       // output chains' B, 64-column chunks T_SUB apart).
       constexpr uint32_t kHi = sdesc_hi_sw128(1024);
       const uint32_t lo_r1 = sdesc_lo(sbase + P::OFF_R, 16);
-      const uint32_t lo_r2 = lo_r1 + (P::R_TILE >> 4);
+      const uint32_t lo_r2 = lo_r1 + (P::R1_TILE >> 4);
       const uint32_t lo_t = sdesc_lo(sbase + P::OFF_T, 16);
       const uint32_t lo_tmn = sdesc_lo(sbase + P::OFF_T, P::T_SUB);
       bool ok = true;
@@ -304,16 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             const uint32_t lt = lo_t + ts * (P::T_STAGE >> 4);
             const uint32_t dX = tmem + sb * P::SBUF;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < DQK / 16; ++kk) {
               const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
               const uint32_t ob = ((kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
               if (leader) mma_ss(dX, sdesc_join(lo_r1 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
               __syncwarp();
             }
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < DV / 16; ++kk) {
               const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
-              const uint32_t ob = (P::T_TILE + (kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
+              const uint32_t ob = (P::T1_TILE + (kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
               if (leader)
                 mma_ss(dX + P::TN, sdesc_join(lo_r2 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
               __syncwarp();
@@ -353,21 +363,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
               // dV += P^T dO
 #pragma unroll
               for (int kk = 0; kk < P::TN / 16; ++kk) {
-                const uint64_t db = sdesc_join(lm + ((P::T_TILE + kk * 2048) >> 4), kHi);
+                const uint64_t db = sdesc_join(lm + ((P::T1_TILE + kk * 2048) >> 4), kHi);
                 if (leader)
-                  mma_ts(tmem + P::COL_A, aY + 32 * (kk >> 1) + 8 * (kk & 1), db, idesc_a,
+                  mma_ts(tmem + P::COL_A, aY + 32 * (kk >> 1) + 8 * (kk & 1), db, idesc_v,
                          (first && kk == 0) ? 0u : 1u);
                 __syncwarp();
               }
             }
             // dQ += dS K   /   dK += dS^T Q
-            const uint32_t acc = tmem + P::COL_A + (KV ? D : 0);
+            const uint32_t acc = tmem + P::COL_A + (KV ? DV : 0);
             const uint32_t ds_off = KV ? 16u : 0u;
 #pragma unroll
             for (int kk = 0; kk < P::TN / 16; ++kk) {
               const uint64_t db = sdesc_join(lm + ((kk * 2048) >> 4), kHi);
               if (leader)
-                mma_ts(acc, aY + 32 * (kk >> 1) + ds_off + 8 * (kk & 1), db, idesc_a,
+                mma_ts(acc, aY + 32 * (kk >> 1) + ds_off + 8 * (kk & 1), db, idesc_k,
                        (first && kk == 0) ? 0u : 1u);
               __syncwarp();
             }
@@ -406,12 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       if (w.nt == 0) {
         // no streamed tile touches these rows: zero gradients
         if (row_ok) {
-          const int ncol = min(D / 2, p.d_out - half * (D / 2));  // a multiple of 8
-          const long long off = (w.orow0 + ri) * p.d_out + half * (D / 2);
-          for (int c = 0; c < ncol; c += 8) {
-            *reinterpret_cast<uint4*>(p.out1 + off + c) = make_uint4(0u, 0u, 0u, 0u);
-            if (KV) *reinterpret_cast<uint4*>(p.out2 + off + c) = make_uint4(0u, 0u, 0u, 0u);
-          }
+          // this half's columns of each output row (a multiple of 8 each)
+          auto zero_row = [&](uint16_t* out, int width, int d_real) {
+            const int ncol = min(width / 2, d_real - half * (width / 2));
+            const long long off = (w.orow0 + ri) * d_real + half * (width / 2);
+            for (int c = 0; c < ncol; c += 8)
+              *reinterpret_cast<uint4*>(out + off + c) = make_uint4(0u, 0u, 0u, 0u);
+          };
+          zero_row(p.out1, DQK, p.d_qk);
+          if (KV) zero_row(p.out2, DV, p.d_v);
         }
         continue;
       }
@@ -518,14 +531,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       ok = __all_sync(0xffffffffu, wait_bar_sleep(bar(P::B_TE + tl_last % P::NS), (tl_last / P::NS) & 1u, W));
       if (!ok) break;
       tc_fence_after();
-      constexpr int DH = D / 2;     // columns per thread
-      constexpr int NW = DH / 2;    // packed words
-      constexpr int CW = NW / 4;
       const int q = lane & 3;
-      for (int which = 0; which < (KV ? 2 : 1); ++which) {
-        // dQ pass: dQ (scaled).  KV pass: which 0 = dV (unscaled), 1 = dK (scaled)
-        const uint32_t colA = P::COL_A + (KV ? (which == 0 ? 0 : D) : 0);
-        const float f = (KV && which == 0) ? 1.f : p.sm_scale;
+      // one accumulator of W columns: scale, round, transpose across lane
+      // quads, store whole row segments
+      auto store_acc = [&](auto width, uint32_t colA, float f, uint16_t* out, int d_real) {
+        constexpr int W = decltype(width)::value;
+        constexpr int DH = W / 2;   // columns per thread
+        constexpr int NW = DH / 2;  // packed words
+        constexpr int CW = NW / 4;
         uint32_t pw[NW];
 #pragma unroll
         for (int c0 = 0; c0 < DH; c0 += 32) {
@@ -537,16 +550,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             pw[c0 / 2 + i / 2] = pack2<F16>(__uint_as_float(v[i]) * f, __uint_as_float(v[i + 1]) * f);
         }
         quad_transpose<CW>(pw, q);
-        uint16_t* out = (KV && which == 0) ? p.out2 : p.out1;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int rk = w.rt * kBM + quad * 32 + (lane & ~3) + k;
           const int col = half * DH + q * 2 * CW;
-          if (rk < w.rows && col < p.d_out) {
-            const long long off = (w.orow0 + rk) * p.d_out + col;
+          if (rk < w.rows && col < d_real) {
+            const long long off = (w.orow0 + rk) * d_real + col;
             store_chunk<CW>(out + off, pw + k * CW, false);
           }
         }
+      };
+      if (KV) {
+        // dV (unscaled) then dK (scaled by s)
+        store_acc(std::integral_constant<int, DV>{}, P::COL_A, 1.f, p.out2, p.d_v);
+        store_acc(std::integral_constant<int, DQK>{}, P::COL_A + DV, p.sm_scale, p.out1, p.d_qk);
+      } else {
+        store_acc(std::integral_constant<int, DQK>{}, P::COL_A, p.sm_scale, p.out1, p.d_qk);
       }
     }
   }
@@ -557,24 +576,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, P::TMEM_COLS);
 }
 
-template <int D, bool KV, bool F16>
+template <int DQK, int DV, bool KV, bool F16>
 cudaError_t launch_attn_bwd(const BwdParams& bp, int grid, cudaStream_t stream) {
-  using P = BwdPlan<D, KV>;
+  using P = BwdPlan<DQK, DV, KV>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_done[dev]) {
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D, KV, F16>);
+    e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<DQK, DV, KV, F16>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_bwd_kernel<D, KV, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_bwd_kernel<DQK, DV, KV, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              P::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  attn_bwd_kernel<D, KV, F16><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(bp);
+  attn_bwd_kernel<DQK, DV, KV, F16><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(bp);
   return cudaGetLastError();
 }
 

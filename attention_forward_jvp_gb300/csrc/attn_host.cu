@@ -78,14 +78,22 @@ extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, false>(con
 extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<64, 64, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<128, 128, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, false, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, true, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, false, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, true, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, false, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, true, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, false, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, true, true>(const BwdParams&, int, cudaStream_t);
 }
 
 namespace {
@@ -487,38 +495,45 @@ attn_status run_f8(const attn_shape* s, const void* q, const void* k, const void
 // One block per sequence; rows are d 16-bit elements (d a multiple of 8).
 // A NULL output is left alone (each gradient pass zeroes its own).
 __global__ void attn_bwd_zero_tail_kernel(const int* offsets, int H, long long T, int max_seq_len,
-                                          uint16_t* dq, uint16_t* dk, uint16_t* dv, int d) {
+                                          uint16_t* dq, uint16_t* dk, uint16_t* dv, int dqk, int dv_) {
   const int b = blockIdx.x;
   const int begin = offsets[b], end = offsets[b + 1];
   const int first = begin + max(0, min(end - begin, max_seq_len));
-  const int chunks = d / 8;  // 16-byte chunks per row
-  const long long per_head = static_cast<long long>(end - first) * chunks;
-  for (long long i = threadIdx.x; i < per_head * H; i += blockDim.x) {
-    const long long h = i / per_head, rem = i % per_head;
-    const long long row = h * T + first + rem / chunks;
-    const long long off = row * d + (rem % chunks) * 8;
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    if (dq != nullptr) *reinterpret_cast<uint4*>(dq + off) = z;
-    if (dk != nullptr) *reinterpret_cast<uint4*>(dk + off) = z;
-    if (dv != nullptr) *reinterpret_cast<uint4*>(dv + off) = z;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  // one pass per row width: dq / dk rows are dqk wide, dv rows dv_ wide
+  for (int pass = 0; pass < 2; ++pass) {
+    const int d = pass == 0 ? dqk : dv_;
+    uint16_t* a = pass == 0 ? dq : dv;
+    uint16_t* c = pass == 0 ? dk : nullptr;
+    if (a == nullptr && c == nullptr) continue;
+    const int chunks = d / 8;  // 16-byte chunks per row
+    const long long per_head = static_cast<long long>(end - first) * chunks;
+    for (long long i = threadIdx.x; i < per_head * H; i += blockDim.x) {
+      const long long h = i / per_head, rem = i % per_head;
+      const long long row = h * T + first + rem / chunks;
+      const long long off = row * d + (rem % chunks) * 8;
+      if (a != nullptr) *reinterpret_cast<uint4*>(a + off) = z;
+      if (c != nullptr) *reinterpret_cast<uint4*>(c + off) = z;
+    }
   }
 }
 
-// One pass of the dQ kernel (kv = false) or of the dK / dV kernel.
-cudaError_t dispatch_bwd(int d, bool kv, bool f16, const attn::BwdParams& bp, int grid, cudaStream_t cs) {
-  if (d == 64) {
-    if (f16) return kv ? attn::launch_attn_bwd<64, true, true>(bp, grid, cs)
-                       : attn::launch_attn_bwd<64, false, true>(bp, grid, cs);
-    return kv ? attn::launch_attn_bwd<64, true, false>(bp, grid, cs)
-              : attn::launch_attn_bwd<64, false, false>(bp, grid, cs);
-  }
-  if (d == 128) {
-    if (f16) return kv ? attn::launch_attn_bwd<128, true, true>(bp, grid, cs)
-                       : attn::launch_attn_bwd<128, false, true>(bp, grid, cs);
-    return kv ? attn::launch_attn_bwd<128, true, false>(bp, grid, cs)
-              : attn::launch_attn_bwd<128, false, false>(bp, grid, cs);
+// One pass of the dQ kernel (kv = false) or of the dK / dV kernel; key
+// bit 1 for Dqk = 128, bit 0 for Dv = 128 (else 64).
+template <bool KV, bool F16>
+cudaError_t dispatch_bwd_dims(int key, const attn::BwdParams& bp, int grid, cudaStream_t cs) {
+  switch (key) {
+    case 0: return attn::launch_attn_bwd<64, 64, KV, F16>(bp, grid, cs);
+    case 1: return attn::launch_attn_bwd<64, 128, KV, F16>(bp, grid, cs);
+    case 2: return attn::launch_attn_bwd<128, 64, KV, F16>(bp, grid, cs);
+    case 3: return attn::launch_attn_bwd<128, 128, KV, F16>(bp, grid, cs);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t dispatch_bwd(int key, bool kv, bool f16, const attn::BwdParams& bp, int grid, cudaStream_t cs) {
+  if (f16) return kv ? dispatch_bwd_dims<true, true>(key, bp, grid, cs) : dispatch_bwd_dims<false, true>(key, bp, grid, cs);
+  return kv ? dispatch_bwd_dims<true, false>(key, bp, grid, cs) : dispatch_bwd_dims<false, false>(key, bp, grid, cs);
 }
 
 attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const void* v, const void* o,
@@ -533,7 +548,7 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
   if (jagged && (s->T < 0 || s->T > 0x7fffffffLL || s->max_seq_len < 0)) return ATTN_ERR_INVALID_ARG;
   if (bias != nullptr && (bias->bias != nullptr || bias->mask != nullptr)) return ATTN_ERR_UNSUPPORTED;
   auto dim_ok = [](int d) { return d == 16 || d == 32 || d == 64 || d == 128; };
-  if (!dim_ok(s->Dqk) || s->Dv != s->Dqk) return ATTN_ERR_UNSUPPORTED;
+  if (!dim_ok(s->Dqk) || !dim_ok(s->Dv)) return ATTN_ERR_UNSUPPORTED;
   if (!std::isnan(sm_scale) && !(sm_scale > 0.f && std::isfinite(sm_scale)))
     return ATTN_ERR_INVALID_ARG;
   if (!jagged && causal && s->M != s->N) return ATTN_ERR_INVALID_ARG;
@@ -559,9 +574,10 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
   if (st != ATTN_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const float scale = std::isnan(sm_scale) ? 1.0f / std::sqrt(static_cast<float>(s->Dqk)) : sm_scale;
-  const int D = s->Dqk <= 64 ? 64 : 128;  // 16 and 32 run zero-padded in the 64-wide kernels
-  const uint64_t d = static_cast<uint64_t>(s->Dqk), M = static_cast<uint64_t>(n_q),
-                 N = static_cast<uint64_t>(n_k);
+  // 16 and 32 run zero-padded in the 64-wide kernels
+  const int key = (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
+  const uint64_t dqk = static_cast<uint64_t>(s->Dqk), dv_ = static_cast<uint64_t>(s->Dv),
+                 M = static_cast<uint64_t>(n_q), N = static_cast<uint64_t>(n_k);
   // tensor-map z: b * H + h dense, h jagged (rows are the packed tokens)
   const uint64_t Z = jagged ? static_cast<uint64_t>(s->H) : static_cast<uint64_t>(BH);
 
@@ -584,7 +600,8 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     const bool zq = (stages & ATTN_BWD_DQ) != 0, zkv = (stages & ATTN_BWD_DKDV) != 0;
     attn_bwd_zero_tail_kernel<<<s->B, 256, 0, cs>>>(
         offsets, s->H, s->T, s->max_seq_len, zq ? static_cast<uint16_t*>(dq) : nullptr,
-        zkv ? static_cast<uint16_t*>(dk) : nullptr, zkv ? static_cast<uint16_t*>(dv) : nullptr, s->Dqk);
+        zkv ? static_cast<uint16_t*>(dk) : nullptr, zkv ? static_cast<uint16_t*>(dv) : nullptr, s->Dqk,
+        s->Dv);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1);
   }
@@ -610,7 +627,8 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     bp.delta = delta;
     bp.out1 = static_cast<uint16_t*>(kv ? dk : dq);
     bp.out2 = static_cast<uint16_t*>(kv ? dv : nullptr);
-    bp.d_out = s->Dqk;
+    bp.d_qk = s->Dqk;
+    bp.d_v = s->Dv;
     bp.err = ds->scratch;
     bp.timeout_ns = g_timeout_ns.load();
     // the streamed side has no rows: its maps are never used, only valid
@@ -621,16 +639,17 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     const void* r2 = kv ? v : dout;
     const void* t1 = other ? (kv ? q : k) : r1;
     const void* t2 = other ? (kv ? dout : v) : r2;
-    bool ok = encode_map(&bp.tm_r1, r1, d, rows, Z, attn::kBM, f16);
-    ok = ok && encode_map(&bp.tm_r2, r2, d, rows, Z, attn::kBM, f16);
-    ok = ok && encode_map(&bp.tm_t1, t1, d, Ro, Z, 64, f16);
-    ok = ok && encode_map(&bp.tm_t2, t2, d, Ro, Z, 64, f16);
+    // R1 / T1 (q or k) are Dqk wide, R2 / T2 (do or v) Dv wide
+    bool ok = encode_map(&bp.tm_r1, r1, dqk, rows, Z, attn::kBM, f16);
+    ok = ok && encode_map(&bp.tm_r2, r2, dv_, rows, Z, attn::kBM, f16);
+    ok = ok && encode_map(&bp.tm_t1, t1, other ? dqk : dqk, Ro, Z, 64, f16);
+    ok = ok && encode_map(&bp.tm_t2, t2, other ? dv_ : dv_, Ro, Z, 64, f16);
     if (!ok) return ATTN_ERR_CUDA;
     const int64_t units = BH * bp.n_rt;
     if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     bp.num_units = static_cast<int>(units);
     const int grid = static_cast<int>(units < ds->num_sms ? units : ds->num_sms);
-    if (dispatch_bwd(D, kv, f16, bp, grid, cs) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dispatch_bwd(key, kv, f16, bp, grid, cs) != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1);
   }
   return ATTN_OK;

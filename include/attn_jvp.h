@@ -195,10 +195,10 @@ attn_status attn_fwd_jvp_noalloc(const attn_shape* shape,
  * dout = dL/dO of a loss L, writes
  *
  *   Delta = rowsum(dout o O)             delta [B, H, M] fp32
- *   dV    = P^T dout                     dv    [B, H, N, D]
+ *   dV    = P^T dout                     dv    [B, H, N, Dv]
  *   dS    = P o (dout V^T - Delta)
- *   dQ    = sm_scale dS K                dq    [B, H, M, D]
- *   dK    = sm_scale dS^T Q              dk    [B, H, N, D]
+ *   dQ    = sm_scale dS K                dq    [B, H, M, Dqk]
+ *   dK    = sm_scale dS^T Q              dk    [B, H, N, Dqk]
  *
  * with P = exp(sm_scale Q K^T - LSE) over the valid set (0 elsewhere and
  * on rows with LSE = -inf).  Sources: the Triton fused-attention tutorial's
@@ -207,7 +207,8 @@ attn_status attn_fwd_jvp_noalloc(const attn_shape* shape,
  * (triton_flashattn) _attn_bwd_dkdv_inner / _attn_bwd_dq_inner.
  *
  * This version: no bias or mask (bias must be NULL or hold two NULL
- * pointers) and Dqk == Dv = D in {16, 32, 64, 128}; otherwise
+ * pointers) and Dqk, Dv in {16, 32, 64, 128} (16 and 32 zero-padded to 64
+ * inside; unequal dims as in "flash_attention.py"); otherwise
  * ATTN_ERR_UNSUPPORTED.  Dense (offsets NULL; causal requires M == N) or
  * jagged (offsets != NULL, the FBGEMM jagged backward's layout:
  * q, k, v, o, dout, dq, dk, dv [H, T, D], lse and delta [H, T]); a jagged

@@ -133,13 +133,13 @@ def _bwd(L, shape, q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, offsets=No
 
 def test_bwd_validation(L):
     assert _bwd(L, None) == 1
-    assert _bwd(L, _shape(Dqk=64, Dv=128)) == 2          # Dqk != Dv
+    assert _bwd(L, _shape(Dqk=64, Dv=256)) == 2          # Dv outside {16, 32, 64, 128}
     assert _bwd(L, _shape(Dqk=256, Dv=256)) == 2
     assert _bwd(L, _shape(Dqk=8, Dv=8), f16=True) == 2
     off = ctypes.c_void_p(0x20000)
     assert _bwd(L, _shape(T=-1, msl=64), offsets=off) == 1          # jagged, bad T
     assert _bwd(L, _shape(T=100, msl=-2), offsets=off) == 1         # jagged, bad cap
-    assert _bwd(L, _shape(T=100, msl=64, Dqk=64, Dv=128), offsets=off) == 2
+    assert _bwd(L, _shape(T=100, msl=64, Dqk=96, Dv=64), offsets=off) == 2
     assert _bwd(L, _shape(T=0, msl=64), offsets=off) == 0           # no tokens: no-op
     b = binding.AttnBias()
     b.mask = 0x10000
@@ -166,4 +166,4 @@ def test_bwd_stages_validation(L):
     assert st(0) == 1            # no stage selected
     assert st(8) == 1            # unknown stage bit
     assert st(7, _shape(B=0)) == 0
-    assert st(2, _shape(Dqk=64, Dv=128)) == 2
+    assert st(2, _shape(Dqk=256, Dv=128)) == 2

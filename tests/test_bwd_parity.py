@@ -85,6 +85,11 @@ CASES = [
     ("d16", _w(M=200, N=260, Dqk=16, Dv=16)),
     ("d32_causal", _w(M=257, N=257, Dqk=32, Dv=32, causal=True)),
     ("scale_std2", _w(M=256, N=384, input_std=2.0, sm_scale=0.2)),
+    # unequal head dims (the flash_attention.py backward's Dqk != Dv)
+    ("dqk128_dv64_causal", _w(M=320, N=320, Dqk=128, Dv=64, causal=True)),
+    ("dqk64_dv128", _w(M=200, N=333, Dqk=64, Dv=128)),
+    ("dqk32_dv128_causal", _w(M=257, N=257, Dqk=32, Dv=128, causal=True)),
+    ("dqk128_dv16", _w(M=130, N=260, Dqk=128, Dv=16)),
 ]
 
 
@@ -94,7 +99,7 @@ def test_bwd_parity(name, w):
     assert_grads_close(run_gpu_bwd(inp), oracle_bwd(inp), what=name)
 
 
-@pytest.mark.parametrize("name,w", [CASES[1], CASES[2]], ids=["causal_d64", "nc_d128"])
+@pytest.mark.parametrize("name,w", [CASES[1], CASES[2], CASES[11]], ids=["causal_d64", "nc_d128", "dqk128_dv64"])
 def test_bwd_parity_f16(name, w):
     inp = make_bwd_inputs(w, seed=8)
     assert_grads_close(run_gpu_bwd(inp, f16=True), oracle_bwd(inp, f16=True), what=name + "_f16")
@@ -116,12 +121,12 @@ def test_bwd_empty_sides():
 
 
 def test_bwd_unsupported_configs():
-    inp = make_bwd_inputs(_w(M=128, N=128, Dqk=64, Dv=128), seed=1)
+    inp = make_bwd_inputs(_w(M=128, N=128, Dqk=64, Dv=256), seed=1)
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
     lse = torch.zeros(1, 2, 128, device="cuda")
     with pytest.raises(binding.AttnError) as e:
         binding.attn_bwd(q, k, v, do, lse, do)
-    assert e.value.status == 2  # Dqk != Dv
+    assert e.value.status == 2  # Dv = 256
 
 
 def test_bwd_full_size_sampled_heads():
@@ -162,11 +167,12 @@ JAGGED_LENS = [3, 64, 130, 257, 1, 0, 300, 128]
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128, 32])
+@pytest.mark.parametrize("D", [64, 128, 32, (128, 64)])
 def test_bwd_jagged(causal, D):
     # lengths around the tile sizes, an empty sequence and two sequences
     # past max_seq_len = 256 (their capped tokens get zero gradients)
-    w = Workload("jb", B=len(JAGGED_LENS), H=2, Dqk=D, Dv=D, jagged=True, max_seq_len=256,
+    dqk, dv = D if isinstance(D, tuple) else (D, D)
+    w = Workload("jb", B=len(JAGGED_LENS), H=2, Dqk=dqk, Dv=dv, jagged=True, max_seq_len=256,
                  max_len_draw=1, causal=causal)
     inp = make_bwd_inputs(w, seed=21, lengths=JAGGED_LENS)
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
