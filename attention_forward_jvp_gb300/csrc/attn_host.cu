@@ -642,8 +642,8 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     // R1 / T1 (q or k) are Dqk wide, R2 / T2 (do or v) Dv wide
     bool ok = encode_map(&bp.tm_r1, r1, dqk, rows, Z, attn::kBM, f16);
     ok = ok && encode_map(&bp.tm_r2, r2, dv_, rows, Z, attn::kBM, f16);
-    ok = ok && encode_map(&bp.tm_t1, t1, other ? dqk : dqk, Ro, Z, 64, f16);
-    ok = ok && encode_map(&bp.tm_t2, t2, other ? dv_ : dv_, Ro, Z, 64, f16);
+    ok = ok && encode_map(&bp.tm_t1, t1, dqk, Ro, Z, 64, f16);
+    ok = ok && encode_map(&bp.tm_t2, t2, dv_, Ro, Z, 64, f16);
     if (!ok) return ATTN_ERR_CUDA;
     const int64_t units = BH * bp.n_rt;
     if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
