@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // With a bias that has a tensor map it also loads each key tile's bias
     // (two 128 x 32 fp32 boxes) into the bias ring.
     if (lane == 0) {
-      uint32_t vfill = 0;
+      uint32_t vfill = 0, bfill = 0;
       const bool bias_ring = P::NB > 0 && p.bias_tma != 0;
       bool ok = true;
       for (int rnd = 0; ok; ++rnd) {
@@ -616,6 +616,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const Unit w = decode_unit(p, u, list);
         for (int j = 0; j < w.nt; ++j) {
           const int r = w.row0 + j * kBN;
+          if constexpr (P::NB > 0) {
+            // The bias goes first: its stage frees as soon as the softmax
+            // warps have read tile j - NB's bias, well before the output
+            // MMAs of that tile release its V stage, so its copy is not
+            // held back behind the V wait.
+            if (bias_ring) {
+              // the bias streams from HBM once: its boxes are pulled into L2
+              // kBiasLead tiles ahead of their copy into the ring
+              const int hb = p.bias_bcast_h ? 0 : w.h, bb = p.bias_bcast_b ? 0 : w.b;
+              for (int jj = (j == 0 ? 0 : j + kBiasLead); jj <= j + kBiasLead && jj < w.nt; ++jj) {
+                tma_prefetch_l2_4d(&p.tm_bias, jj * kBN, w.mt * kBM, hb, bb);
+                tma_prefetch_l2_4d(&p.tm_bias, jj * kBN + 32, w.mt * kBM, hb, bb);
+              }
+              const uint32_t bs = bfill % P::NB;
+              ok = wait_bar(bar(P::B_BE + bs), ((bfill / P::NB) & 1u) ^ 1u, W);
+              if (!ok) break;
+              mbar_arrive_expect_tx(bar(P::B_BF + bs), P::BIAS_STAGE);
+              const uint32_t bdst = sbase + P::OFF_BIAS + bs * P::BIAS_STAGE;
+              tma_load_4d(bdst, &p.tm_bias, bar(P::B_BF + bs), j * kBN, w.mt * kBM, hb, bb);
+              tma_load_4d(bdst + P::BIAS_BOX, &p.tm_bias, bar(P::B_BF + bs), j * kBN + 32,
+                          w.mt * kBM, hb, bb);
+              ++bfill;
+            }
+          }
           const uint32_t vs = vfill % P::NV;
           ok = wait_bar(bar(P::B_VE + vs), ((vfill / P::NV) & 1u) ^ 1u, W);
           if (!ok) break;
@@ -633,25 +657,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                           w.z);
           }
           }
-          if constexpr (P::NB > 0) {
-            if (bias_ring) {
-              // the bias streams from HBM once: its boxes are pulled into L2
-              // kBiasLead tiles ahead of their copy into the ring
-              const int hb = p.bias_bcast_h ? 0 : w.h, bb = p.bias_bcast_b ? 0 : w.b;
-              for (int jj = (j == 0 ? 0 : j + kBiasLead); jj <= j + kBiasLead && jj < w.nt; ++jj) {
-                tma_prefetch_l2_4d(&p.tm_bias, jj * kBN, w.mt * kBM, hb, bb);
-                tma_prefetch_l2_4d(&p.tm_bias, jj * kBN + 32, w.mt * kBM, hb, bb);
-              }
-              const uint32_t bs = vfill % P::NB;
-              ok = wait_bar(bar(P::B_BE + bs), ((vfill / P::NB) & 1u) ^ 1u, W);
-              if (!ok) break;
-              mbar_arrive_expect_tx(bar(P::B_BF + bs), P::BIAS_STAGE);
-              const uint32_t bdst = sbase + P::OFF_BIAS + bs * P::BIAS_STAGE;
-              tma_load_4d(bdst, &p.tm_bias, bar(P::B_BF + bs), j * kBN, w.mt * kBM, hb, bb);
-              tma_load_4d(bdst + P::BIAS_BOX, &p.tm_bias, bar(P::B_BF + bs), j * kBN + 32,
-                          w.mt * kBM, hb, bb);
-            }
-          }
           ++vfill;
         }
       }
@@ -661,8 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       if constexpr (P::NB > 0) {
         if (bias_ring) {
-          for (uint32_t s = 0; s < static_cast<uint32_t>(P::NB) && s < vfill; ++s) {
-            const uint32_t nf = (vfill - s + P::NB - 1) / P::NB;
+          for (uint32_t s = 0; s < static_cast<uint32_t>(P::NB) && s < bfill; ++s) {
+            const uint32_t nf = (bfill - s + P::NB - 1) / P::NB;
             drain_bar(bar(P::B_BF + s), (nf - 1) & 1u, p.timeout_ns);
           }
         }
@@ -1173,6 +1178,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
         float sc;  // factor taking x to log2 units inside the exponent
         float mx;
+        bool dead = false;  // no key of the tile kept for any row of this warp
         if (fast) {
           sc = p.scale_log2;
           float xo[kHalf];
@@ -1189,41 +1195,86 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
           uint32_t kmo = keep_bits(keyo, w.kv_len, qi, p.causal);
           if (has_mask) {
-            km &= mask_bits32(mv);
-            kmo &= mask_bits32(mvo);
+            // Most tiles of a key-padding or block mask are wholly kept or
+            // wholly masked: only mixed mask bytes need the bit gather.
+            uint32_t any_set = 0u, any_zero = 0u;
+#pragma unroll
+            for (int wd = 0; wd < kHalf / 4; ++wd) {
+              any_set |= mv[wd] | mvo[wd];
+              any_zero |= __vcmpeq4(mv[wd], 0u) | __vcmpeq4(mvo[wd], 0u);
+            }
+            if (any_set == 0u) {
+              km = 0u;
+              kmo = 0u;
+            } else if (any_zero != 0u) {
+              km &= mask_bits32(mv);
+              kmo &= mask_bits32(mvo);
+            }
           }
+          // warp-uniform tile classes: every key kept (no per-element
+          // selects) or none kept (no arithmetic; P = H = 0)
+          const bool all_keep = __all_sync(0xffffffffu, (km & kmo) == 0xffffffffu);
+          dead = __all_sync(0xffffffffu, (km | kmo) == 0u);
           if (has_bias) {
+            // the stage is waited on even when unused, so that its next
+            // fill cannot start before this one has landed
             ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_BF + g % NBR), (g / NBR) & 1u, W));
             if (!ok) break;
           }
           const uint8_t* bbase = smem + P::OFF_BIAS + (g % NBR) * P::BIAS_STAGE + row * 128;
           float xo[kHalf];
+          if (dead) {
+            mx = -INFINITY;
+          } else if (all_keep) {
+            const uint64_t sl2 = f2_make(p.scale_log2, p.scale_log2), e2 = f2_make(kLog2e, kLog2e);
 #pragma unroll
-          for (int k4 = 0; k4 < kHalf / 4; ++k4) {
-            float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), bo4 = b4;
-            if (has_bias) {
-              const int phys = (k4 ^ (row & 7)) * 16;
-              b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
-              bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
+            for (int k4 = 0; k4 < kHalf / 4; ++k4) {
+              float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), bo4 = b4;
+              if (has_bias) {
+                const int phys = (k4 ^ (row & 7)) * 16;
+                b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
+                bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
+              }
+              const int c = 4 * k4;
+              f2_split(f2_fma(f2_make(b4.x, b4.y), e2, f2_mul(f2_make(x[c], x[c + 1]), sl2)), x[c], x[c + 1]);
+              f2_split(f2_fma(f2_make(b4.z, b4.w), e2, f2_mul(f2_make(x[c + 2], x[c + 3]), sl2)), x[c + 2],
+                       x[c + 3]);
+              f2_split(f2_fma(f2_make(bo4.x, bo4.y), e2,
+                              f2_mul(f2_make(__uint_as_float(so[c]), __uint_as_float(so[c + 1])), sl2)),
+                       xo[c], xo[c + 1]);
+              f2_split(f2_fma(f2_make(bo4.z, bo4.w), e2,
+                              f2_mul(f2_make(__uint_as_float(so[c + 2]), __uint_as_float(so[c + 3])), sl2)),
+                       xo[c + 2], xo[c + 3]);
             }
-            const float bo[4] = {bo4.x, bo4.y, bo4.z, bo4.w};
-            const float bw[4] = {b4.x, b4.y, b4.z, b4.w};
+            mx = fmaxf(rowmax32(x), rowmax32(xo));
+          } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 4 * k4 + e;
-              const float v = fmaf(bw[e], kLog2e, x[c] * p.scale_log2);
-              const float vo = fmaf(bo[e], kLog2e, __uint_as_float(so[c]) * p.scale_log2);
-              x[c] = ((km >> c) & 1u) ? v : -INFINITY;
-              xo[c] = ((kmo >> c) & 1u) ? vo : -INFINITY;
-              if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
+            for (int k4 = 0; k4 < kHalf / 4; ++k4) {
+              float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), bo4 = b4;
+              if (has_bias) {
+                const int phys = (k4 ^ (row & 7)) * 16;
+                b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
+                bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
+              }
+              const float bo[4] = {bo4.x, bo4.y, bo4.z, bo4.w};
+              const float bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = 4 * k4 + e;
+                const float v = fmaf(bw[e], kLog2e, x[c] * p.scale_log2);
+                const float vo = fmaf(bo[e], kLog2e, __uint_as_float(so[c]) * p.scale_log2);
+                x[c] = ((km >> c) & 1u) ? v : -INFINITY;
+                xo[c] = ((kmo >> c) & 1u) ? vo : -INFINITY;
+                if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
+              }
             }
+            mx = fmaxf(rowmax32(x), rowmax32(xo));
           }
           if (has_bias) {
             // this warp is done with the tile's bias
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(P::B_BE + g % NBR));
           }
-          mx = fmaxf(rowmax32(x), rowmax32(xo));
         } else {
           sc = 1.f;
           if constexpr (!BM) {
@@ -1279,7 +1330,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         uint64_t ls = 0;
         float lt0 = 0.f, lt1 = 0.f, rt0 = 0.f, rt1 = 0.f;
         uint64_t pv[kHalf / 2];
-        if constexpr (F8) {
+        if (!F8 && dead) {
+          // P = H = 0 for the output MMAs; m, l and r stay as they are
+          uint32_t zk[kHalf / 2];
+#pragma unroll
+          for (int c = 0; c < kHalf / 2; ++c) zk[c] = 0u;
+          tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, zk);
+          if constexpr (JVP) tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf + kHalf / 2, zk);
+        } else if constexpr (F8) {
           // four e5m2 weights per column, half h in the 8 columns at 8 h
           uint32_t pk8[kHalf / 4];
 #pragma unroll
@@ -1310,7 +1368,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, pk);
         }
-        if constexpr (JVP) {
+        if (JVP && !dead) {
           uint32_t hk[kHalf / 2];
           tmem_wait_ld_regs(tr);
 #pragma unroll

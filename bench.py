@@ -56,9 +56,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 10**6  # GB300 L2
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(backward: bool = False) -> str:
+    """Hash of the sources a line's kernels are built from (the forward
+    kernels do not include the backward's files)."""
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(ROOT, "attention_forward_jvp_gb300", "csrc", "*")))
+    if not backward:
+        files = [f for f in files if not os.path.basename(f).startswith("attn_bwd")]
     files += sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
     for f in files:
         with open(f, "rb") as fh:
@@ -586,7 +590,7 @@ def run_ours_bwd(args, w, world, rank, local):
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk.summary(),
-        "kernel_hash": kernel_source_hash(),
+        "kernel_hash": kernel_source_hash(backward=True),
     }
     print(json.dumps(line), flush=True)
     return 0
