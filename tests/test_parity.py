@@ -224,6 +224,29 @@ def test_bias_ring_shared_by_batch_with_full_mask():
     assert_close(*run_gpu(inp), *oracle_dense(inp), what="bias shared by batch + mask")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_mask_with_dead_key_tiles(causal):
+    # A mask that does not depend on the query row, [B, H, 1, N]: key tiles
+    # with no kept key (one alone, runs of them, the ragged last tile) are
+    # skipped by the softmax warps (P = H = 0, no exponentials).  Tiles with
+    # a single kept key, nonzero mask values other than 1, and a different
+    # pattern per (batch, head) around them.
+    N = 64 * 40 + 17
+    w = Workload("dk", B=2, H=2, M=N if causal else 130, N=N, Dqk=64, Dv=64, bias=True, causal=causal)
+    inp = make_inputs(w, seed=41)
+    g = torch.Generator().manual_seed(42)
+    mask = (torch.rand((2, 2, 1, N), generator=g) < 0.8).to(torch.uint8) * 5
+    for b in range(2):
+        for h in range(2):
+            dead = [3, 39, 40] + list(range(30 + b, 36 + h))
+            for t in dead:
+                mask[b, h, 0, 64 * t: 64 * t + 64] = 0
+            mask[b, h, 0, 64 * 10: 64 * 11] = 0
+            mask[b, h, 0, 64 * 10 + 17 * (b + 2 * h)] = 1   # a single kept key
+    inp["mask"] = mask
+    assert_close(*run_gpu(inp), *oracle_dense(inp), what=f"dead key tiles (causal={causal})")
+
+
 def test_mask_without_bias():
     w = Workload("mo", B=2, H=2, M=190, N=300, Dqk=128, Dv=64)
     inp = make_inputs(w, seed=15)
