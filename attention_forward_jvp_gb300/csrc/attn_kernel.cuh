@@ -1225,28 +1225,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           float xo[kHalf];
           if (dead) {
             mx = -INFINITY;
+          } else if (all_keep && !has_bias) {
+            // as without a mask: the row maximum of the raw scores, scaled once
+            sc = p.scale_log2;
+#pragma unroll
+            for (int c = 0; c < kHalf; ++c) xo[c] = __uint_as_float(so[c]);
+            mx = fmaxf(rowmax32(x), rowmax32(xo)) * p.scale_log2;
           } else if (all_keep) {
-            const uint64_t sl2 = f2_make(p.scale_log2, p.scale_log2), e2 = f2_make(kLog2e, kLog2e);
+            // x = s S + bias in natural units (one packed FMA per pair); the
+            // exponent's factor becomes log2 e
+            sc = kLog2e;
+            const uint64_t s2 = f2_make(p.sm_scale, p.sm_scale);
 #pragma unroll
             for (int k4 = 0; k4 < kHalf / 4; ++k4) {
-              float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), bo4 = b4;
-              if (has_bias) {
-                const int phys = (k4 ^ (row & 7)) * 16;
-                b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
-                bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
-              }
+              const int phys = (k4 ^ (row & 7)) * 16;
+              const float4 b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
+              const float4 bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
               const int c = 4 * k4;
-              f2_split(f2_fma(f2_make(b4.x, b4.y), e2, f2_mul(f2_make(x[c], x[c + 1]), sl2)), x[c], x[c + 1]);
-              f2_split(f2_fma(f2_make(b4.z, b4.w), e2, f2_mul(f2_make(x[c + 2], x[c + 3]), sl2)), x[c + 2],
-                       x[c + 3]);
-              f2_split(f2_fma(f2_make(bo4.x, bo4.y), e2,
-                              f2_mul(f2_make(__uint_as_float(so[c]), __uint_as_float(so[c + 1])), sl2)),
+              f2_split(f2_fma(f2_make(x[c], x[c + 1]), s2, f2_make(b4.x, b4.y)), x[c], x[c + 1]);
+              f2_split(f2_fma(f2_make(x[c + 2], x[c + 3]), s2, f2_make(b4.z, b4.w)), x[c + 2], x[c + 3]);
+              f2_split(f2_fma(f2_make(__uint_as_float(so[c]), __uint_as_float(so[c + 1])), s2,
+                              f2_make(bo4.x, bo4.y)),
                        xo[c], xo[c + 1]);
-              f2_split(f2_fma(f2_make(bo4.z, bo4.w), e2,
-                              f2_mul(f2_make(__uint_as_float(so[c + 2]), __uint_as_float(so[c + 3])), sl2)),
+              f2_split(f2_fma(f2_make(__uint_as_float(so[c + 2]), __uint_as_float(so[c + 3])), s2,
+                              f2_make(bo4.z, bo4.w)),
                        xo[c + 2], xo[c + 3]);
             }
-            mx = fmaxf(rowmax32(x), rowmax32(xo));
+            mx = fmaxf(rowmax32(x), rowmax32(xo)) * kLog2e;
           } else {
 #pragma unroll
             for (int k4 = 0; k4 < kHalf / 4; ++k4) {
