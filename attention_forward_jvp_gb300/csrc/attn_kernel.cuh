@@ -142,9 +142,17 @@ struct Plan {
   // [V | tV] is one N = 2 Dv operand.
   static constexpr int V_STAGE = NQ * V_TILE;
   static constexpr int QSET = NQ * Q_TILE;  // one Q (+ tQ) buffer
+  // Ping-pong softmax (head dims 64, no bias / mask, 16-bit operands): the
+  // two softmax warps of a TMEM lane quadrant take alternate key tiles of a
+  // unit (all 64 columns each) instead of the two column halves of every
+  // tile, each with its own running max, sums and O / tO accumulator (the
+  // two O buffers); the epilogue merges the two.  The two warps of a
+  // sub-partition then work on different tiles, so their latencies overlap.
+  static constexpr bool PP = !F8 && BMODE == kNoBias && DQK == 64 && DV == 64;
   // exchange slots between the two softmax warps of a row:
-  // [parity][half][row] plus one [row] array (the epilogue's third value)
-  static constexpr int XCHG_FLOATS = 2 * 2 * kBM + kBM;
+  // [parity][half][row] plus one [row] array (the epilogue's third value);
+  // ping-pong: [unit parity][value][tile parity][row], four values
+  static constexpr int XCHG_FLOATS = PP ? 2 * 4 * 2 * kBM : 2 * 2 * kBM + kBM;
   static constexpr int BUDGET = 227 * 1024 - 512 - XCHG_FLOATS * 4;
   // Q buffers: two (the next unit's Q loads while the current unit runs and
   // score MMAs flow across unit boundaries) when they fit beside three K and
@@ -185,6 +193,7 @@ struct Plan {
   // whose output MMAs write the other buffer) with two Q buffers, when the
   // tensor memory holds them.
   static constexpr int NOB = (NQB == 2 && COL_O + 2 * OBUF <= 512) ? 2 : 1;
+  static_assert(!PP || (NQB == 2 && NOB == 2), "ping-pong softmax: two Q and two O buffers");
   static constexpr int B_QF = 0, B_QE = B_QF + NQB, B_KF = B_QE + NQB, B_KE = B_KF + NK,
                        B_VF = B_KE + NK, B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2,
                        B_DRAIN = B_PF + 2, B_PAIR = B_DRAIN + 1, B_BF = B_PAIR + 4,
@@ -498,7 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(P::B_SF + i), 1);
-      mbar_init(bar(P::B_PF + i), 9);  // one arrival per softmax warp + the release warp
+      // one arrival per softmax warp of the tile (all eight, or the four of
+      // its parity in the ping-pong softmax) + the release warp
+      mbar_init(bar(P::B_PF + i), P::PP ? 5 : 9);
     }
     mbar_init(bar(P::B_DRAIN), 1);
     for (int i = 0; i < 4; ++i) mbar_init(bar(P::B_PAIR + i), 64);
@@ -794,13 +805,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // half of the first chain.  The first output MMAs of a unit overwrite
     // the O buffer: with two buffers they wait until the epilogue of unit
     // un - 2 has read it.
-    auto issue_pv = [&](uint32_t t, bool first, uint32_t un, auto&& mid) -> bool {
+    // jt: the tile's index within its unit.  Ping-pong softmax: tile jt
+    // accumulates into O buffer jt % 2, whose first write in a unit waits
+    // until the previous unit's epilogue has read both buffers.
+    auto issue_pv = [&](uint32_t t, int jt, uint32_t un, auto&& mid) -> bool {
       const uint32_t sb = t & 1u;
+      const bool first = P::PP ? jt < 2 : jt == 0;
       if (!wait_v(t) || !wait_all(bar(P::B_PF + sb), (t >> 1) & 1u)) return false;
-      if (P::NOB == 2 && first && !wait_all(bar(P::B_OE + un % P::NOB), ((un / P::NOB) & 1u) ^ 1u))
-        return false;
+      if constexpr (P::PP) {
+        if (first && !wait_all(bar(P::B_OE + jt), (un & 1u) ^ 1u)) return false;
+      } else {
+        if (P::NOB == 2 && first && !wait_all(bar(P::B_OE + un % P::NOB), ((un / P::NOB) & 1u) ^ 1u))
+          return false;
+      }
       tc_fence_after();
-      const uint32_t colo = P::COL_O + (un % P::NOB) * P::OBUF;
+      const uint32_t colo = P::COL_O + (P::PP ? static_cast<uint32_t>(jt & 1) : un % P::NOB) * P::OBUF;
       const uint32_t lv = lo_v + (t % P::NV) * (P::V_STAGE >> 4);
       // keys [16 kk, 16 kk + 16): P at column base + 32 (kk / 2) + 8 (kk % 2),
       // H 16 columns further (the layout the softmax halves write)
@@ -861,22 +880,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           });
           if (!ok) break;
           if (j > 0) {
-            ok = issue_pv(g - 1, j == 1, quse, [&]() {
+            ok = issue_pv(g - 1, j - 1, quse, [&]() {
               if (j + 1 < w.nt) poll_k(g + 1);
             });
             if (!ok) break;
           }
         }
         if (!ok) break;
-        ok = issue_pv(g - 1, w.nt == 1, quse, []() {});
+        ok = issue_pv(g - 1, w.nt - 1, quse, []() {});
         ++quse;
       }
     } else {
       // Two Q buffers: the tiles of consecutive units form one stream,
       // S(t+1) issued before PV(t) also when t ends a unit.  The pending
-      // output batch (tile pt of unit pu, first tile of its unit: pfirst)
+      // output batch (tile pt of unit pu, its index in the unit: pj)
       // is issued after the next score batch; polls as above.
-      bool pend = false, pfirst = false;
+      bool pend = false;
+      int pj = 0;
       uint32_t pt = 0, pu = 0;
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
@@ -892,18 +912,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           });
           if (!ok) break;
           if (pend) {
-            ok = issue_pv(pt, pfirst, pu, [&]() { poll_k(g + 1); });
+            ok = issue_pv(pt, pj, pu, [&]() { poll_k(g + 1); });
             if (!ok) break;
           }
           pend = true;
           pt = g;
-          pfirst = j == 0;
+          pj = j;
           pu = quse;
         }
         if (!ok) break;
         ++quse;
       }
-      if (ok && pend) ok = issue_pv(pt, pfirst, pu, []() {});
+      if (ok && pend) ok = issue_pv(pt, pj, pu, []() {});
     }
     // Teardown: all MMAs issued by the leader complete before TMEM is freed.
     if (leader) {
@@ -1048,409 +1068,660 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       return true;
     };
-    uint32_t un = 0;         // units with keys seen so far
-    Epi pend{};              // with two O buffers: the unit whose epilogue is due
-    bool has_pend = false;
-    uint32_t g = 0;           // global key-tile counter (same in every role)
-    uint32_t gen = 0;         // masked tiles seen (slot parity of the max exchange)
     bool ok = true;
-    for (int rnd = 0; ok; ++rnd) {
-      const int u = unit_of_round(rnd);
-      if (u >= num_units) break;
-      const Unit w = decode_unit(p, u, list);
-      if (!w.active) continue;
-      const int qi = w.mt * kBM + row;
-      const bool row_ok = qi < w.q_len;
-      if (w.nt == 0) {  // no keys at all: empty rows
-        // this half's output columns: [half * DVH, min((half + 1) * DVH, dv_out))
-        const int ncol = min(DVH, p.dv_out - half * DVH);
-        if (row_ok && ncol > 0) {
-          uint32_t z[DVH / 2];
+    if constexpr (P::PP) {
+      // ------------------------------------------------ ping-pong softmax
+      // This warp takes the tiles j = par, par + 2, ... of every unit, all
+      // 64 key columns, accumulating through O buffer par; at the unit's
+      // end the two parities of a row merge their (m, l, lt, r) and O / tO.
+      const int par = half;
+      const uint32_t colo_par = P::COL_O + static_cast<uint32_t>(par) * P::OBUF;
+      const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
+      uint32_t un = 0;  // units with keys seen so far
+      uint32_t g = 0;   // global key-tile counter of the unit's first tile (same in every role)
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_of_round(rnd);
+        if (u >= num_units) break;
+        const Unit w = decode_unit(p, u, list);
+        if (!w.active) continue;
+        const int qi = w.mt * kBM + row;
+        const bool row_ok = qi < w.q_len;
+        if (w.nt == 0) {  // no keys at all: empty rows (this warp: columns [par DVH, ...))
+          const int ncol = min(DVH, p.dv_out - par * DVH);
+          if (row_ok && ncol > 0) {
+            uint32_t z[DVH / 2];
 #pragma unroll
-          for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
-          if constexpr (F8) {
-            // e5m2 output: one byte per element
-            uint8_t* orow8 = reinterpret_cast<uint8_t*>(p.o) + (w.out0 + qi) * p.dv_out + half * DVH;
-            store_row_bf16(reinterpret_cast<uint16_t*>(orow8), z, ncol / 4);
-          } else {
-            uint16_t* orow = p.o + (w.out0 + qi) * p.dv_out + half * DVH;
-            uint16_t* torow = JVP ? p.to + (w.out0 + qi) * p.dv_out + half * DVH : nullptr;
-            store_row_bf16(orow, z, ncol / 2);
-            if (JVP) store_row_bf16(torow, z, ncol / 2);
+            for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
+            store_row_bf16(p.o + (w.out0 + qi) * p.dv_out + par * DVH, z, ncol / 2);
+            if (JVP) store_row_bf16(p.to + (w.out0 + qi) * p.dv_out + par * DVH, z, ncol / 2);
           }
+          if (row_ok && par == 0) p.lse[w.out0 + qi] = -INFINITY;
+          continue;
         }
-        if (row_ok && half == 0) p.lse[w.out0 + qi] = -INFINITY;
-        continue;
-      }
-      const float* brow = nullptr;
-      const unsigned char* mrow = nullptr;
-      if (has_bias)
-        brow = p.bias + w.b * p.bias_stride[0] + w.h * p.bias_stride[1] +
-               static_cast<long long>(qi) * p.bias_stride[2];
-      if (has_mask)
-        mrow = p.mask + w.b * p.mask_stride[0] + w.h * p.mask_stride[1] +
-               static_cast<long long>(qi) * p.mask_stride[2];
-
-      // m_run: reference max (log2 units), shared by both halves of a row.
-      // l2: exact partial sum of p (for LSE); lt2 / r2: partial sums of the
-      // bf16 values of p and p*tS that the MMAs consume, so O and tO are
-      // normalised by the weights actually used.  Pairs of fp32 lanes.
-      float m_run = -INFINITY;
-      uint64_t l2 = 0, lt2 = 0, r2 = 0;
-      const uint32_t colo_cur = P::COL_O + (un % P::NOB) * P::OBUF;  // this unit's O buffer
-      for (int j = 0; j < w.nt; ++j, ++g) {
-        const uint32_t sb = g & 1u;
-        const int key0 = j * kBN + half * kHalf;  // first key of this thread's columns
-        // Bias rows stream from HBM once: pull this thread's segment of the
-        // tile two steps ahead into L2 (the first two tiles at unit start),
-        // then load this tile's entries before waiting on S.
-        if (GLOB && has_bias && row_ok && p.bias_stride[3] == 1) {
-          const float* bp = brow + half * kHalf;
-          if (j == 0) {
-            prefetch_l2(bp);
-            if (w.nt > 1) prefetch_l2(bp + kBN);
-          }
-          if (j + 2 < w.nt) prefetch_l2(bp + (j + 2) * kBN);
-        }
-        float bv[kHalf];
-        uint32_t mv[kHalf / 4];
-        uint32_t mvo[kHalf / 4];  // the partner's columns (local row maximum)
-        if (GLOB && has_bias) {
-#pragma unroll
-          for (int c = 0; c < kHalf; ++c) bv[c] = 0.f;
-          if (row_ok) {
-            const float* bp = brow + static_cast<long long>(key0) * p.bias_stride[3];
-            if (p.bias_stride[3] == 1 && (reinterpret_cast<uintptr_t>(bp) & 15u) == 0 &&
-                key0 + kHalf <= w.kv_len) {
-#pragma unroll
-              for (int c = 0; c < kHalf / 4; ++c) {
-                const float4 t4 = __ldg(reinterpret_cast<const float4*>(bp) + c);
-                bv[4 * c] = t4.x;
-                bv[4 * c + 1] = t4.y;
-                bv[4 * c + 2] = t4.z;
-                bv[4 * c + 3] = t4.w;
-              }
-            } else {
-              for (int c = 0; c < kHalf; ++c)
-                if (key0 + c < w.kv_len) bv[c] = __ldg(bp + c * p.bias_stride[3]);
-            }
-          }
-        }
-        if (has_mask) {
-          load_mask32(mrow, key0, w.kv_len, p.mask_stride[3], row_ok, mv);
-          if (RING) load_mask32(mrow, j * kBN + (half ^ 1) * kHalf, w.kv_len, p.mask_stride[3], row_ok, mvo);
-        }
-
-        ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
-        if (!ok) break;
-        tc_fence_after();
-        // Each warp also reads the partner half's 32 score columns and takes
-        // the row maximum over all 64 itself, so the two warps of a quadrant
-        // never wait for each other: unmasked tiles (`fast`) and masked tiles
-        // (`local`: causal diagonal, ragged tail, mask, and bias read from
-        // the shared-memory ring), the mask applied to both halves.  Only a
-        // bias read per thread from global memory makes the two warps
-        // exchange partial maxima through shared memory instead.
-        const bool diag = p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
-        const bool fast = !BM && !diag && (j * kBN + kBN <= w.kv_len);
-        const bool local = !GLOB && !fast;
-        uint32_t sr[kHalf];
-        uint32_t so[kHalf];
-        uint32_t tr[kHalf];
-        tmem_ld_32x32b_x32(tl + sb * P::SBUF + half * kHalf, sr);
-        if (fast) {
-          tmem_ld_32x32b_x32(tl + sb * P::SBUF + (half ^ 1) * kHalf, so);
-          tmem_wait_ld_regs(sr);
-          tmem_regs_ready(so);
-          // the tangent scores are needed only after the exponentials, so
-          // their load overlaps the row maximum and exp2 below
-          if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
-        } else {
-          if (local) tmem_ld_32x32b_x32(tl + sb * P::SBUF + (half ^ 1) * kHalf, so);
-          if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
-          tmem_wait_ld_regs(sr);
-          tmem_regs_ready(so);
-          if constexpr (JVP) tmem_regs_ready(tr);
-        }
-        float x[kHalf];
-#pragma unroll
-        for (int c = 0; c < kHalf; ++c) x[c] = __uint_as_float(sr[c]);
-
-        float sc;  // factor taking x to log2 units inside the exponent
-        float mx;
-        bool dead = false;  // no key of the tile kept for any row of this warp
-        if (fast) {
-          sc = p.scale_log2;
-          float xo[kHalf];
-#pragma unroll
-          for (int c = 0; c < kHalf; ++c) xo[c] = __uint_as_float(so[c]);
-          mx = fmaxf(rowmax32(x), rowmax32(xo)) * p.scale_log2;
-        } else if (RING) {
-          // bias from the shared-memory ring (rows 128-byte swizzled: 16-byte
-          // chunk k of row r at chunk k ^ (r mod 8)) for both halves'
-          // columns, so the row maximum needs no exchange
-          sc = 1.f;
-          constexpr int NBR = P::NB > 0 ? P::NB : 1;
-          const int keyo = j * kBN + (half ^ 1) * kHalf;
-          uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
-          uint32_t kmo = keep_bits(keyo, w.kv_len, qi, p.causal);
-          if (has_mask) {
-            // Most tiles of a key-padding or block mask are wholly kept or
-            // wholly masked: only mixed mask bytes need the bit gather.
-            uint32_t any_set = 0u, any_zero = 0u;
-#pragma unroll
-            for (int wd = 0; wd < kHalf / 4; ++wd) {
-              any_set |= mv[wd] | mvo[wd];
-              any_zero |= __vcmpeq4(mv[wd], 0u) | __vcmpeq4(mvo[wd], 0u);
-            }
-            if (any_set == 0u) {
-              km = 0u;
-              kmo = 0u;
-            } else if (any_zero != 0u) {
-              km &= mask_bits32(mv);
-              kmo &= mask_bits32(mvo);
-            }
-          }
-          // warp-uniform tile classes: every key kept (no per-element
-          // selects) or none kept (no arithmetic; P = H = 0)
-          const bool all_keep = __all_sync(0xffffffffu, (km & kmo) == 0xffffffffu);
-          dead = __all_sync(0xffffffffu, (km | kmo) == 0u);
-          if (has_bias) {
-            // the stage is waited on even when unused, so that its next
-            // fill cannot start before this one has landed
-            ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_BF + g % NBR), (g / NBR) & 1u, W));
-            if (!ok) break;
-          }
-          const uint8_t* bbase = smem + P::OFF_BIAS + (g % NBR) * P::BIAS_STAGE + row * 128;
-          float xo[kHalf];
-          if (dead) {
-            mx = -INFINITY;
-          } else if (all_keep && !has_bias) {
-            // as without a mask: the row maximum of the raw scores, scaled once
-            sc = p.scale_log2;
-#pragma unroll
-            for (int c = 0; c < kHalf; ++c) xo[c] = __uint_as_float(so[c]);
-            mx = fmaxf(rowmax32(x), rowmax32(xo)) * p.scale_log2;
-          } else if (all_keep) {
-            // x = s S + bias in natural units (one packed FMA per pair); the
-            // exponent's factor becomes log2 e
-            sc = kLog2e;
-            const uint64_t s2 = f2_make(p.sm_scale, p.sm_scale);
-#pragma unroll
-            for (int k4 = 0; k4 < kHalf / 4; ++k4) {
-              const int phys = (k4 ^ (row & 7)) * 16;
-              const float4 b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
-              const float4 bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
-              const int c = 4 * k4;
-              f2_split(f2_fma(f2_make(x[c], x[c + 1]), s2, f2_make(b4.x, b4.y)), x[c], x[c + 1]);
-              f2_split(f2_fma(f2_make(x[c + 2], x[c + 3]), s2, f2_make(b4.z, b4.w)), x[c + 2], x[c + 3]);
-              f2_split(f2_fma(f2_make(__uint_as_float(so[c]), __uint_as_float(so[c + 1])), s2,
-                              f2_make(bo4.x, bo4.y)),
-                       xo[c], xo[c + 1]);
-              f2_split(f2_fma(f2_make(__uint_as_float(so[c + 2]), __uint_as_float(so[c + 3])), s2,
-                              f2_make(bo4.z, bo4.w)),
-                       xo[c + 2], xo[c + 3]);
-            }
-            mx = fmaxf(rowmax32(x), rowmax32(xo)) * kLog2e;
-          } else {
-#pragma unroll
-            for (int k4 = 0; k4 < kHalf / 4; ++k4) {
-              float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), bo4 = b4;
-              if (has_bias) {
-                const int phys = (k4 ^ (row & 7)) * 16;
-                b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
-                bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
-              }
-              const float bo[4] = {bo4.x, bo4.y, bo4.z, bo4.w};
-              const float bw[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int c = 4 * k4 + e;
-                const float v = fmaf(bw[e], kLog2e, x[c] * p.scale_log2);
-                const float vo = fmaf(bo[e], kLog2e, __uint_as_float(so[c]) * p.scale_log2);
-                x[c] = ((km >> c) & 1u) ? v : -INFINITY;
-                xo[c] = ((kmo >> c) & 1u) ? vo : -INFINITY;
-                if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
-              }
-            }
-            mx = fmaxf(rowmax32(x), rowmax32(xo));
-          }
-          if (has_bias) {
-            // this warp is done with the tile's bias
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(P::B_BE + g % NBR));
-          }
-        } else {
-          sc = 1.f;
-          if constexpr (!BM) {
-            // causal diagonal / ragged tail: both halves under the same mask
-            const int keyo = j * kBN + (half ^ 1) * kHalf;
-            const uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
-            const uint32_t kmo = keep_bits(keyo, w.kv_len, qi, p.causal);
-            float xo[kHalf];
-#pragma unroll
-            for (int c = 0; c < kHalf; ++c) {
-              x[c] = ((km >> c) & 1u) ? x[c] * p.scale_log2 : -INFINITY;
-              xo[c] = ((kmo >> c) & 1u) ? __uint_as_float(so[c]) * p.scale_log2 : -INFINITY;
-              if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
-            }
-            mx = fmaxf(rowmax32(x), rowmax32(xo));
-          } else {
-            uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
-            if (has_mask) km &= mask_bits32(mv);
-#pragma unroll
-            for (int c = 0; c < kHalf; ++c) {
-              float v = x[c] * p.scale_log2;
-              if (has_bias) v = fmaf(bv[c], kLog2e, v);
-              x[c] = ((km >> c) & 1u) ? v : -INFINITY;
-              if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
-            }
-            mx = rowmax32(x);
-            // the pair's row maximum over all 64 columns of the tile; the
-            // slot alternates per tile, and a writer can only come back to a
-            // slot after the rendezvous of the tile in between
-            float* mine = (gen & 1u) ? my_x1 : my_x0;
-            const float* theirs = (gen & 1u) ? other_x1 : other_x0;
-            ++gen;
-            *mine = mx;
-            ok = pair_sync();
-            if (!ok) break;
-            mx = fmaxf(mx, *theirs);
-          }
-        }
-
-        // lazy online-softmax update (identical in both halves)
-        const float m_new = fmaxf(m_run, mx);
-        float alpha = 1.f;
-        bool resc = false;
-        if (m_new > m_run + kRescaleThreshold) {
-          if (m_run != -INFINITY) {
-            alpha = ex2(m_run - m_new);
-            resc = true;
-          }
-          m_run = m_new;
-        }
-        const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-        const uint64_t sc2 = f2_make(sc, sc), nm2 = f2_make(neg_m, neg_m);
-        uint64_t ls = 0;
-        float lt0 = 0.f, lt1 = 0.f, rt0 = 0.f, rt1 = 0.f;
-        uint64_t pv[kHalf / 2];
-        if (!F8 && dead) {
-          // P = H = 0 for the output MMAs; m, l and r stay as they are
-          uint32_t zk[kHalf / 2];
-#pragma unroll
-          for (int c = 0; c < kHalf / 2; ++c) zk[c] = 0u;
-          tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, zk);
-          if constexpr (JVP) tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf + kHalf / 2, zk);
-        } else if constexpr (F8) {
-          // four e5m2 weights per column, half h in the 8 columns at 8 h
-          uint32_t pk8[kHalf / 4];
-#pragma unroll
-          for (int c = 0; c < kHalf; c += 4) {
-            float a0, a1, a2, a3;
-            f2_split(f2_fma(f2_make(x[c], x[c + 1]), sc2, nm2), a0, a1);
-            f2_split(f2_fma(f2_make(x[c + 2], x[c + 3]), sc2, nm2), a2, a3);
-            const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
-            ls = f2_add(ls, f2_add(f2_make(p0, p1), f2_make(p2, p3)));
-            const uint32_t pw = pack_e5m2x4(p0, p1, p2, p3);
-            pk8[c / 4] = pw;
-            add_e5m2x4_f32(pw, lt0, lt1);
-          }
-          tmem_st_32x32b_x8(tl + sb * P::SBUF + kBN + half * (kHalf / 4), pk8);
-        } else {
-        uint32_t pk[kHalf / 2];
-#pragma unroll
-        for (int c = 0; c < kHalf; c += 2) {
-          float a0, a1;
-          f2_split(f2_fma(f2_make(x[c], x[c + 1]), sc2, nm2), a0, a1);
-          const float p0 = ex2(a0), p1 = ex2(a1);
-          const uint64_t pp = f2_make(p0, p1);
-          pv[c / 2] = pp;
-          ls = f2_add(ls, pp);
-          const uint32_t pw = pack2<F16>(p0, p1);
-          pk[c / 2] = pw;
-          add2_f32<F16>(pw, lt0, lt1);
-        }
-        tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, pk);
-        }
-        if (JVP && !dead) {
-          uint32_t hk[kHalf / 2];
-          tmem_wait_ld_regs(tr);
-#pragma unroll
-          for (int c = 0; c < kHalf; c += 2) {
-            const uint64_t ts =
-                f2_mul(f2_make(__uint_as_float(tr[c]), __uint_as_float(tr[c + 1])), scale2);
-            float h0, h1;
-            f2_split(f2_mul(pv[c / 2], ts), h0, h1);
-            const uint32_t hw = pack2<F16>(h0, h1);
-            hk[c / 2] = hw;
-            add2_f32<F16>(hw, rt0, rt1);
-          }
-          tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf + kHalf / 2, hk);
-        }
-        const uint64_t a2 = f2_make(alpha, alpha);
-        l2 = f2_fma(l2, a2, ls);
-        lt2 = f2_fma(lt2, a2, f2_make(lt0, lt1));
-        if constexpr (JVP) r2 = f2_fma(r2, a2, f2_make(rt0, rt1));
-
-        if (__any_sync(0xffffffffu, resc)) {
-          // O and tO are rescaled in place, so the previous tile's output
-          // MMAs must have completed: phase (g-1) / NV of v_empty of its
-          // stage.  The phase after it needs the output MMAs of tile
-          // g-1+NV > g, whose P this thread has not written yet, so the
-          // parity wait is unambiguous.  (resc is never set on a unit's
-          // first tile, where m_run starts at -inf.)
-          ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + (g - 1) % P::NV), ((g - 1) / P::NV) & 1u, W));
+        float m_run = -INFINITY;
+        uint64_t l2 = 0, lt2 = 0, r2 = 0;
+        for (int j = par; j < w.nt; j += 2) {
+          const uint32_t gt = g + static_cast<uint32_t>(j);
+          const uint32_t sb = gt & 1u;
+          ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (gt >> 1) & 1u, W));
           if (!ok) break;
           tc_fence_after();
-          {
-            // (rare: kept as a rolled loop so the tile loop's code stays small)
+          const bool diag = p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
+          const bool fast = !diag && (j * kBN + kBN <= w.kv_len);
+          uint32_t s0[kHalf], s1[kHalf];
+          tmem_ld_32x32b_x32(tl + sb * P::SBUF, s0);
+          tmem_ld_32x32b_x32(tl + sb * P::SBUF + kHalf, s1);
+          tmem_wait_ld_regs(s0);
+          tmem_regs_ready(s1);
+          float x0[kHalf], x1[kHalf];
+#pragma unroll
+          for (int c = 0; c < kHalf; ++c) {
+            x0[c] = __uint_as_float(s0[c]);
+            x1[c] = __uint_as_float(s1[c]);
+          }
+          uint32_t km0 = 0xffffffffu, km1 = 0xffffffffu;
+          if (!fast) {
+            // causal diagonal / ragged tail: masked keys at -inf (raw scores;
+            // the exponent scales them by s log2 e > 0)
+            km0 = keep_bits(j * kBN, w.kv_len, qi, p.causal);
+            km1 = keep_bits(j * kBN + kHalf, w.kv_len, qi, p.causal);
+#pragma unroll
+            for (int c = 0; c < kHalf; ++c) {
+              x0[c] = ((km0 >> c) & 1u) ? x0[c] : -INFINITY;
+              x1[c] = ((km1 >> c) & 1u) ? x1[c] : -INFINITY;
+            }
+          }
+          const float mx = fmaxf(rowmax32(x0), rowmax32(x1)) * p.scale_log2;
+          // lazy online-softmax update of this parity's reference max
+          const float m_new = fmaxf(m_run, mx);
+          float alpha = 1.f;
+          bool resc = false;
+          if (m_new > m_run + kRescaleThreshold) {
+            if (m_run != -INFINITY) {
+              alpha = ex2(m_run - m_new);
+              resc = true;
+            }
+            m_run = m_new;
+          }
+          const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+          const uint64_t nm2 = f2_make(neg_m, neg_m);
+          uint64_t ls = 0;
+          float lt0 = 0.f, lt1 = 0.f, rt0 = 0.f, rt1 = 0.f;
+          // one 32-column half: P (16 columns) then H (16 columns) over the
+          // half's own tS columns, whose load is issued before P is stored
+          auto half_step = [&](const float (&x)[kHalf], uint32_t km, int hh) {
+            const uint32_t colh = tl + sb * P::SBUF + kBN + hh * kHalf;
+            uint32_t tr[kHalf];
+            if constexpr (JVP) tmem_ld_32x32b_x32(colh, tr);
+            uint64_t pv[kHalf / 2];
+            uint32_t pk[kHalf / 2];
+#pragma unroll
+            for (int c = 0; c < kHalf; c += 2) {
+              float a0, a1;
+              f2_split(f2_fma(f2_make(x[c], x[c + 1]), sc2, nm2), a0, a1);
+              const float p0 = ex2(a0), p1 = ex2(a1);
+              const uint64_t pp = f2_make(p0, p1);
+              pv[c / 2] = pp;
+              ls = f2_add(ls, pp);
+              const uint32_t pw = pack2<F16>(p0, p1);
+              pk[c / 2] = pw;
+              add2_f32<F16>(pw, lt0, lt1);
+            }
+            tmem_st_32x32b_x16(colh, pk);
+            if constexpr (JVP) {
+              tmem_wait_ld_regs(tr);
+              if (!fast) {
+#pragma unroll
+                for (int c = 0; c < kHalf; ++c) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
+              }
+              uint32_t hk[kHalf / 2];
+#pragma unroll
+              for (int c = 0; c < kHalf; c += 2) {
+                const uint64_t ts = f2_mul(f2_make(__uint_as_float(tr[c]), __uint_as_float(tr[c + 1])), scale2);
+                float h0, h1;
+                f2_split(f2_mul(pv[c / 2], ts), h0, h1);
+                const uint32_t hw = pack2<F16>(h0, h1);
+                hk[c / 2] = hw;
+                add2_f32<F16>(hw, rt0, rt1);
+              }
+              tmem_st_32x32b_x16(colh + kHalf / 2, hk);
+            }
+          };
+          half_step(x0, km0, 0);
+          half_step(x1, km1, 1);
+          const uint64_t a2 = f2_make(alpha, alpha);
+          l2 = f2_fma(l2, a2, ls);
+          lt2 = f2_fma(lt2, a2, f2_make(lt0, lt1));
+          if constexpr (JVP) r2 = f2_fma(r2, a2, f2_make(rt0, rt1));
+          if (__any_sync(0xffffffffu, resc)) {
+            // O buffer par is rescaled in place once the previous output MMAs
+            // into it (tile gt - 2 of this unit: a parity's first tile never
+            // rescales) are done; the phase after that one needs this tile's
+            // P, so the parity wait is unambiguous
+            const uint32_t gp = gt - 2u;
+            ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + gp % P::NV), (gp / P::NV) & 1u, W));
+            if (!ok) break;
+            tc_fence_after();
             const float a = resc ? alpha : 1.f;
 #pragma unroll 1
-            for (int c0 = 0; c0 < DVH; c0 += 32) {
+            for (int c0 = 0; c0 < P::OBUF; c0 += 32) {
               uint32_t v[32];
-              tmem_ld_32x32b_x32(tl + colo_cur + half * DVH + c0, v);
+              tmem_ld_32x32b_x32(tl + colo_par + c0, v);
               tmem_wait_ld_regs(v);
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-              tmem_st_32x32b_x32(tl + colo_cur + half * DVH + c0, v);
-              if constexpr (JVP) {
-                tmem_ld_32x32b_x32(tl + colo_cur + DV + half * DVH + c0, v);
-                tmem_wait_ld_regs(v);
+              tmem_st_32x32b_x32(tl + colo_par + c0, v);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(P::B_PF + sb));
+        }
+        if (!ok) break;
+
+        // ---------------------------------------------- merge and store
+        float l_a, l_b, lt_a, lt_b, r_a, r_b;
+        f2_split(l2, l_a, l_b);
+        f2_split(lt2, lt_a, lt_b);
+        f2_split(r2, r_a, r_b);
+        // slots [unit parity][value][tile parity][row]: a warp can reuse a
+        // unit parity's slots only after the next unit's rendezvous, which
+        // its partner reaches after reading them
+        float* slot = xchg + (un & 1u) * (8 * kBM);
+        slot[(0 * 2 + par) * kBM + row] = m_run;
+        slot[(1 * 2 + par) * kBM + row] = l_a + l_b;
+        slot[(2 * 2 + par) * kBM + row] = lt_a + lt_b;
+        slot[(3 * 2 + par) * kBM + row] = r_a + r_b;
+        ok = pair_sync();
+        if (!ok) break;
+        // weights of buffer 0 / 1 relative to the merged reference max (an
+        // empty parity weighs 0; both warps compute identical sums)
+        const float m0 = slot[(0 * 2 + 0) * kBM + row], m1 = slot[(0 * 2 + 1) * kBM + row];
+        const float m = fmaxf(m0, m1);
+        const float a0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - m);
+        const float a1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - m);
+        const float l_sum = a0 * slot[(1 * 2 + 0) * kBM + row] + a1 * slot[(1 * 2 + 1) * kBM + row];
+        const float lt_sum = a0 * slot[(2 * 2 + 0) * kBM + row] + a1 * slot[(2 * 2 + 1) * kBM + row];
+        const float r_sum = a0 * slot[(3 * 2 + 0) * kBM + row] + a1 * slot[(3 * 2 + 1) * kBM + row];
+        // every MMA of the unit is done once the output MMAs of its last
+        // tile are; the phase after that one needs a P of the next unit,
+        // which neither warp of this quadrant has written
+        const uint32_t gl = g + static_cast<uint32_t>(w.nt) - 1u;
+        ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + gl % P::NV), (gl / P::NV) & 1u, W));
+        if (!ok) break;
+        tc_fence_after();
+        const bool empty = !(lt_sum > 0.f);
+        const float inv_l = empty ? 0.f : 1.f / lt_sum;
+        // buffer 1 holds no tile of this unit when it has a single tile (a1
+        // is then 0 and its stale contents are not read into the sum)
+        const bool use1 = a1 != 0.f;
+        constexpr int NW = DVH / 2;  // packed words of this warp's columns
+        constexpr int CW = NW / 4;
+        uint32_t po[NW], pt[NW];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-                tmem_st_32x32b_x32(tl + colo_cur + DV + half * DVH + c0, v);
+        for (int c0 = 0; c0 < DVH; c0 += 32) {
+          uint32_t ov0[32], ov1[32], tv0[32], tv1[32];
+          tmem_ld_32x32b_x32(tl + P::COL_O + par * DVH + c0, ov0);
+          tmem_ld_32x32b_x32(tl + P::COL_O + P::OBUF + par * DVH + c0, ov1);
+          if constexpr (JVP) {
+            tmem_ld_32x32b_x32(tl + P::COL_O + DV + par * DVH + c0, tv0);
+            tmem_ld_32x32b_x32(tl + P::COL_O + P::OBUF + DV + par * DVH + c0, tv1);
+          }
+          tmem_wait_ld_regs(ov0);
+          tmem_regs_ready(ov1);
+          if constexpr (JVP) {
+            tmem_regs_ready(tv0);
+            tmem_regs_ready(tv1);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float o[2], t[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float oa = a0 * __uint_as_float(ov0[i + e]);
+              if (use1) oa = fmaf(a1, __uint_as_float(ov1[i + e]), oa);
+              o[e] = oa * inv_l;
+              if constexpr (JVP) {
+                float ta = a0 * __uint_as_float(tv0[i + e]);
+                if (use1) ta = fmaf(a1, __uint_as_float(tv1[i + e]), ta);
+                t[e] = (ta - r_sum * o[e]) * inv_l;
+              }
+            }
+            po[c0 / 2 + i / 2] = pack2<F16>(o[0], o[1]);
+            if constexpr (JVP) pt[c0 / 2 + i / 2] = pack2<F16>(t[0], t[1]);
+          }
+        }
+        // this warp has read both O buffers: the next unit's output MMAs
+        // may write them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(P::B_OE + 0));
+          mbar_arrive(bar(P::B_OE + 1));
+        }
+        if (row_ok && par == 0) p.lse[w.out0 + qi] = empty ? -INFINITY : (m + __log2f(l_sum)) * kLn2;
+        // quad-of-lanes transpose, then whole row segments per store
+        const int q = lane & 3;
+        quad_transpose<CW>(po, q);
+        if constexpr (JVP) quad_transpose<CW>(pt, q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int qk = w.mt * kBM + quad * 32 + (lane & ~3) + k;  // row of slot k
+          const int col = par * DVH + q * 2 * CW;                     // first column of the chunk
+          if (qk < w.q_len && col < p.dv_out) {
+            const long long off = (w.out0 + qk) * p.dv_out + col;
+            store_chunk<CW>(p.o + off, po + k * CW, out32);
+            if constexpr (JVP) store_chunk<CW>(p.to + off, pt + k * CW, out32);
+          }
+        }
+        g += static_cast<uint32_t>(w.nt);
+        ++un;
+      }
+    } else {
+      uint32_t un = 0;         // units with keys seen so far
+      Epi pend{};              // with two O buffers: the unit whose epilogue is due
+      bool has_pend = false;
+      uint32_t g = 0;           // global key-tile counter (same in every role)
+      uint32_t gen = 0;         // masked tiles seen (slot parity of the max exchange)
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_of_round(rnd);
+        if (u >= num_units) break;
+        const Unit w = decode_unit(p, u, list);
+        if (!w.active) continue;
+        const int qi = w.mt * kBM + row;
+        const bool row_ok = qi < w.q_len;
+        if (w.nt == 0) {  // no keys at all: empty rows
+          // this half's output columns: [half * DVH, min((half + 1) * DVH, dv_out))
+          const int ncol = min(DVH, p.dv_out - half * DVH);
+          if (row_ok && ncol > 0) {
+            uint32_t z[DVH / 2];
+#pragma unroll
+            for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
+            if constexpr (F8) {
+              // e5m2 output: one byte per element
+              uint8_t* orow8 = reinterpret_cast<uint8_t*>(p.o) + (w.out0 + qi) * p.dv_out + half * DVH;
+              store_row_bf16(reinterpret_cast<uint16_t*>(orow8), z, ncol / 4);
+            } else {
+              uint16_t* orow = p.o + (w.out0 + qi) * p.dv_out + half * DVH;
+              uint16_t* torow = JVP ? p.to + (w.out0 + qi) * p.dv_out + half * DVH : nullptr;
+              store_row_bf16(orow, z, ncol / 2);
+              if (JVP) store_row_bf16(torow, z, ncol / 2);
+            }
+          }
+          if (row_ok && half == 0) p.lse[w.out0 + qi] = -INFINITY;
+          continue;
+        }
+        const float* brow = nullptr;
+        const unsigned char* mrow = nullptr;
+        if (has_bias)
+          brow = p.bias + w.b * p.bias_stride[0] + w.h * p.bias_stride[1] +
+                 static_cast<long long>(qi) * p.bias_stride[2];
+        if (has_mask)
+          mrow = p.mask + w.b * p.mask_stride[0] + w.h * p.mask_stride[1] +
+                 static_cast<long long>(qi) * p.mask_stride[2];
+
+        // m_run: reference max (log2 units), shared by both halves of a row.
+        // l2: exact partial sum of p (for LSE); lt2 / r2: partial sums of the
+        // bf16 values of p and p*tS that the MMAs consume, so O and tO are
+        // normalised by the weights actually used.  Pairs of fp32 lanes.
+        float m_run = -INFINITY;
+        uint64_t l2 = 0, lt2 = 0, r2 = 0;
+        const uint32_t colo_cur = P::COL_O + (un % P::NOB) * P::OBUF;  // this unit's O buffer
+        for (int j = 0; j < w.nt; ++j, ++g) {
+          const uint32_t sb = g & 1u;
+          const int key0 = j * kBN + half * kHalf;  // first key of this thread's columns
+          // Bias rows stream from HBM once: pull this thread's segment of the
+          // tile two steps ahead into L2 (the first two tiles at unit start),
+          // then load this tile's entries before waiting on S.
+          if (GLOB && has_bias && row_ok && p.bias_stride[3] == 1) {
+            const float* bp = brow + half * kHalf;
+            if (j == 0) {
+              prefetch_l2(bp);
+              if (w.nt > 1) prefetch_l2(bp + kBN);
+            }
+            if (j + 2 < w.nt) prefetch_l2(bp + (j + 2) * kBN);
+          }
+          float bv[kHalf];
+          uint32_t mv[kHalf / 4];
+          uint32_t mvo[kHalf / 4];  // the partner's columns (local row maximum)
+          if (GLOB && has_bias) {
+#pragma unroll
+            for (int c = 0; c < kHalf; ++c) bv[c] = 0.f;
+            if (row_ok) {
+              const float* bp = brow + static_cast<long long>(key0) * p.bias_stride[3];
+              if (p.bias_stride[3] == 1 && (reinterpret_cast<uintptr_t>(bp) & 15u) == 0 &&
+                  key0 + kHalf <= w.kv_len) {
+#pragma unroll
+                for (int c = 0; c < kHalf / 4; ++c) {
+                  const float4 t4 = __ldg(reinterpret_cast<const float4*>(bp) + c);
+                  bv[4 * c] = t4.x;
+                  bv[4 * c + 1] = t4.y;
+                  bv[4 * c + 2] = t4.z;
+                  bv[4 * c + 3] = t4.w;
+                }
+              } else {
+                for (int c = 0; c < kHalf; ++c)
+                  if (key0 + c < w.kv_len) bv[c] = __ldg(bp + c * p.bias_stride[3]);
               }
             }
           }
+          if (has_mask) {
+            load_mask32(mrow, key0, w.kv_len, p.mask_stride[3], row_ok, mv);
+            if (RING) load_mask32(mrow, j * kBN + (half ^ 1) * kHalf, w.kv_len, p.mask_stride[3], row_ok, mvo);
+          }
+
+          ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
+          if (!ok) break;
+          tc_fence_after();
+          // Each warp also reads the partner half's 32 score columns and takes
+          // the row maximum over all 64 itself, so the two warps of a quadrant
+          // never wait for each other: unmasked tiles (`fast`) and masked tiles
+          // (`local`: causal diagonal, ragged tail, mask, and bias read from
+          // the shared-memory ring), the mask applied to both halves.  Only a
+          // bias read per thread from global memory makes the two warps
+          // exchange partial maxima through shared memory instead.
+          const bool diag = p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
+          const bool fast = !BM && !diag && (j * kBN + kBN <= w.kv_len);
+          const bool local = !GLOB && !fast;
+          uint32_t sr[kHalf];
+          uint32_t so[kHalf];
+          uint32_t tr[kHalf];
+          tmem_ld_32x32b_x32(tl + sb * P::SBUF + half * kHalf, sr);
+          if (fast) {
+            tmem_ld_32x32b_x32(tl + sb * P::SBUF + (half ^ 1) * kHalf, so);
+            tmem_wait_ld_regs(sr);
+            tmem_regs_ready(so);
+            // the tangent scores are needed only after the exponentials, so
+            // their load overlaps the row maximum and exp2 below
+            if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
+          } else {
+            if (local) tmem_ld_32x32b_x32(tl + sb * P::SBUF + (half ^ 1) * kHalf, so);
+            if constexpr (JVP) tmem_ld_32x32b_x32(tl + sb * P::SBUF + kBN + half * kHalf, tr);
+            tmem_wait_ld_regs(sr);
+            tmem_regs_ready(so);
+            if constexpr (JVP) tmem_regs_ready(tr);
+          }
+          float x[kHalf];
+#pragma unroll
+          for (int c = 0; c < kHalf; ++c) x[c] = __uint_as_float(sr[c]);
+
+          float sc;  // factor taking x to log2 units inside the exponent
+          float mx;
+          bool dead = false;  // no key of the tile kept for any row of this warp
+          if (fast) {
+            sc = p.scale_log2;
+            float xo[kHalf];
+#pragma unroll
+            for (int c = 0; c < kHalf; ++c) xo[c] = __uint_as_float(so[c]);
+            mx = fmaxf(rowmax32(x), rowmax32(xo)) * p.scale_log2;
+          } else if (RING) {
+            // bias from the shared-memory ring (rows 128-byte swizzled: 16-byte
+            // chunk k of row r at chunk k ^ (r mod 8)) for both halves'
+            // columns, so the row maximum needs no exchange
+            sc = 1.f;
+            constexpr int NBR = P::NB > 0 ? P::NB : 1;
+            const int keyo = j * kBN + (half ^ 1) * kHalf;
+            uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
+            uint32_t kmo = keep_bits(keyo, w.kv_len, qi, p.causal);
+            if (has_mask) {
+              // Most tiles of a key-padding or block mask are wholly kept or
+              // wholly masked: only mixed mask bytes need the bit gather.
+              uint32_t any_set = 0u, any_zero = 0u;
+#pragma unroll
+              for (int wd = 0; wd < kHalf / 4; ++wd) {
+                any_set |= mv[wd] | mvo[wd];
+                any_zero |= __vcmpeq4(mv[wd], 0u) | __vcmpeq4(mvo[wd], 0u);
+              }
+              if (any_set == 0u) {
+                km = 0u;
+                kmo = 0u;
+              } else if (any_zero != 0u) {
+                km &= mask_bits32(mv);
+                kmo &= mask_bits32(mvo);
+              }
+            }
+            // warp-uniform tile classes: every key kept (no per-element
+            // selects) or none kept (no arithmetic; P = H = 0)
+            const bool all_keep = __all_sync(0xffffffffu, (km & kmo) == 0xffffffffu);
+            dead = __all_sync(0xffffffffu, (km | kmo) == 0u);
+            if (has_bias) {
+              // the stage is waited on even when unused, so that its next
+              // fill cannot start before this one has landed
+              ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_BF + g % NBR), (g / NBR) & 1u, W));
+              if (!ok) break;
+            }
+            const uint8_t* bbase = smem + P::OFF_BIAS + (g % NBR) * P::BIAS_STAGE + row * 128;
+            float xo[kHalf];
+            if (dead) {
+              mx = -INFINITY;
+            } else if (all_keep && !has_bias) {
+              // as without a mask: the row maximum of the raw scores, scaled once
+              sc = p.scale_log2;
+#pragma unroll
+              for (int c = 0; c < kHalf; ++c) xo[c] = __uint_as_float(so[c]);
+              mx = fmaxf(rowmax32(x), rowmax32(xo)) * p.scale_log2;
+            } else if (all_keep) {
+              // x = s S + bias in natural units (one packed FMA per pair); the
+              // exponent's factor becomes log2 e
+              sc = kLog2e;
+              const uint64_t s2 = f2_make(p.sm_scale, p.sm_scale);
+#pragma unroll
+              for (int k4 = 0; k4 < kHalf / 4; ++k4) {
+                const int phys = (k4 ^ (row & 7)) * 16;
+                const float4 b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
+                const float4 bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
+                const int c = 4 * k4;
+                f2_split(f2_fma(f2_make(x[c], x[c + 1]), s2, f2_make(b4.x, b4.y)), x[c], x[c + 1]);
+                f2_split(f2_fma(f2_make(x[c + 2], x[c + 3]), s2, f2_make(b4.z, b4.w)), x[c + 2], x[c + 3]);
+                f2_split(f2_fma(f2_make(__uint_as_float(so[c]), __uint_as_float(so[c + 1])), s2,
+                                f2_make(bo4.x, bo4.y)),
+                         xo[c], xo[c + 1]);
+                f2_split(f2_fma(f2_make(__uint_as_float(so[c + 2]), __uint_as_float(so[c + 3])), s2,
+                                f2_make(bo4.z, bo4.w)),
+                         xo[c + 2], xo[c + 3]);
+              }
+              mx = fmaxf(rowmax32(x), rowmax32(xo)) * kLog2e;
+            } else {
+#pragma unroll
+              for (int k4 = 0; k4 < kHalf / 4; ++k4) {
+                float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), bo4 = b4;
+                if (has_bias) {
+                  const int phys = (k4 ^ (row & 7)) * 16;
+                  b4 = *reinterpret_cast<const float4*>(bbase + half * P::BIAS_BOX + phys);
+                  bo4 = *reinterpret_cast<const float4*>(bbase + (half ^ 1) * P::BIAS_BOX + phys);
+                }
+                const float bo[4] = {bo4.x, bo4.y, bo4.z, bo4.w};
+                const float bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int c = 4 * k4 + e;
+                  const float v = fmaf(bw[e], kLog2e, x[c] * p.scale_log2);
+                  const float vo = fmaf(bo[e], kLog2e, __uint_as_float(so[c]) * p.scale_log2);
+                  x[c] = ((km >> c) & 1u) ? v : -INFINITY;
+                  xo[c] = ((kmo >> c) & 1u) ? vo : -INFINITY;
+                  if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
+                }
+              }
+              mx = fmaxf(rowmax32(x), rowmax32(xo));
+            }
+            if (has_bias) {
+              // this warp is done with the tile's bias
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(P::B_BE + g % NBR));
+            }
+          } else {
+            sc = 1.f;
+            if constexpr (!BM) {
+              // causal diagonal / ragged tail: both halves under the same mask
+              const int keyo = j * kBN + (half ^ 1) * kHalf;
+              const uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
+              const uint32_t kmo = keep_bits(keyo, w.kv_len, qi, p.causal);
+              float xo[kHalf];
+#pragma unroll
+              for (int c = 0; c < kHalf; ++c) {
+                x[c] = ((km >> c) & 1u) ? x[c] * p.scale_log2 : -INFINITY;
+                xo[c] = ((kmo >> c) & 1u) ? __uint_as_float(so[c]) * p.scale_log2 : -INFINITY;
+                if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
+              }
+              mx = fmaxf(rowmax32(x), rowmax32(xo));
+            } else {
+              uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
+              if (has_mask) km &= mask_bits32(mv);
+#pragma unroll
+              for (int c = 0; c < kHalf; ++c) {
+                float v = x[c] * p.scale_log2;
+                if (has_bias) v = fmaf(bv[c], kLog2e, v);
+                x[c] = ((km >> c) & 1u) ? v : -INFINITY;
+                if constexpr (JVP) tr[c] = ((km >> c) & 1u) ? tr[c] : 0u;
+              }
+              mx = rowmax32(x);
+              // the pair's row maximum over all 64 columns of the tile; the
+              // slot alternates per tile, and a writer can only come back to a
+              // slot after the rendezvous of the tile in between
+              float* mine = (gen & 1u) ? my_x1 : my_x0;
+              const float* theirs = (gen & 1u) ? other_x1 : other_x0;
+              ++gen;
+              *mine = mx;
+              ok = pair_sync();
+              if (!ok) break;
+              mx = fmaxf(mx, *theirs);
+            }
+          }
+
+          // lazy online-softmax update (identical in both halves)
+          const float m_new = fmaxf(m_run, mx);
+          float alpha = 1.f;
+          bool resc = false;
+          if (m_new > m_run + kRescaleThreshold) {
+            if (m_run != -INFINITY) {
+              alpha = ex2(m_run - m_new);
+              resc = true;
+            }
+            m_run = m_new;
+          }
+          const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+          const uint64_t sc2 = f2_make(sc, sc), nm2 = f2_make(neg_m, neg_m);
+          uint64_t ls = 0;
+          float lt0 = 0.f, lt1 = 0.f, rt0 = 0.f, rt1 = 0.f;
+          uint64_t pv[kHalf / 2];
+          if (!F8 && dead) {
+            // P = H = 0 for the output MMAs; m, l and r stay as they are
+            uint32_t zk[kHalf / 2];
+#pragma unroll
+            for (int c = 0; c < kHalf / 2; ++c) zk[c] = 0u;
+            tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, zk);
+            if constexpr (JVP) tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf + kHalf / 2, zk);
+          } else if constexpr (F8) {
+            // four e5m2 weights per column, half h in the 8 columns at 8 h
+            uint32_t pk8[kHalf / 4];
+#pragma unroll
+            for (int c = 0; c < kHalf; c += 4) {
+              float a0, a1, a2, a3;
+              f2_split(f2_fma(f2_make(x[c], x[c + 1]), sc2, nm2), a0, a1);
+              f2_split(f2_fma(f2_make(x[c + 2], x[c + 3]), sc2, nm2), a2, a3);
+              const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
+              ls = f2_add(ls, f2_add(f2_make(p0, p1), f2_make(p2, p3)));
+              const uint32_t pw = pack_e5m2x4(p0, p1, p2, p3);
+              pk8[c / 4] = pw;
+              add_e5m2x4_f32(pw, lt0, lt1);
+            }
+            tmem_st_32x32b_x8(tl + sb * P::SBUF + kBN + half * (kHalf / 4), pk8);
+          } else {
+          uint32_t pk[kHalf / 2];
+#pragma unroll
+          for (int c = 0; c < kHalf; c += 2) {
+            float a0, a1;
+            f2_split(f2_fma(f2_make(x[c], x[c + 1]), sc2, nm2), a0, a1);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            const uint64_t pp = f2_make(p0, p1);
+            pv[c / 2] = pp;
+            ls = f2_add(ls, pp);
+            const uint32_t pw = pack2<F16>(p0, p1);
+            pk[c / 2] = pw;
+            add2_f32<F16>(pw, lt0, lt1);
+          }
+          tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf, pk);
+          }
+          if (JVP && !dead) {
+            uint32_t hk[kHalf / 2];
+            tmem_wait_ld_regs(tr);
+#pragma unroll
+            for (int c = 0; c < kHalf; c += 2) {
+              const uint64_t ts =
+                  f2_mul(f2_make(__uint_as_float(tr[c]), __uint_as_float(tr[c + 1])), scale2);
+              float h0, h1;
+              f2_split(f2_mul(pv[c / 2], ts), h0, h1);
+              const uint32_t hw = pack2<F16>(h0, h1);
+              hk[c / 2] = hw;
+              add2_f32<F16>(hw, rt0, rt1);
+            }
+            tmem_st_32x32b_x16(tl + sb * P::SBUF + kBN + half * kHalf + kHalf / 2, hk);
+          }
+          const uint64_t a2 = f2_make(alpha, alpha);
+          l2 = f2_fma(l2, a2, ls);
+          lt2 = f2_fma(lt2, a2, f2_make(lt0, lt1));
+          if constexpr (JVP) r2 = f2_fma(r2, a2, f2_make(rt0, rt1));
+
+          if (__any_sync(0xffffffffu, resc)) {
+            // O and tO are rescaled in place, so the previous tile's output
+            // MMAs must have completed: phase (g-1) / NV of v_empty of its
+            // stage.  The phase after it needs the output MMAs of tile
+            // g-1+NV > g, whose P this thread has not written yet, so the
+            // parity wait is unambiguous.  (resc is never set on a unit's
+            // first tile, where m_run starts at -inf.)
+            ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + (g - 1) % P::NV), ((g - 1) / P::NV) & 1u, W));
+            if (!ok) break;
+            tc_fence_after();
+            {
+              // (rare: kept as a rolled loop so the tile loop's code stays small)
+              const float a = resc ? alpha : 1.f;
+#pragma unroll 1
+              for (int c0 = 0; c0 < DVH; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tl + colo_cur + half * DVH + c0, v);
+                tmem_wait_ld_regs(v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+                tmem_st_32x32b_x32(tl + colo_cur + half * DVH + c0, v);
+                if constexpr (JVP) {
+                  tmem_ld_32x32b_x32(tl + colo_cur + DV + half * DVH + c0, v);
+                  tmem_wait_ld_regs(v);
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+                  tmem_st_32x32b_x32(tl + colo_cur + DV + half * DVH + c0, v);
+                }
+              }
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(P::B_PF + sb));
+          if (P::NOB == 2 && j == 0 && has_pend) {
+            // the previous unit's epilogue, now that this unit's first output
+            // MMAs can run
+            has_pend = false;
+            ok = epilogue(pend);
+            if (!ok) break;
+          }
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(P::B_PF + sb));
-        if (P::NOB == 2 && j == 0 && has_pend) {
-          // the previous unit's epilogue, now that this unit's first output
-          // MMAs can run
-          has_pend = false;
-          ok = epilogue(pend);
+        if (!ok) break;
+
+        // ------------------------------------------------------------ epilogue
+        const Epi cur{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g, un};
+        ++un;
+        if constexpr (P::NOB == 2) {
+          // runs after the next unit's first tile
+          pend = cur;
+          has_pend = true;
+        } else {
+          ok = epilogue(cur);
           if (!ok) break;
         }
       }
-      if (!ok) break;
-
-      // ------------------------------------------------------------ epilogue
-      const Epi cur{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g, un};
-      ++un;
-      if constexpr (P::NOB == 2) {
-        // runs after the next unit's first tile
-        pend = cur;
-        has_pend = true;
-      } else {
-        ok = epilogue(cur);
-        if (!ok) break;
-      }
+      if (ok && has_pend) ok = epilogue(pend);
     }
-    if (ok && has_pend) ok = epilogue(pend);
 
     // Jagged rows past max_seq_len inside their sequence: empty rows.  (The
     // e5m2 kernel is dense only.)
