@@ -1079,6 +1079,110 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
       uint32_t un = 0;  // units with keys seen so far
       uint32_t g = 0;   // global key-tile counter of the unit's first tile (same in every role)
+      // Merge the two parities' state of unit e and store its rows.  It
+      // runs after this warp's first tile of the next unit (or at once
+      // when there is none): that tile's softmax needs neither O buffer,
+      // and the next unit's output MMAs wait for o_empty of the merge.
+      auto pp_merge = [&](const Epi& e) -> bool {
+        const int qi = e.mt * kBM + row;
+        const bool row_ok = qi < e.q_len;
+        float l_a, l_b, lt_a, lt_b, r_a, r_b;
+        f2_split(e.l2, l_a, l_b);
+        f2_split(e.lt2, lt_a, lt_b);
+        f2_split(e.r2, r_a, r_b);
+        // slots [unit parity][value][tile parity][row]: a warp can reuse a
+        // unit parity's slots only after the next unit's rendezvous, which
+        // its partner reaches after reading them
+        float* slot = xchg + (e.un & 1u) * (8 * kBM);
+        slot[(0 * 2 + par) * kBM + row] = e.m_run;
+        slot[(1 * 2 + par) * kBM + row] = l_a + l_b;
+        slot[(2 * 2 + par) * kBM + row] = lt_a + lt_b;
+        slot[(3 * 2 + par) * kBM + row] = r_a + r_b;
+        if (!pair_sync()) return false;
+        // weights of buffer 0 / 1 relative to the merged reference max (an
+        // empty parity weighs 0; both warps compute identical sums)
+        const float m0 = slot[(0 * 2 + 0) * kBM + row], m1 = slot[(0 * 2 + 1) * kBM + row];
+        const float m = fmaxf(m0, m1);
+        const float a0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - m);
+        const float a1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - m);
+        const float l_sum = a0 * slot[(1 * 2 + 0) * kBM + row] + a1 * slot[(1 * 2 + 1) * kBM + row];
+        const float lt_sum = a0 * slot[(2 * 2 + 0) * kBM + row] + a1 * slot[(2 * 2 + 1) * kBM + row];
+        const float r_sum = a0 * slot[(3 * 2 + 0) * kBM + row] + a1 * slot[(3 * 2 + 1) * kBM + row];
+        // every MMA of the unit is done once the output MMAs of its last
+        // tile are; the phase after that one is tile gl + NV (NV >= 3), a
+        // tile of the next unit past the first one of each parity, whose P
+        // neither warp of this quadrant has written
+        const uint32_t gl = e.g_end - 1u;
+        if (!__all_sync(0xffffffffu, wait_bar(bar(P::B_VE + gl % P::NV), (gl / P::NV) & 1u, W))) return false;
+        tc_fence_after();
+        const bool empty = !(lt_sum > 0.f);
+        const float inv_l = empty ? 0.f : 1.f / lt_sum;
+        // buffer 1 holds no tile of this unit when it has a single tile (a1
+        // is then 0 and its stale contents are not read into the sum)
+        const bool use1 = a1 != 0.f;
+        constexpr int NW = DVH / 2;  // packed words of this warp's columns
+        constexpr int CW = NW / 4;
+        uint32_t po[NW], pt[NW];
+#pragma unroll
+        for (int c0 = 0; c0 < DVH; c0 += 32) {
+          uint32_t ov0[32], ov1[32], tv0[32], tv1[32];
+          tmem_ld_32x32b_x32(tl + P::COL_O + par * DVH + c0, ov0);
+          tmem_ld_32x32b_x32(tl + P::COL_O + P::OBUF + par * DVH + c0, ov1);
+          if constexpr (JVP) {
+            tmem_ld_32x32b_x32(tl + P::COL_O + DV + par * DVH + c0, tv0);
+            tmem_ld_32x32b_x32(tl + P::COL_O + P::OBUF + DV + par * DVH + c0, tv1);
+          }
+          tmem_wait_ld_regs(ov0);
+          tmem_regs_ready(ov1);
+          if constexpr (JVP) {
+            tmem_regs_ready(tv0);
+            tmem_regs_ready(tv1);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float o[2], t[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float oa = a0 * __uint_as_float(ov0[i + e]);
+              if (use1) oa = fmaf(a1, __uint_as_float(ov1[i + e]), oa);
+              o[e] = oa * inv_l;
+              if constexpr (JVP) {
+                float ta = a0 * __uint_as_float(tv0[i + e]);
+                if (use1) ta = fmaf(a1, __uint_as_float(tv1[i + e]), ta);
+                t[e] = (ta - r_sum * o[e]) * inv_l;
+              }
+            }
+            po[c0 / 2 + i / 2] = pack2<F16>(o[0], o[1]);
+            if constexpr (JVP) pt[c0 / 2 + i / 2] = pack2<F16>(t[0], t[1]);
+          }
+        }
+        // this warp has read both O buffers: the next unit's output MMAs
+        // may write them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(P::B_OE + 0));
+          mbar_arrive(bar(P::B_OE + 1));
+        }
+        if (row_ok && par == 0) p.lse[e.out0 + qi] = empty ? -INFINITY : (m + __log2f(l_sum)) * kLn2;
+        // quad-of-lanes transpose, then whole row segments per store
+        const int q = lane & 3;
+        quad_transpose<CW>(po, q);
+        if constexpr (JVP) quad_transpose<CW>(pt, q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int qk = e.mt * kBM + quad * 32 + (lane & ~3) + k;  // row of slot k
+          const int col = par * DVH + q * 2 * CW;                     // first column of the chunk
+          if (qk < e.q_len && col < p.dv_out) {
+            const long long off = (e.out0 + qk) * p.dv_out + col;
+            store_chunk<CW>(p.o + off, po + k * CW, out32);
+            if constexpr (JVP) store_chunk<CW>(p.to + off, pt + k * CW, out32);
+          }
+        }
+        return true;
+      };
+      Epi ppend{};
+      bool has_ppend = false;
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
@@ -1217,107 +1321,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(P::B_PF + sb));
+          if (has_ppend) {
+            has_ppend = false;
+            ok = pp_merge(ppend);
+            if (!ok) break;
+          }
         }
         if (!ok) break;
-
-        // ---------------------------------------------- merge and store
-        float l_a, l_b, lt_a, lt_b, r_a, r_b;
-        f2_split(l2, l_a, l_b);
-        f2_split(lt2, lt_a, lt_b);
-        f2_split(r2, r_a, r_b);
-        // slots [unit parity][value][tile parity][row]: a warp can reuse a
-        // unit parity's slots only after the next unit's rendezvous, which
-        // its partner reaches after reading them
-        float* slot = xchg + (un & 1u) * (8 * kBM);
-        slot[(0 * 2 + par) * kBM + row] = m_run;
-        slot[(1 * 2 + par) * kBM + row] = l_a + l_b;
-        slot[(2 * 2 + par) * kBM + row] = lt_a + lt_b;
-        slot[(3 * 2 + par) * kBM + row] = r_a + r_b;
-        ok = pair_sync();
-        if (!ok) break;
-        // weights of buffer 0 / 1 relative to the merged reference max (an
-        // empty parity weighs 0; both warps compute identical sums)
-        const float m0 = slot[(0 * 2 + 0) * kBM + row], m1 = slot[(0 * 2 + 1) * kBM + row];
-        const float m = fmaxf(m0, m1);
-        const float a0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - m);
-        const float a1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - m);
-        const float l_sum = a0 * slot[(1 * 2 + 0) * kBM + row] + a1 * slot[(1 * 2 + 1) * kBM + row];
-        const float lt_sum = a0 * slot[(2 * 2 + 0) * kBM + row] + a1 * slot[(2 * 2 + 1) * kBM + row];
-        const float r_sum = a0 * slot[(3 * 2 + 0) * kBM + row] + a1 * slot[(3 * 2 + 1) * kBM + row];
-        // every MMA of the unit is done once the output MMAs of its last
-        // tile are; the phase after that one needs a P of the next unit,
-        // which neither warp of this quadrant has written
-        const uint32_t gl = g + static_cast<uint32_t>(w.nt) - 1u;
-        ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_VE + gl % P::NV), (gl / P::NV) & 1u, W));
-        if (!ok) break;
-        tc_fence_after();
-        const bool empty = !(lt_sum > 0.f);
-        const float inv_l = empty ? 0.f : 1.f / lt_sum;
-        // buffer 1 holds no tile of this unit when it has a single tile (a1
-        // is then 0 and its stale contents are not read into the sum)
-        const bool use1 = a1 != 0.f;
-        constexpr int NW = DVH / 2;  // packed words of this warp's columns
-        constexpr int CW = NW / 4;
-        uint32_t po[NW], pt[NW];
-#pragma unroll
-        for (int c0 = 0; c0 < DVH; c0 += 32) {
-          uint32_t ov0[32], ov1[32], tv0[32], tv1[32];
-          tmem_ld_32x32b_x32(tl + P::COL_O + par * DVH + c0, ov0);
-          tmem_ld_32x32b_x32(tl + P::COL_O + P::OBUF + par * DVH + c0, ov1);
-          if constexpr (JVP) {
-            tmem_ld_32x32b_x32(tl + P::COL_O + DV + par * DVH + c0, tv0);
-            tmem_ld_32x32b_x32(tl + P::COL_O + P::OBUF + DV + par * DVH + c0, tv1);
-          }
-          tmem_wait_ld_regs(ov0);
-          tmem_regs_ready(ov1);
-          if constexpr (JVP) {
-            tmem_regs_ready(tv0);
-            tmem_regs_ready(tv1);
-          }
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float o[2], t[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float oa = a0 * __uint_as_float(ov0[i + e]);
-              if (use1) oa = fmaf(a1, __uint_as_float(ov1[i + e]), oa);
-              o[e] = oa * inv_l;
-              if constexpr (JVP) {
-                float ta = a0 * __uint_as_float(tv0[i + e]);
-                if (use1) ta = fmaf(a1, __uint_as_float(tv1[i + e]), ta);
-                t[e] = (ta - r_sum * o[e]) * inv_l;
-              }
-            }
-            po[c0 / 2 + i / 2] = pack2<F16>(o[0], o[1]);
-            if constexpr (JVP) pt[c0 / 2 + i / 2] = pack2<F16>(t[0], t[1]);
-          }
+        if (has_ppend) {  // this parity had no tile in this unit
+          has_ppend = false;
+          ok = pp_merge(ppend);
+          if (!ok) break;
         }
-        // this warp has read both O buffers: the next unit's output MMAs
-        // may write them
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(P::B_OE + 0));
-          mbar_arrive(bar(P::B_OE + 1));
-        }
-        if (row_ok && par == 0) p.lse[w.out0 + qi] = empty ? -INFINITY : (m + __log2f(l_sum)) * kLn2;
-        // quad-of-lanes transpose, then whole row segments per store
-        const int q = lane & 3;
-        quad_transpose<CW>(po, q);
-        if constexpr (JVP) quad_transpose<CW>(pt, q);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int qk = w.mt * kBM + quad * 32 + (lane & ~3) + k;  // row of slot k
-          const int col = par * DVH + q * 2 * CW;                     // first column of the chunk
-          if (qk < w.q_len && col < p.dv_out) {
-            const long long off = (w.out0 + qk) * p.dv_out + col;
-            store_chunk<CW>(p.o + off, po + k * CW, out32);
-            if constexpr (JVP) store_chunk<CW>(p.to + off, pt + k * CW, out32);
-          }
-        }
+        ppend = Epi{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g + static_cast<uint32_t>(w.nt), un};
+        has_ppend = true;
         g += static_cast<uint32_t>(w.nt);
         ++un;
       }
+      if (ok && has_ppend) ok = pp_merge(ppend);
     } else {
       uint32_t un = 0;         // units with keys seen so far
       Epi pend{};              // with two O buffers: the unit whose epilogue is due
