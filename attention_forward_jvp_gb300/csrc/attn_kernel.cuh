@@ -25,14 +25,18 @@
 //   warp 3      release warp: frees each K stage (and Q at the end of a
 //               unit) as soon as the score MMAs that read it are done.
 //   warps 4..11 softmax / rescale / epilogue: two warps per TMEM lane
-//               quadrant, each taking 32 of the 64 key columns of a row
-//               (row = TMEM lane).  The pair exchanges its partial row
-//               maximum through shared memory once per tile.  Rescaling
-//               is lazy: the reference max m moves (and O, tO, l, r are
-//               multiplied by exp2(m_old - m_new)) only when the row
-//               maximum grows by more than kRescaleThreshold; the result
-//               is exact because l, r and both accumulators share the
-//               same stale reference.
+//               quadrant (row = TMEM lane).  Column halves: each warp
+//               writes P / H for 32 of the 64 key columns of a tile and
+//               reads all 64 scores for the row maximum (only the
+//               per-thread global bias mode exchanges partial maxima
+//               through shared memory).  Ping-pong (head dims 64, no bias
+//               or mask): the two warps take alternate key tiles, all 64
+//               columns, each into its own O / tO buffer, and merge their
+//               row states and buffers once per unit.  Rescaling is lazy:
+//               the reference max m moves (and O, tO, l, r are multiplied
+//               by exp2(m_old - m_new)) only when the row maximum grows by
+//               more than kRescaleThreshold; the result is exact because
+//               l, r and the accumulators share the same stale reference.
 //   Work units (query tile, head, batch or sequence) are walked by every
 //   CTA in a snake over a longest-first order.
 //

@@ -56,18 +56,47 @@ FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 10**6  # GB300 L2
 
 
+def strip_comments(src: str) -> str:
+    """C / C++ / CUDA source without its comments, blank lines and trailing
+    blanks.  One pass: string and character literals are copied as they
+    are, `//` runs to the end of the line, `/* */` to its close."""
+    out = []
+    i, n = 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash(backward: bool = False) -> str:
-    """Hash of the sources a line's kernels are built from (the forward
-    kernels do not include the backward's files)."""
+    """Hash of the code a line's kernels are built from: the sources with
+    comments and blank lines removed, so an edit of the comments keeps the
+    hash (and the profiles recorded for it).  The forward kernels do not
+    include the backward's files."""
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(ROOT, "attention_forward_jvp_gb300", "csrc", "*")))
     if not backward:
         files = [f for f in files if not os.path.basename(f).startswith("attn_bwd")]
     files += sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
     for f in files:
-        with open(f, "rb") as fh:
+        with open(f, encoding="utf-8") as fh:
             h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

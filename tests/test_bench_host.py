@@ -1,0 +1,51 @@
+"""Host logic of bench.py that needs no GPU: the kernel source hash that
+keys the recorded DRAM traffic (profiles/traffic.json) to the code it was
+measured on."""
+import os
+import shutil
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_strip_comments_keeps_code_and_literals():
+    src = ("int a = 1; // line comment /* not a block\n"
+           "/* block\n   // inside */ int b = 2;\n"
+           "\n"
+           "const char* s = \"a // b /* c */\";   \n"
+           "char q = '\\'';  // a quote\n")
+    out = bench.strip_comments(src)
+    assert out.splitlines() == ["int a = 1;", "  int b = 2;",
+                                "const char* s = \"a // b /* c */\";", "char q = '\\'';"]
+
+
+def _copy_sources(dst):
+    for sub in (os.path.join("attention_forward_jvp_gb300", "csrc"), "include"):
+        shutil.copytree(os.path.join(ROOT, sub), os.path.join(dst, sub))
+
+
+def test_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    _copy_sources(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base_f, base_b = bench.kernel_source_hash(), bench.kernel_source_hash(backward=True)
+    k = tmp_path / "attention_forward_jvp_gb300" / "csrc" / "attn_kernel.cuh"
+    text = k.read_text()
+    # a comment edit and blank lines: same hashes
+    k.write_text("// an added comment line\n\n" + text.replace("namespace attn {", "namespace attn {  /* x */", 1))
+    assert bench.kernel_source_hash() == base_f
+    assert bench.kernel_source_hash(backward=True) == base_b
+    # a code edit: both change (the backward includes the forward header)
+    k.write_text(text.replace("namespace attn {", "namespace attn {\nconstexpr int kProbe = 1;", 1))
+    assert bench.kernel_source_hash() != base_f
+    assert bench.kernel_source_hash(backward=True) != base_b
+
+
+def test_backward_sources_do_not_change_the_forward_hash(tmp_path, monkeypatch):
+    _copy_sources(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base_f, base_b = bench.kernel_source_hash(), bench.kernel_source_hash(backward=True)
+    b = tmp_path / "attention_forward_jvp_gb300" / "csrc" / "attn_bwd_kernel.cuh"
+    b.write_text(b.read_text() + "\nconstexpr int kProbe = 2;\n")
+    assert bench.kernel_source_hash() == base_f
+    assert bench.kernel_source_hash(backward=True) != base_b
