@@ -167,3 +167,23 @@ def test_bwd_stages_validation(L):
     assert st(8) == 1            # unknown stage bit
     assert st(7, _shape(B=0)) == 0
     assert st(2, _shape(Dqk=256, Dv=128)) == 2
+
+
+def test_plain_c_caller_compiles_links_and_validates(L, tmp_path):
+    """tests/c/abi_from_c.c, a C99 program using only include/attn_jvp.h,
+    compiles with -pedantic, links against the library and gets the
+    documented status codes back from calls that need no GPU."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "abi_from_c")
+    libdir = os.path.dirname(build.LIB_PATH)
+    cmd = [cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c", "abi_from_c.c"), "-o", exe, "-L", libdir, "-l:libattn_jvp.so",
+           "-Wl,-rpath," + libdir, "-Wl,--allow-shlib-undefined", "-lm"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip().splitlines()[-1] == "0", r.stdout + r.stderr
