@@ -357,19 +357,87 @@ def attn_fwd_f8(q, k, vt, causal: bool = False, sm_scale: Optional[float] = None
     return o, lse
 
 
+_STREAMS = {}
+
+
+def _chunk_streams(dev, n=3):
+    """Streams of the chunked host path (per device, created once)."""
+    key = dev.index
+    if key not in _STREAMS:
+        _STREAMS[key] = [torch.cuda.Stream(dev) for _ in range(n)]
+    return _STREAMS[key]
+
+
+def _slab_chunks(fn, tensors, kw) -> int:
+    """How many chunks of whole (batch, head) slabs the host path of a dense
+    forward call is cut into: 4 when there are at least 8 slabs, every
+    tensor is contiguous and every chunk boundary keeps the 16-byte
+    alignment of the lse rows (M a multiple of 4); else 1."""
+    if fn not in (attn_fwd_jvp, attn_fwd):
+        return 1
+    if any(kw.get(k) is not None for k in ("offsets", "bias", "mask")):
+        return 1
+    q = tensors[0]
+    if q.dim() != 4 or any(t.dim() != 4 or t.shape[:2] != q.shape[:2] or not t.is_contiguous()
+                           for t in tensors):
+        return 1
+    if q.shape[0] * q.shape[1] < 8 or q.shape[2] % 4 != 0:
+        return 1
+    return 4
+
+
 def _host_call(fn, tensors, kw, n_out):
-    """End-to-end path for host tensors: copy in, compute, copy out."""
+    """End-to-end path for host tensors: copy in, compute, copy out.
+
+    A dense forward without bias or mask is cut into chunks of whole
+    (batch, head) slabs, each an independent problem computed by its own
+    call; a chunk's input copies, kernel and output copies run in order on
+    one of three streams, so the copies of one chunk overlap the kernel of
+    another.  The results are those of one call over the whole batch."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    dt = [t.to(dev, non_blocking=True) for t in tensors]
-    for key in ("offsets", "bias", "mask"):
-        if kw.get(key) is not None:
-            kw[key] = kw[key].to(dev, non_blocking=True)
-    outs = fn(*dt, **kw)
-    host = tuple(torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs)
-    for h, o in zip(host, outs):
-        h.copy_(o, non_blocking=True)
-    torch.cuda.current_stream(dev).synchronize()
-    return host[:n_out]
+    n = _slab_chunks(fn, tensors, kw)
+    if n == 1:
+        dt = [t.to(dev, non_blocking=True) for t in tensors]
+        for key in ("offsets", "bias", "mask"):
+            if kw.get(key) is not None:
+                kw[key] = kw[key].to(dev, non_blocking=True)
+        outs = fn(*dt, **kw)
+        host = tuple(torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs)
+        for h, o in zip(host, outs):
+            h.copy_(o, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+        return host[:n_out]
+
+    q, v = tensors[0], tensors[2]
+    B, H, M = q.shape[0], q.shape[1], q.shape[2]
+    S = B * H
+    shapes = [(B, H, M, v.shape[3])] * (n_out - 1) + [(B, H, M)]
+    dtypes = [q.dtype] * (n_out - 1) + [torch.float32]
+    d_in = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in tensors]
+    d_out = [torch.empty(sh, dtype=dt, device=dev) for sh, dt in zip(shapes, dtypes)]
+    h_out = [torch.empty(sh, dtype=dt, pin_memory=True) for sh, dt in zip(shapes, dtypes)]
+
+    def slab(t, a, b):  # slabs [a, b) of a [B, H, ...] tensor, as [1, b - a, ...]
+        return t.view(S, *t.shape[2:])[a:b].view(1, b - a, *t.shape[2:])
+
+    cur = torch.cuda.current_stream(dev)
+    streams = _chunk_streams(dev)
+    for st in streams:
+        st.wait_stream(cur)
+    for c in range(n):
+        a, b = S * c // n, S * (c + 1) // n
+        with torch.cuda.stream(streams[c % len(streams)]):
+            ins = []
+            for h, d in zip(tensors, d_in):
+                dc = slab(d, a, b)
+                dc.copy_(slab(h, a, b), non_blocking=True)
+                ins.append(dc)
+            fn(*ins, out=tuple(slab(o, a, b) for o in d_out), **kw)
+            for ho, o in zip(h_out, d_out):
+                slab(ho, a, b).copy_(slab(o, a, b), non_blocking=True)
+    for st in streams:
+        st.synchronize()
+    return tuple(h_out[:n_out])
 
 
 def default_scale(dqk: int) -> float:

@@ -393,6 +393,24 @@ def test_host_buffers_end_to_end_match_device_path():
     assert np.array_equal(hl.numpy(), L)
 
 
+@pytest.mark.parametrize("jvp", [True, False])
+def test_chunked_host_path_matches_device_path_bitwise(jvp):
+    # 2 x 8 (batch, head) slabs: the host path cuts them into four chunks on
+    # three streams; each slab is an independent problem, so the results are
+    # bit-identical to one call over the whole batch on the device
+    w = Workload("hc", B=2, H=8, M=200, N=200, Dqk=64, Dv=64, causal=True)
+    inp = make_inputs(w, seed=21)
+    assert binding._slab_chunks(binding.attn_fwd_jvp if jvp else binding.attn_fwd,
+                                (inp["q"], inp["k"], inp["v"]), {}) == 4
+    dev_out = run_gpu(inp, jvp=jvp)
+    names = ("q", "k", "v", "tq", "tk", "tv") if jvp else ("q", "k", "v")
+    fn = binding.attn_fwd_jvp if jvp else binding.attn_fwd
+    host_out = fn(*[inp[n].pin_memory() for n in names], causal=True, sm_scale=inp["sm_scale"])
+    assert all(t.device.type == "cpu" for t in host_out)
+    for h, d in zip(host_out, dev_out):
+        assert np.array_equal(h.float().numpy(), d)
+
+
 def test_default_scale_is_inverse_sqrt_dqk():
     inp = make_inputs(Workload("s", B=1, H=1, M=128, N=128, Dqk=128, Dv=64), seed=12)
     inp["sm_scale"] = None
