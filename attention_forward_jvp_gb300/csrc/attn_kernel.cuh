@@ -1076,8 +1076,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if constexpr (P::PP) {
       // ------------------------------------------------ ping-pong softmax
       // This warp takes the tiles j = par, par + 2, ... of every unit, all
-      // 64 key columns, accumulating through O buffer par; at the unit's
-      // end the two parities of a row merge their (m, l, lt, r) and O / tO.
+      // 64 key columns, accumulating through O buffer par; the two parities
+      // of a row merge their (m, l, lt, r) and O / tO once per unit (after
+      // each one's first tile of the next unit, see pp_merge).
       const int par = half;
       const uint32_t colo_par = P::COL_O + static_cast<uint32_t>(par) * P::OBUF;
       const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
