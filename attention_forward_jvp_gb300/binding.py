@@ -424,19 +424,23 @@ def _host_call(fn, tensors, kw, n_out):
     streams = _chunk_streams(dev)
     for st in streams:
         st.wait_stream(cur)
-    for c in range(n):
-        a, b = S * c // n, S * (c + 1) // n
-        with torch.cuda.stream(streams[c % len(streams)]):
-            ins = []
-            for h, d in zip(tensors, d_in):
-                dc = slab(d, a, b)
-                dc.copy_(slab(h, a, b), non_blocking=True)
-                ins.append(dc)
-            fn(*ins, out=tuple(slab(o, a, b) for o in d_out), **kw)
-            for ho, o in zip(h_out, d_out):
-                slab(ho, a, b).copy_(slab(o, a, b), non_blocking=True)
-    for st in streams:
-        st.synchronize()
+    try:
+        for c in range(n):
+            a, b = S * c // n, S * (c + 1) // n
+            with torch.cuda.stream(streams[c % len(streams)]):
+                ins = []
+                for h, d in zip(tensors, d_in):
+                    dc = slab(d, a, b)
+                    dc.copy_(slab(h, a, b), non_blocking=True)
+                    ins.append(dc)
+                fn(*ins, out=tuple(slab(o, a, b) for o in d_out), **kw)
+                for ho, o in zip(h_out, d_out):
+                    slab(ho, a, b).copy_(slab(o, a, b), non_blocking=True)
+    finally:
+        # also when a chunk's call raises: no copy may still be running
+        # when the device buffers are released
+        for st in streams:
+            st.synchronize()
     return tuple(h_out[:n_out])
 
 
