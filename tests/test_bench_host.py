@@ -49,3 +49,27 @@ def test_backward_sources_do_not_change_the_forward_hash(tmp_path, monkeypatch):
     b.write_text(b.read_text() + "\nconstexpr int kProbe = 2;\n")
     assert bench.kernel_source_hash() == base_f
     assert bench.kernel_source_hash(backward=True) != base_b
+
+
+def test_host_path_chunking_decision():
+    """Which host calls the binding cuts into (batch, head) slab chunks: a
+    dense forward without bias, mask or offsets, contiguous, at least 8
+    slabs and M a multiple of 4 (lse rows of a chunk stay 16-byte aligned)."""
+    import torch
+    from attention_forward_jvp_gb300 import binding
+    t = torch.zeros(2, 8, 200, 64, dtype=torch.bfloat16)
+    six, three = (t,) * 6, (t,) * 3
+    assert binding._slab_chunks(binding.attn_fwd_jvp, six, {}) == 4
+    assert binding._slab_chunks(binding.attn_fwd, three, {"bias": None, "mask": None}) == 4
+    assert binding._slab_chunks(binding.attn_fwd, three, {"bias": t}) == 1
+    assert binding._slab_chunks(binding.attn_fwd, three, {"mask": t}) == 1
+    assert binding._slab_chunks(binding.attn_fwd, three, {"offsets": t}) == 1
+    assert binding._slab_chunks(binding.attn_bwd, six, {}) == 1
+    small = torch.zeros(1, 4, 200, 64, dtype=torch.bfloat16)
+    assert binding._slab_chunks(binding.attn_fwd, (small,) * 3, {}) == 1      # 4 slabs
+    odd = torch.zeros(2, 8, 202, 64, dtype=torch.bfloat16)
+    assert binding._slab_chunks(binding.attn_fwd, (odd, t, t), {}) == 1       # M % 4 != 0
+    strided = torch.zeros(2, 8, 64, 200, dtype=torch.bfloat16).transpose(2, 3)
+    assert binding._slab_chunks(binding.attn_fwd, (strided, t, t), {}) == 1   # not contiguous
+    jag = torch.zeros(8, 1000, 64, dtype=torch.bfloat16)
+    assert binding._slab_chunks(binding.attn_fwd, (jag,) * 3, {}) == 1        # [H, T, D]
