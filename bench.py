@@ -53,6 +53,7 @@ METRIC_BWD = "attn backward (dQ, dK, dV) TFLOP/s (bf16, 1xGB300) and fraction of
 METRIC_F8 = "attn FP8 (e5m2) forward TFLOP/s (1xGB300) and fraction of the fp8 tensor peak"
 FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense fp8 : bf16 tensor rate of a GB300
 FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 10**6  # GB300 L2
 
 
@@ -114,7 +115,26 @@ def peaks():
         with open(p) as fh:
             d = json.load(fh)
         return d, "measured"
-    return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+    return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def roofline(flops: float, nbytes: float, seconds: float, pk: dict, pk_kind: str) -> dict:
+    """Roofline of one launch of the forward kernel.  The bound is whichever
+    takes longer at the measured peaks: the tensor time (flops at the bf16
+    peak) or the HBM time (algorithmic bytes at the copy bandwidth); achieved
+    is that unit's algorithmic work over the measured launch time, and the
+    other unit's figure is kept beside it."""
+    tf_peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    gb_peak = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
+    tflops = flops / seconds / 1e12
+    gbs = nbytes / seconds / 1e9
+    if nbytes / (gb_peak * 1e9) > flops / (tf_peak * 1e12):
+        return {"bound": "hbm", "achieved": gbs, "peak": gb_peak, "unit": "GB/s", "frac": gbs / gb_peak,
+                "peak_kind": f"{pk_kind} copy bandwidth", "algorithmic_bytes": nbytes,
+                "tflops": tflops, "tflops_frac": tflops / tf_peak}
+    return {"bound": "tensor", "achieved": tflops, "peak": tf_peak, "unit": "TFLOP/s", "frac": tflops / tf_peak,
+            "peak_kind": f"{pk_kind} bf16 burst (kernel timed alone)", "algorithmic_bytes": nbytes,
+            "hbm_gbs": gbs}
 
 
 class ClockSampler:
@@ -386,9 +406,9 @@ def run_ours(args, w, world, rank, local):
         ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms, world)
     value = world * flops / (ms_max * 1e-3) / 1e12
-    # the step is exactly one launch of the fused kernel, so its average
-    # launch duration is the per-step device time measured on its stream
-    achieved = flops / (ms * 1e-3) / 1e12
+    # (the step is exactly one launch of the fused kernel, so ms, its
+    # per-step device time measured on its stream, is also the launch
+    # duration the roofline below divides by)
 
     # end to end through the public API with pinned host buffers
     host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "tq", "tk", "tv")}
@@ -422,11 +442,8 @@ def run_ours(args, w, world, rank, local):
             rec = json.load(fh).get(w.name)
         if rec and rec.get("kernel_hash") == kernel_source_hash():
             traffic = rec.get("dram_bytes_per_launch")
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": traffic,
-            "peak_kind": f"{pk_kind} bf16 burst (kernel timed alone)",
-            "algorithmic_bytes": min_hbm_bytes(w, inp),
-            "hbm_gbs": min_hbm_bytes(w, inp) / (ms * 1e-3) / 1e9}
+    roof = roofline(flops, min_hbm_bytes(w, inp), ms * 1e-3, pk, pk_kind)
+    roof["traffic"] = traffic
     cpu = None
     if world == 1 and not args.skip_cpu_baseline:
         # heads (jagged: sequences) one at a time until about cpu_seconds of

@@ -73,3 +73,18 @@ def test_host_path_chunking_decision():
     assert binding._slab_chunks(binding.attn_fwd, (strided, t, t), {}) == 1   # not contiguous
     jag = torch.zeros(8, 1000, 64, dtype=torch.bfloat16)
     assert binding._slab_chunks(binding.attn_fwd, (jag,) * 3, {}) == 1        # [H, T, D]
+
+
+def test_roofline_bound_follows_the_longer_time():
+    """bias + mask (77.3 GFLOP, 318.9 MB) is HBM-bound at the measured
+    peaks (47.6 us of copies against 41.4 us of tensor work); the causal
+    workload (412 GFLOP, 269 MB) is tensor-bound."""
+    pk = {"bf16_tflops": 1868.7, "hbm_gbs": 6695.5}
+    r = bench.roofline(77.3e9, 318.9e6, 107.4e-6, pk, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - 318.9e6 / 107.4e-6 / 1e9) < 1e-6
+    assert abs(r["frac"] - r["achieved"] / 6695.5) < 1e-12
+    assert abs(r["tflops"] - 77.3e9 / 107.4e-6 / 1e12) < 1e-9
+    r = bench.roofline(412.3e9, 269.0e6, 276.1e-6, pk, "measured")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["frac"] - 412.3e9 / 276.1e-6 / 1e12 / 1868.7) < 1e-12
