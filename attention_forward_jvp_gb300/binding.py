@@ -12,7 +12,6 @@ call raises.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from typing import Optional
 
@@ -154,6 +153,15 @@ def _need(t: torch.Tensor, name: str, dtype, dev):
         raise ValueError(f"{name} is on {t.device}, expected {dev}")
 
 
+def _need_out(t: torch.Tensor, name: str, shape, dtype, dev):
+    """A caller-given output: the library writes its whole extent, so it
+    must be exactly the shape, dtype and device the call produces, and
+    contiguous."""
+    _need(t, name, dtype, dev)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 def _describe(q, k, v, offsets, max_seq_len, bias, mask):
     """Shape struct + bias struct (with the tensors kept alive)."""
     sh = AttnShape()
@@ -239,6 +247,9 @@ def attn_fwd_jvp(q, k, v, tq, tk, tv, causal: bool = False, sm_scale: Optional[f
         lse = torch.empty(out_shape[:-1], dtype=torch.float32, device=dev)
     else:
         o, to, lse = out
+        _need_out(o, "o", out_shape, dt, dev)
+        _need_out(to, "to", out_shape, dt, dev)
+        _need_out(lse, "lse", out_shape[:-1], torch.float32, dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
     fn = lib().attn_fwd_jvp_f16 if dt == torch.float16 else lib().attn_fwd_jvp
     st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(tq), _ptr(tk),
@@ -270,6 +281,8 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: Optional[float] = None,
         lse = torch.empty(out_shape[:-1], dtype=torch.float32, device=dev)
     else:
         o, lse = out
+        _need_out(o, "o", out_shape, dt, dev)
+        _need_out(lse, "lse", out_shape[:-1], torch.float32, dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
     fn = lib().attn_fwd_f16 if dt == torch.float16 else lib().attn_fwd
     st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(offsets),
@@ -312,6 +325,10 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float
         delta = torch.empty(out_shape[:-1], dtype=torch.float32, device=dev)
     else:
         dq, dk, dv, delta = out
+        _need_out(dq, "dq", q.shape, dt, dev)
+        _need_out(dk, "dk", k.shape, dt, dev)
+        _need_out(dv, "dv", v.shape, dt, dev)
+        _need_out(delta, "delta", out_shape[:-1], torch.float32, dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
     if stages == BWD_ALL:
         fn = lib().attn_bwd_f16 if dt == torch.float16 else lib().attn_bwd
@@ -350,6 +367,8 @@ def attn_fwd_f8(q, k, vt, causal: bool = False, sm_scale: Optional[float] = None
         lse = torch.empty((B, H, M), dtype=torch.float32, device=dev)
     else:
         o, lse = out
+        _need_out(o, "o", (B, H, M, D), dt, dev)
+        _need_out(lse, "lse", (B, H, M), torch.float32, dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
     st = lib().attn_fwd_f8(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(vt), 1 if causal else 0,
                            _scale(sm_scale), _ptr(o), _ptr(lse), ctypes.c_void_p(stream))
@@ -442,7 +461,3 @@ def _host_call(fn, tensors, kw, n_out):
         for st in streams:
             st.synchronize()
     return tuple(h_out[:n_out])
-
-
-def default_scale(dqk: int) -> float:
-    return 1.0 / math.sqrt(dqk)

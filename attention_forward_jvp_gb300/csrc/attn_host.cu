@@ -772,24 +772,40 @@ attn_status attn_fwd_f8(const attn_shape* shape, const void* q, const void* k, c
 
 attn_status attn_sync_check(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
-  DeviceState* ds = nullptr;
-  attn_status st = device_state(&ds);
-  if (st != ATTN_OK) return st;
-  int word = 0;
-  if (cudaMemcpy(&word, ds->scratch, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  if (word != 0) {
-    if (cudaMemset(ds->scratch, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_ERR_TIMEOUT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  // The error words that exist on this device: the per-device scratch of
+  // the allocating entry points and the fixed array of the allocation-free
+  // one, each only once a call has set it up.  Nothing here allocates.
+  int* words[2];
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    words[0] = g_dev[dev].scratch;
   }
-  return ATTN_OK;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    words[1] = g_noalloc_dev[dev].scratch;
+  }
+  bool timed_out = false;
+  for (int* w : words) {
+    if (w == nullptr) continue;
+    int word = 0;
+    if (cudaMemcpy(&word, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (word != 0) {
+      if (cudaMemset(w, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+      timed_out = true;
+    }
+  }
+  return timed_out ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 const char* attn_status_string(attn_status s) {
   switch (s) {
     case ATTN_OK: return "ok";
     case ATTN_ERR_INVALID_ARG: return "invalid argument";
-    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration (head dims must be 64 or 128; bias/mask dense only)";
+    case ATTN_ERR_UNSUPPORTED:
+      return "unsupported configuration for this entry point (head dims, bias / mask with jagged inputs, "
+             "FP8 key count; attn_jvp.h lists each entry point's supported set)";
     case ATTN_ERR_MISALIGNED: return "a device pointer is not 16-byte aligned";
     case ATTN_ERR_CUDA: return "CUDA error (no device, launch failure or driver entry point missing)";
     case ATTN_ERR_TIMEOUT: return "a device pipeline wait ran out of time; outputs are undefined";

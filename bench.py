@@ -139,12 +139,12 @@ def roofline(flops: float, nbytes: float, seconds: float, pk: dict, pk_kind: str
 
 class ClockSampler:
     """Samples the SM clock and the clock-event (throttle) reasons of one GPU
-    every few milliseconds through NVML (read-only queries), in a thread.
+    every millisecond through NVML (read-only queries), in a thread.
     mark() tags the samples taken from then on as the timed region."""
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index: int, period_s: float = 0.005):
+    def __init__(self, device_index: int, period_s: float = 0.001):
         import ctypes
         import threading
         self.period = period_s

@@ -181,8 +181,9 @@ attn_status attn_fwd_f8(const attn_shape* shape,
  * array's device address; make that first call before any stream capture.
  * Each call clears the error word on `stream` before its launch.  All calls
  * share the array, so calls that overlap on the GPU (other streams) race on
- * it; a wait that runs out of time in this variant is not reported to the
- * host (use attn_fwd_jvp with attn_sync_check where that matters). */
+ * it.  A wait that runs out of time in this variant is reported by the next
+ * attn_sync_check on the device, which reads (and clears) this array's
+ * error word too and allocates nothing. */
 attn_status attn_fwd_jvp_noalloc(const attn_shape* shape,
                                  const void* q, const void* k, const void* v,
                                  const void* tq, const void* tk, const void* tv,
@@ -257,10 +258,12 @@ attn_status attn_bwd_stages(const attn_shape* shape,
                             void* dq, void* dk, void* dv, float* delta,
                             int f16, unsigned stages, void* stream);
 
-/* Synchronises `stream`, then reads and clears the error word of the
- * current device.  Returns ATTN_ERR_TIMEOUT if a launch since the last
- * check reported a timed-out wait, ATTN_ERR_CUDA on a CUDA error, else
- * ATTN_OK. */
+/* Synchronises `stream`, then reads and clears the error words of the
+ * current device: the scratch of the allocating entry points and the fixed
+ * array of attn_fwd_jvp_noalloc, each once a call on the device has set it
+ * up (nothing is allocated here).  Returns ATTN_ERR_TIMEOUT if a launch
+ * since the last check reported a timed-out wait, ATTN_ERR_CUDA on a CUDA
+ * error, else ATTN_OK. */
 attn_status attn_sync_check(void* stream);
 
 /* Static description of a status code; never NULL. */
