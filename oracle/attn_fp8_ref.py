@@ -73,10 +73,9 @@ def attention_fwd_e5m2(q, k, v, causal=False, sm_scale=None):
 def e5m2_bound_terms(q, k, v, sm_scale, causal=False):
     """Float64 quantities the e5m2 roundings are bounded by, per output
     element of one head: B = sum_j w_j |V_j| (w the exact softmax weights)
-    and the exact output O = sum_j w_j V_j.  A weight w_j rounded to
-    w_j (1 + d_j), |d_j| <= 2^-3, moves the output by at most 2^-3 B when the
-    row sum is the unrounded one and by at most 2^-3 / (1 - 2^-3) * sum_j
-    w_j |V_j - O| <= 0.143 (B + |O|) when it is the rounded one."""
+    and the exact output O = sum_j w_j V_j.  Weights w_j rounded to
+    w_j (1 + d_j), |d_j| <= 2^-3, with the row sum of the unrounded weights
+    (the tutorial's order), move the output by at most 2^-3 B."""
     m_rows, n = q.shape[0], k.shape[0]
     ok = valid_keys(m_rows, n, causal, None, None)
     if n == 0:

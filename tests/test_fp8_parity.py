@@ -1,24 +1,30 @@
 """GPU parity of the FP8 (e5m2) forward (attn_fwd_f8) against the FP8
 oracle (oracle.attention_fwd_e5m2: the tutorial's steps in float64 on the
-e5m2 inputs).
+e5m2 inputs: the row sum l from the unrounded weights, the weights cast to
+e5m2 for the P V product, O = e5m2((e5m2(p) V) / l)).
 
-Tolerance, derived from the arithmetic (the pages' own test allows atol 3):
+Tolerance, derived from the arithmetic for that step order (the pages' own
+test allows atol 3):
   * LSE within 1e-3: S is the exact e5m2 products summed in fp32 on both
     sides; only the exponent and the log differ;
-  * O elementwise.  Both sides round every weight w_j to e5m2 (|d_j| <=
-    2^-3), but the kernel rounds it relative to its running maximum, which
-    does not trail the row maximum by a power of two, so its rounding
-    decisions are independent of the oracle's.  With B = sum_j w_j |V_j| and
-    O_x the exact output (oracle.e5m2_bound_terms): the oracle (row sum of
-    the unrounded weights) moves by at most 2^-3 B, the kernel (row sum of
-    the rounded ones) by at most 0.143 (B + |O_x|), and each output rounding
-    by 2^-3 of its value:
-        |O - O_oracle| <= 0.27 B + 0.15 |O_x| + 2^-3 (|O| + |O_oracle|) + 2^-15
-    (2^-15: twice the subnormal spacing of e5m2);
-  * O in aggregate: ||O - O_oracle||_2 <= 0.2 ||O_oracle||_2.  Two
-    independent roundings to a grid of relative spacing <= 2^-2 differ by
-    at most 2^-2 / sqrt(6) = 0.10 relative RMS; the weights add less unless
-    a row has very few keys.
+  * O elementwise.  Both sides normalise by the sum of the unrounded
+    weights and round every weight w_j to e5m2 (|d_j| <= 2^-3 relative),
+    but the kernel rounds it relative to its running maximum, which does not
+    trail the row maximum by a power of two, so its rounding decisions are
+    independent of the oracle's.  With B = sum_j w_j |V_j| and O_x the
+    exact output (oracle.e5m2_bound_terms), each side's output before its
+    final rounding is within (2^-3 + 2^-20) B of O_x (2^-20 covers the
+    kernel's fp32 exponentials, products and row sum), and the final
+    rounding moves a value u by at most 2^-3 |u| <= |O| / 7 (normal range;
+    2^-17 absolute for subnormals):
+        |O - O_oracle| <= 0.2502 B + 0.143 (|O| + |O_oracle|) + 2^-15;
+  * O in aggregate: ||O - O_oracle||_2 <= 0.15 ||O_oracle||_2.  The
+    difference is the sum of four independent roundings (the weights on
+    each side, the output on each side), each at most 2^-2 / sqrt(12) =
+    0.072 relative RMS (uniform error at the coarsest relative spacing of
+    the e5m2 grid, 2^-2); with i.i.d. zero-mean V the weight roundings
+    relate to ||O|| the way the output roundings do, so the sum is at most
+    2 x 0.072 = 0.144 relative RMS.
 """
 import numpy as np
 import pytest
@@ -56,17 +62,19 @@ def run_f8(q, k, v, causal, sm_scale):
 
 
 def assert_f8_close(O, L, Or, Lr, Bt, Ox, what):
+    """Ox is kept for callers; the bound needs B and the two outputs."""
     assert np.isfinite(O).all(), what
     inf_r = np.isneginf(Lr)
     assert np.array_equal(np.isneginf(L), inf_r), f"{what}: empty-row LSE pattern"
     if (~inf_r).any():
         el = np.abs(L[~inf_r] - Lr[~inf_r]).max()
         assert el <= 1e-3, f"{what}: LSE err {el:.3e}"
-    bound = 0.27 * Bt + 0.15 * np.abs(Ox) + 2.0 ** -3 * (np.abs(O) + np.abs(Or)) + 2.0 ** -15
+    bound = 0.2502 * Bt + 0.143 * (np.abs(O) + np.abs(Or)) + 2.0 ** -15
     bad = np.abs(O - Or) > bound
     assert not bad.any(), f"{what}: {int(bad.sum())} elements outside the bound, e.g. {O[bad][:4]} vs {Or[bad][:4]}"
     rel = np.linalg.norm(O - Or) / max(np.linalg.norm(Or), 1e-30)
-    assert rel <= 0.2, f"{what}: relative L2 {rel:.3f}"
+    assert rel <= 0.15, f"{what}: relative L2 {rel:.3f}"
+    print(f"{what}: relative L2 {rel:.4f}, worst element at {float((np.abs(O - Or) / bound).max()):.3f} of its bound")
     return rel
 
 
