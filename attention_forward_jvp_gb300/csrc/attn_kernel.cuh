@@ -1648,10 +1648,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               f2_split(f2_fma(f2_make(x[c + 2], x[c + 3]), sc2, nm2), a2, a3);
               const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
               ls = f2_add(ls, f2_add(f2_make(p0, p1), f2_make(p2, p3)));
-              const uint32_t pw = pack_e5m2x4(p0, p1, p2, p3);
-              pk8[c / 4] = pw;
-              add_e5m2x4_f32(pw, lt0, lt1);
+              pk8[c / 4] = pack_e5m2x4(p0, p1, p2, p3);
             }
+            // the normaliser is the row sum of the unrounded weights: the
+            // tutorial takes it before the cast to e5m2
+            f2_split(ls, lt0, lt1);
             tmem_st_32x32b_x8(tl + sb * P::SBUF + kBN + half * (kHalf / 4), pk8);
           } else {
           uint32_t pk[kHalf / 2];

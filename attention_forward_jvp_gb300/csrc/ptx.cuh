@@ -387,11 +387,5 @@ __device__ __forceinline__ uint32_t pack_e5m2x4(float a, float b, float c, float
   asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
-// acc0 += bytes 0 + 2, acc1 += bytes 1 + 3 of a packed e5m2 word, widened
-// exactly: an e5m2 value is the upper byte of the fp16 with the same value.
-__device__ __forceinline__ void add_e5m2x4_f32(uint32_t w, float& acc0, float& acc1) {
-  add_f16x2_f32(__byte_perm(w, 0u, 0x1404u), acc0, acc1);  // bytes 0, 1 as fp16 pair
-  add_f16x2_f32(__byte_perm(w, 0u, 0x3424u), acc0, acc1);  // bytes 2, 3
-}
 
 }  // namespace attn

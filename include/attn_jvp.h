@@ -152,9 +152,10 @@ attn_status attn_fwd_f16(const attn_shape* shape,
  * D = Dqk = Dv in {64, 128} (else ATTN_ERR_UNSUPPORTED); N a multiple of
  * 16 (the rows of vt are N bytes and bulk copies need 16-byte strides;
  * else ATTN_ERR_UNSUPPORTED); causal requires M == N.  S is accumulated in
- * fp32 from the e5m2 products, P is rounded to e5m2 for the P V product,
- * and O is normalised by the sum of the rounded weights, then rounded to
- * e5m2 (nearest even, saturating).  Other conventions as attn_fwd.
+ * fp32 from the e5m2 products, the row sum is taken from the fp32 weights,
+ * P is then rounded to e5m2 for the P V product (the tutorial's order), and
+ * O = (e5m2(P) V) / sum is rounded to e5m2 (nearest even, saturating).
+ * Other conventions as attn_fwd.
  * Pointers, shape fields T / max_seq_len: as attn_fwd (T ignored). */
 attn_status attn_fwd_f8(const attn_shape* shape,
                         const void* q, const void* k, const void* vt,
