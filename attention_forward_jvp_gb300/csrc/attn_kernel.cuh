@@ -809,21 +809,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // half of the first chain.  The first output MMAs of a unit overwrite
     // the O buffer: with two buffers they wait until the epilogue of unit
     // un - 2 has read it.
-    // jt: the tile's index within its unit.  Ping-pong softmax: tile jt
-    // accumulates into O buffer jt % 2, whose first write in a unit waits
-    // until the previous unit's epilogue has read both buffers.
+    // jt: the tile's index within its unit.  Ping-pong softmax: tile t
+    // accumulates into O buffer t % 2 (the buffer of the softmax warps that
+    // take the tiles of its global parity); the first write of a unit into
+    // each buffer (tiles jt = 0 and 1) overwrites it, once the previous
+    // unit's merge has read both buffers: the unit's first tile waits for
+    // that on both o_empty barriers, so every unit waits each barrier's
+    // phases in order.
     auto issue_pv = [&](uint32_t t, int jt, uint32_t un, auto&& mid) -> bool {
       const uint32_t sb = t & 1u;
       const bool first = P::PP ? jt < 2 : jt == 0;
       if (!wait_v(t) || !wait_all(bar(P::B_PF + sb), (t >> 1) & 1u)) return false;
       if constexpr (P::PP) {
-        if (first && !wait_all(bar(P::B_OE + jt), (un & 1u) ^ 1u)) return false;
+        if (jt == 0 && !(wait_all(bar(P::B_OE + 0), (un & 1u) ^ 1u) &&
+                         wait_all(bar(P::B_OE + 1), (un & 1u) ^ 1u)))
+          return false;
       } else {
         if (P::NOB == 2 && first && !wait_all(bar(P::B_OE + un % P::NOB), ((un / P::NOB) & 1u) ^ 1u))
           return false;
       }
       tc_fence_after();
-      const uint32_t colo = P::COL_O + (P::PP ? static_cast<uint32_t>(jt & 1) : un % P::NOB) * P::OBUF;
+      const uint32_t colo = P::COL_O + (P::PP ? sb : un % P::NOB) * P::OBUF;
       const uint32_t lv = lo_v + (t % P::NV) * (P::V_STAGE >> 4);
       // keys [16 kk, 16 kk + 16): P at column base + 32 (kk / 2) + 8 (kk % 2),
       // H 16 columns further (the layout the softmax halves write)
@@ -1075,10 +1081,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     bool ok = true;
     if constexpr (P::PP) {
       // ------------------------------------------------ ping-pong softmax
-      // This warp takes the tiles j = par, par + 2, ... of every unit, all
-      // 64 key columns, accumulating through O buffer par; the two parities
-      // of a row merge their (m, l, lt, r) and O / tO once per unit (after
-      // each one's first tile of the next unit, see pp_merge).
+      // This warp takes the key tiles whose global index (the counter every
+      // role keeps) is par mod 2 -- the tiles of score buffer par -- all 64
+      // key columns, accumulating through O buffer par; the two parities of
+      // a row merge their (m, l, lt, r) and O / tO once per unit (after each
+      // one's first tile of the next unit, see pp_merge).  Binding the warp
+      // to the buffer, not to the tile's index within its unit, makes it
+      // wait every phase of its s_full and p_full barriers in order: after
+      // a unit with an odd tile count the in-unit parity would hand it a
+      // tile whose barrier's previous phase belonged to the other warp and
+      // could still be pending, and a parity wait two phases behind returns
+      // at once.
       const int par = half;
       const uint32_t colo_par = P::COL_O + static_cast<uint32_t>(par) * P::OBUF;
       const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
@@ -1122,9 +1135,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_fence_after();
         const bool empty = !(lt_sum > 0.f);
         const float inv_l = empty ? 0.f : 1.f / lt_sum;
-        // buffer 1 holds no tile of this unit when it has a single tile (a1
-        // is then 0 and its stale contents are not read into the sum)
-        const bool use1 = a1 != 0.f;
+        // a buffer holds no tile of this unit when its parity had none (its
+        // weight is then 0 and its stale contents are not read into the sum)
+        const bool use0 = a0 != 0.f, use1 = a1 != 0.f;
         constexpr int NW = DVH / 2;  // packed words of this warp's columns
         constexpr int CW = NW / 4;
         uint32_t po[NW], pt[NW];
@@ -1148,11 +1161,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             float o[2], t[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              float oa = a0 * __uint_as_float(ov0[i + e]);
+              float oa = use0 ? a0 * __uint_as_float(ov0[i + e]) : 0.f;
               if (use1) oa = fmaf(a1, __uint_as_float(ov1[i + e]), oa);
               o[e] = oa * inv_l;
               if constexpr (JVP) {
-                float ta = a0 * __uint_as_float(tv0[i + e]);
+                float ta = use0 ? a0 * __uint_as_float(tv0[i + e]) : 0.f;
                 if (use1) ta = fmaf(a1, __uint_as_float(tv1[i + e]), ta);
                 t[e] = (ta - r_sum * o[e]) * inv_l;
               }
@@ -1209,7 +1222,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         float m_run = -INFINITY;
         uint64_t l2 = 0, lt2 = 0, r2 = 0;
-        for (int j = par; j < w.nt; j += 2) {
+        for (int j = (par ^ static_cast<int>(g)) & 1; j < w.nt; j += 2) {
           const uint32_t gt = g + static_cast<uint32_t>(j);
           const uint32_t sb = gt & 1u;
           ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (gt >> 1) & 1u, W));

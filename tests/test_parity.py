@@ -105,6 +105,34 @@ def test_full_size_forward_only_equals_jvp_primal():
     assert np.array_equal(O, O2) and np.array_equal(L, L2)
 
 
+@pytest.mark.parametrize("case", ["dense", "jagged"])
+def test_many_units_per_cta_with_odd_tile_counts(case):
+    """Units with odd key-tile counts, many per CTA: each unit boundary
+    shifts which score buffer a unit's first tile uses, so the softmax
+    warps' barrier phases must stay in order across boundaries.  Dense
+    D = 64 with 15 key tiles per unit (8 x 16 x 8 = 1024 units); jagged
+    D = 64 with 400 sequences of 64 k + 1 .. 64 k + 64 tokens (odd and
+    even tile counts, one-tile units).  NaN-prefilled, whole output."""
+    if case == "dense":
+        w = Workload("odd", B=8, H=16, M=1024, N=960, Dqk=64, Dv=64, sm_scale=0.125)
+        inp = make_inputs(w, seed=50)
+        ref = None
+    else:
+        g = torch.Generator().manual_seed(51)
+        lens = (64 * torch.randint(0, 7, (400,), generator=g) + torch.randint(1, 65, (400,), generator=g)).tolist()
+        w = Workload("oddj", B=400, H=4, Dqk=64, Dv=64, jagged=True, max_seq_len=448, max_len_draw=1,
+                     sm_scale=0.125)
+        inp = make_inputs(w, seed=52, lengths=lens)
+        ref = oracle.attention_fwd_jvp_jagged(inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"],
+                                              inp["offsets"], 448, sm_scale=0.125)
+    for rep in range(2):
+        O, tO, L = run_gpu(inp, nan_prefill=True)
+        assert not np.isnan(O).any() and not np.isnan(tO).any() and not np.isnan(L).any()
+        if ref is None:
+            ref = oracle_dense(inp)
+        assert_close(O, tO, L, *ref, what=f"{case} run {rep}")
+
+
 # ------------------------------------------------------------- edge shapes
 EDGE = [
     # B, H, M, N, Dqk, Dv, causal
