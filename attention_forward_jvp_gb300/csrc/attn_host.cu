@@ -21,61 +21,33 @@ static_assert(attn::kPlanBM == attn::kBM && attn::kPlanBN == attn::kBN,
 
 // The kernels are instantiated once, in the attn_inst_*.cu files; these
 // declarations keep this file from instantiating its own copies.
+#define ATTN_FWD_DECL(DQ, DVV, JVP, BM, F16) \
+  extern template cudaError_t launch_attn<DQ, DVV, JVP, BM, F16>(const KernelParams&, int, cudaStream_t);
+// every bias mode, both element types
+#define ATTN_FWD_DECL_ALL(DQ, DVV, JVP)                                                   \
+  ATTN_FWD_DECL(DQ, DVV, JVP, kNoBias, false) ATTN_FWD_DECL(DQ, DVV, JVP, kNoBias, true)       \
+  ATTN_FWD_DECL(DQ, DVV, JVP, kBiasRing, false) ATTN_FWD_DECL(DQ, DVV, JVP, kBiasRing, true)   \
+  ATTN_FWD_DECL(DQ, DVV, JVP, kBiasGlobal, false) ATTN_FWD_DECL(DQ, DVV, JVP, kBiasGlobal, true)
+// no bias ring (its plan does not fit shared memory)
+#define ATTN_FWD_DECL_NORING(DQ, DVV, JVP)                                              \
+  ATTN_FWD_DECL(DQ, DVV, JVP, kNoBias, false) ATTN_FWD_DECL(DQ, DVV, JVP, kNoBias, true)       \
+  ATTN_FWD_DECL(DQ, DVV, JVP, kBiasGlobal, false) ATTN_FWD_DECL(DQ, DVV, JVP, kBiasGlobal, true)
 namespace attn {
-extern template cudaError_t launch_attn<64, 64, true, kNoBias, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, true, kNoBias, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, true, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, true, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, true, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, true, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, kNoBias, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, kNoBias, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, true, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, kNoBias, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, kNoBias, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, true, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, kNoBias, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, kNoBias, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, true, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 64, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<64, 128, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 64, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<128, 128, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<256, 256, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<256, 256, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<256, 256, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<256, 256, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn<256, 256, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+ATTN_FWD_DECL_ALL(64, 64, true)
+ATTN_FWD_DECL_ALL(64, 128, true)
+ATTN_FWD_DECL_ALL(128, 64, true)
+ATTN_FWD_DECL_ALL(128, 128, true)
+ATTN_FWD_DECL_NORING(256, 64, true)
+ATTN_FWD_DECL_NORING(256, 128, true)
+ATTN_FWD_DECL_ALL(64, 64, false)
+ATTN_FWD_DECL_ALL(64, 128, false)
+ATTN_FWD_DECL_ALL(128, 64, false)
+ATTN_FWD_DECL_ALL(128, 128, false)
+ATTN_FWD_DECL_ALL(256, 64, false)
+ATTN_FWD_DECL_ALL(256, 128, false)
+ATTN_FWD_DECL_ALL(64, 256, false)
+ATTN_FWD_DECL_ALL(128, 256, false)
+ATTN_FWD_DECL_ALL(256, 256, false)
 extern template cudaError_t launch_attn<64, 64, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<128, 128, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn_bwd<64, 64, false, false>(const BwdParams&, int, cudaStream_t);
@@ -98,38 +70,58 @@ extern template cudaError_t launch_attn_bwd<128, 128, true, true>(const BwdParam
 
 namespace {
 
-// The kernel instantiation for (Dqk, Dv) = key (0..3: bit 1 set for
-// Dqk = 128, bit 0 for Dv = 128, else 64; 4: 256 x 256, forward only),
-// tangents, bias / mask mode and element type.
+// One instantiation; a bias ring whose plan does not fit shared memory
+// (Dqk = 256 with tangents) reads the bias per thread instead.
+template <int DQ, int DVK, bool JVP, int BMODE, bool F16>
+cudaError_t launch_fitting(const attn::KernelParams& kp, int grid, cudaStream_t cs) {
+  if constexpr (BMODE == attn::kBiasRing && !attn::Plan<DQ, DVK, JVP, attn::kBiasRing>::FITS)
+    return attn::launch_attn<DQ, DVK, JVP, attn::kBiasGlobal, F16>(kp, grid, cs);
+  else
+    return attn::launch_attn<DQ, DVK, JVP, BMODE, F16>(kp, grid, cs);
+}
+
+// The kernel instantiation for the kernel head dims (kq, kv), each 64, 128
+// or 256 (16 and 32 run as 64; with tangents kv = 256 runs as two column
+// slices of kv = 128), tangents, bias / mask mode and element type.
 template <bool JVP, int BMODE, bool F16>
-cudaError_t dispatch_dims(int key, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
-  switch (key) {
-    case 0: return attn::launch_attn<64, 64, JVP, BMODE, F16>(kp, grid, cs);
-    case 1: return attn::launch_attn<64, 128, JVP, BMODE, F16>(kp, grid, cs);
-    case 2: return attn::launch_attn<128, 64, JVP, BMODE, F16>(kp, grid, cs);
-    case 3: return attn::launch_attn<128, 128, JVP, BMODE, F16>(kp, grid, cs);
-    case 4:  // head dims 256 x 256, forward only
-      if constexpr (!JVP) return attn::launch_attn<256, 256, false, BMODE, F16>(kp, grid, cs);
+cudaError_t dispatch_dims(int kq, int kv, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
+  switch (kq * 1000 + kv) {
+    case 64064: return launch_fitting<64, 64, JVP, BMODE, F16>(kp, grid, cs);
+    case 64128: return launch_fitting<64, 128, JVP, BMODE, F16>(kp, grid, cs);
+    case 128064: return launch_fitting<128, 64, JVP, BMODE, F16>(kp, grid, cs);
+    case 128128: return launch_fitting<128, 128, JVP, BMODE, F16>(kp, grid, cs);
+    case 256064: return launch_fitting<256, 64, JVP, BMODE, F16>(kp, grid, cs);
+    case 256128: return launch_fitting<256, 128, JVP, BMODE, F16>(kp, grid, cs);
+    case 64256:
+      if constexpr (!JVP) return launch_fitting<64, 256, false, BMODE, F16>(kp, grid, cs);
+      break;
+    case 128256:
+      if constexpr (!JVP) return launch_fitting<128, 256, false, BMODE, F16>(kp, grid, cs);
+      break;
+    case 256256:
+      if constexpr (!JVP) return launch_fitting<256, 256, false, BMODE, F16>(kp, grid, cs);
       break;
   }
   return cudaErrorInvalidValue;
 }
 
 template <bool JVP, bool F16>
-cudaError_t dispatch_mode(int key, int mode, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
+cudaError_t dispatch_mode(int kq, int kv, int mode, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
   switch (mode) {
-    case attn::kNoBias: return dispatch_dims<JVP, attn::kNoBias, F16>(key, kp, grid, cs);
-    case attn::kBiasRing: return dispatch_dims<JVP, attn::kBiasRing, F16>(key, kp, grid, cs);
-    case attn::kBiasGlobal: return dispatch_dims<JVP, attn::kBiasGlobal, F16>(key, kp, grid, cs);
+    case attn::kNoBias: return dispatch_dims<JVP, attn::kNoBias, F16>(kq, kv, kp, grid, cs);
+    case attn::kBiasRing: return dispatch_dims<JVP, attn::kBiasRing, F16>(kq, kv, kp, grid, cs);
+    case attn::kBiasGlobal: return dispatch_dims<JVP, attn::kBiasGlobal, F16>(kq, kv, kp, grid, cs);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t dispatch_attn(int key, bool jvp, int mode, bool f16, const attn::KernelParams& kp, int grid,
+cudaError_t dispatch_attn(int kq, int kv, bool jvp, int mode, bool f16, const attn::KernelParams& kp, int grid,
                           cudaStream_t cs) {
   if (f16)
-    return jvp ? dispatch_mode<true, true>(key, mode, kp, grid, cs) : dispatch_mode<false, true>(key, mode, kp, grid, cs);
-  return jvp ? dispatch_mode<true, false>(key, mode, kp, grid, cs) : dispatch_mode<false, false>(key, mode, kp, grid, cs);
+    return jvp ? dispatch_mode<true, true>(kq, kv, mode, kp, grid, cs)
+               : dispatch_mode<false, true>(kq, kv, mode, kp, grid, cs);
+  return jvp ? dispatch_mode<true, false>(kq, kv, mode, kp, grid, cs)
+             : dispatch_mode<false, false>(kq, kv, mode, kp, grid, cs);
 }
 
 constexpr int kMaxDevices = 64;
@@ -273,11 +265,20 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   if (s == nullptr) return ATTN_ERR_INVALID_ARG;
   const bool jagged = offsets != nullptr;
   if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0) return ATTN_ERR_INVALID_ARG;
-  auto dim_ok = [](int d) { return d == 16 || d == 32 || d == 64 || d == 128; };
-  // 256 x 256 only without tangents: O and tO of 256 columns each would take
-  // all 512 tensor-memory columns, leaving none for the scores
-  const bool d256 = s->Dqk == 256 && s->Dv == 256;
-  if (!(d256 && !jvp) && (!dim_ok(s->Dqk) || !dim_ok(s->Dv))) return ATTN_ERR_UNSUPPORTED;
+  auto dim_ok = [](int d) { return d == 16 || d == 32 || d == 64 || d == 128 || d == 256; };
+  if (!dim_ok(s->Dqk) || !dim_ok(s->Dv)) return ATTN_ERR_UNSUPPORTED;
+  // kernel head dims: 16 and 32 run zero-padded to 64 (the tensor maps keep
+  // the true dims and their 64-column boxes read zeros past them).  With
+  // tangents, Dv = 256 runs as two column slices of 128: O and tO of 256
+  // columns each would take all 512 tensor-memory columns, leaving none for
+  // the scores, so each slice is its own work unit.
+  const int kq = s->Dqk < 64 ? 64 : s->Dqk;
+  int kv = s->Dv < 64 ? 64 : s->Dv;
+  int n_vh = 1;  // (the kernels with tangents and kv = 128 read it)
+  if (jvp && kv == 256) {
+    kv = 128;
+    n_vh = 2;
+  }
   if (!std::isnan(sm_scale) && !(sm_scale > 0.f && std::isfinite(sm_scale)))
     return ATTN_ERR_INVALID_ARG;
   const bool has_bias = bias != nullptr && (bias->bias != nullptr || bias->mask != nullptr);
@@ -322,6 +323,7 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   const float scale = std::isnan(sm_scale) ? 1.0f / std::sqrt(static_cast<float>(s->Dqk)) : sm_scale;
   kp.B = s->B;
   kp.H = s->H;
+  kp.n_vh = n_vh;
   kp.jagged = jagged ? 1 : 0;
   kp.causal = causal ? 1 : 0;
   kp.sm_scale = scale;
@@ -386,7 +388,7 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
     }
   }
   if (!ok) return ATTN_ERR_CUDA;
-  const int64_t units = static_cast<int64_t>(s->B) * s->H * kp.n_mt;
+  const int64_t units = static_cast<int64_t>(s->B) * s->H * kp.n_mt * n_vh;
   if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   kp.num_units = static_cast<int>(units);
   int grid = static_cast<int>(units < ds->num_sms ? units : ds->num_sms);
@@ -413,15 +415,12 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
     kp.unit_count = lbuf;
   }
   cudaError_t e = cudaErrorInvalidValue;
-  // head dims 16 and 32 run the 64-wide kernels: the tensor maps keep the
-  // true dims and their 64-column boxes read zeros past them
-  const int key = d256 ? 4 : (s->Dqk == 128 ? 2 : 0) + (s->Dv == 128 ? 1 : 0);
   // bias through the shared-memory ring when a tensor map describes it,
   // else per-thread loads; a mask alone also takes the ring mode
   const int mode = (kp.bias == nullptr && kp.mask == nullptr) ? attn::kNoBias
                    : (kp.bias != nullptr && kp.bias_tma == 0) ? attn::kBiasGlobal
                                                                : attn::kBiasRing;
-  e = dispatch_attn(key, jvp, mode, f16, kp, grid, cs);
+  e = dispatch_attn(kq, kv, jvp, mode, f16, kp, grid, cs);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   g_launches.fetch_add(1);
   return ATTN_OK;
@@ -458,6 +457,7 @@ attn_status run_f8(const attn_shape* s, const void* q, const void* k, const void
   kp.causal = causal ? 1 : 0;
   kp.sm_scale = scale;
   kp.scale_log2 = scale * attn::kLog2e;
+  kp.n_vh = 1;
   kp.o = static_cast<uint16_t*>(o);  // e5m2 bytes; the kernel addresses them as such
   kp.lse = lse;
   kp.dv_out = s->Dv;

@@ -83,7 +83,12 @@ struct KernelParams {
   int B, H, M, N;  // jagged: B = sequences, M = N = max_seq_len
   int jagged, causal;
   int n_mt;        // query tiles per (b, h) or per (sequence, h)
-  int num_units;   // units in the fixed slot order (B * H * n_mt)
+  // output column slices per query tile: 1, or 2 when the kernel's DV is
+  // half of the output head dim (tangents at Dv = 256: O and tO of 256
+  // columns each do not fit tensor memory beside the scores, so each slice
+  // of 128 columns is its own work unit, which recomputes the scores)
+  int n_vh;
+  int num_units;   // units in the fixed slot order (B * H * n_mt * n_vh)
   // Jagged work list (optional): unit_count[0] (sequence, query tile) pairs,
   // costliest first, at unit_list (x = sequence, y = tile); unit u is pair
   // u / H, head u % H.  A count of -1 means the list was not written.
@@ -168,12 +173,16 @@ struct Plan {
   // stages still fit beside them, else one
   static constexpr int NB = BMODE != kBiasRing ? 0 : (FIXED + 2 * BIAS_STAGE + 2 * K_STAGE + 2 * V_STAGE <= BUDGET) ? 2 : 1;
   static constexpr int RING = BUDGET - NB * BIAS_STAGE;
+  // (one K stage only when two do not fit: Dqk = 256 with tangents, whose
+  // Q and tQ take 128 KB)
   static constexpr int NK = (FIXED + 4 * K_STAGE + 4 * V_STAGE <= RING)   ? 4
                             : (FIXED + 3 * K_STAGE + 2 * V_STAGE <= RING) ? 3
-                                                                          : 2;
+                            : (FIXED + 2 * K_STAGE + V_STAGE <= RING)     ? 2
+                                                                          : 1;
   static constexpr int NV = (FIXED + NK * K_STAGE + 4 * V_STAGE <= RING)   ? 4
                             : (FIXED + NK * K_STAGE + 3 * V_STAGE <= RING) ? 3
-                                                                           : 2;
+                            : (FIXED + NK * K_STAGE + 2 * V_STAGE <= RING) ? 2
+                                                                           : 1;
   static constexpr int OFF_Q = 0;       // buffer b at OFF_Q + b * QSET
   static constexpr int OFF_TQ = Q_TILE;  // buffer b at OFF_TQ + b * QSET
   static constexpr int OFF_K = FIXED;
@@ -215,7 +224,10 @@ struct Plan {
   // Requested dynamic shared memory: never less than half an SM's, so one
   // CTA (and its TMEM allocation) owns an SM.
   static constexpr int SMEM_LAUNCH = SMEM_BYTES > 120 * 1024 ? SMEM_BYTES : 120 * 1024;
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
+  // whether the plan fits one CTA's shared memory (the host does not launch
+  // an instantiation that does not: a bias ring at Dqk = 256 with tangents
+  // falls back to per-thread bias loads)
+  static constexpr bool FITS = SMEM_BYTES <= 227 * 1024;
   static_assert(COLS_USED <= 512, "tensor memory plan exceeds 512 columns");
   static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims are multiples of 64");
   static_assert(V_TILE % 1024 == 0, "V tiles keep 1024-byte alignment");
@@ -231,14 +243,27 @@ struct Unit {
   int nt;           // key tiles visited
   int b, h;
   long long out0;   // row index of query 0 in the [.., rows] output view
+  int vh;           // output column slice: columns [vh * DV, vh * DV + DV)
   bool active;
 };
 
 // Work unit u.  Causal dense units and (without a work list) jagged units
 // are ordered by descending query tile, so the costliest units start first;
-// a jagged work list is already ordered by cost.
+// a jagged work list is already ordered by cost.  SLICES: the kernel may
+// run output column slices (tangents with a 128-wide kernel DV); other
+// kernels carry no slice arithmetic.
+template <bool SLICES>
 __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u, const int2* list) {
   Unit w;
+  // the column slices of one query tile are adjacent units (they share Q, K
+  // and V tiles through L2)
+  w.vh = 0;
+  if constexpr (SLICES) {
+    if (p.n_vh > 1) {
+      w.vh = u % p.n_vh;
+      u /= p.n_vh;
+    }
+  }
   const int BH = p.B * p.H;
   if (!p.jagged) {
     int bh, mt;
@@ -475,6 +500,8 @@ __device__ __forceinline__ float rowmax32(const float* x) {
 template <int DQK, int DV, bool JVP, int BMODE, bool F16, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KernelParams p) {
   using P = Plan<DQK, DV, JVP, BMODE, F8>;
+  // output column slices (tangents at Dv = 256 run the 128-wide kernels)
+  constexpr bool kSlices = JVP && DV == 128;
   constexpr bool BM = BMODE != kNoBias;
   constexpr bool RING = BMODE == kBiasRing;
   constexpr bool GLOB = BMODE == kBiasGlobal;
@@ -551,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int c = __ldg(p.unit_count);
     if (c >= 0) {
       list = p.unit_list;
-      num_units = c * p.H;
+      num_units = c * p.H * (kSlices && p.n_vh > 1 ? p.n_vh : 1);
     }
   }
 
@@ -567,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit(p, u, list);
+        const Unit w = decode_unit<kSlices>(p, u, list);
         if (w.nt == 0) continue;
         const uint32_t qb = qfill % P::NQB;
         ok = wait_bar(bar(P::B_QE + qb), ((qfill / P::NQB) & 1u) ^ 1u, W);
@@ -628,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit(p, u, list);
+        const Unit w = decode_unit<kSlices>(p, u, list);
         for (int j = 0; j < w.nt; ++j) {
           const int r = w.row0 + j * kBN;
           if constexpr (P::NB > 0) {
@@ -666,10 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           } else {
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c) {
-            tma_load_3d(vdst + c * P::V_SUB, &p.tm_v, bar(P::B_VF + vs), c * 64, r, w.z);
-            if (JVP)
-              tma_load_3d(vdst + P::V_TILE + c * P::V_SUB, &p.tm_tv, bar(P::B_VF + vs), c * 64, r,
-                          w.z);
+            const int x = w.vh * DV + c * 64;  // this unit's column slice
+            tma_load_3d(vdst + c * P::V_SUB, &p.tm_v, bar(P::B_VF + vs), x, r, w.z);
+            if (JVP) tma_load_3d(vdst + P::V_TILE + c * P::V_SUB, &p.tm_tv, bar(P::B_VF + vs), x, r, w.z);
           }
           }
           ++vfill;
@@ -702,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_of_round(rnd);
       if (u >= num_units) break;
-      const Unit w = decode_unit(p, u, list);
+      const Unit w = decode_unit<kSlices>(p, u, list);
       if (w.nt == 0) continue;
       for (int j = 0; j < w.nt; ++j, ++g) {
         ok = __all_sync(0xffffffffu, wait_bar_sleep(bar(P::B_SF + (g & 1u)), (g >> 1) & 1u, W));
@@ -878,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit(p, u, list);
+        const Unit w = decode_unit<kSlices>(p, u, list);
         if (w.nt == 0) continue;
         ok = wait_all(bar(P::B_QF), quse & 1u);
         if (!ok) break;
@@ -911,7 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit(p, u, list);
+        const Unit w = decode_unit<kSlices>(p, u, list);
         if (w.nt == 0) continue;
         const uint32_t qb = quse % P::NQB;
         ok = wait_all(bar(P::B_QF + qb), (quse / P::NQB) & 1u);
@@ -977,6 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint64_t l2, lt2, r2;
       uint32_t g_end;  // one past the unit's last tile
       uint32_t un;     // unit index among units with keys (O buffer un % NOB)
+      int vh;          // output column slice
     };
     float* my_xl = xchg + 4 * kBM + row;  // the epilogue's third value (l of half 1)
     // Normalise and store one unit's O, tO and LSE rows.
@@ -1055,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(P::B_OE + e.un % P::NOB));
       }
-      if (row_ok && half == 0)
+      if (row_ok && half == 0 && e.vh == 0)
         p.lse[e.out0 + qi] = empty ? -INFINITY : (e.m_run + __log2f(l_sum)) * kLn2;
       // Rows are stored a quad of lanes at a time: after the transpose lane q
       // of a quad holds chunk q of the quad's four rows, so each store
@@ -1065,8 +1092,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if constexpr (JVP) quad_transpose<CW>(pt, q);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int qk = e.mt * kBM + quad * 32 + (lane & ~3) + k;  // row of slot k
-        const int col = half * DVH + q * EPW * CW;                 // first column of the chunk
+        const int qk = e.mt * kBM + quad * 32 + (lane & ~3) + k;       // row of slot k
+        const int col = e.vh * DV + half * DVH + q * EPW * CW;          // first column of the chunk
         if (qk < e.q_len && col < p.dv_out) {
           const long long off = (e.out0 + qk) * p.dv_out + col;
           if constexpr (F8)
@@ -1204,7 +1231,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit(p, u, list);
+        const Unit w = decode_unit<kSlices>(p, u, list);
         if (!w.active) continue;
         const int qi = w.mt * kBM + row;
         const bool row_ok = qi < w.q_len;
@@ -1351,7 +1378,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ok = pp_merge(ppend);
           if (!ok) break;
         }
-        ppend = Epi{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g + static_cast<uint32_t>(w.nt), un};
+        ppend = Epi{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g + static_cast<uint32_t>(w.nt), un, 0};
         has_ppend = true;
         g += static_cast<uint32_t>(w.nt);
         ++un;
@@ -1366,29 +1393,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit(p, u, list);
+        const Unit w = decode_unit<kSlices>(p, u, list);
         if (!w.active) continue;
         const int qi = w.mt * kBM + row;
         const bool row_ok = qi < w.q_len;
         if (w.nt == 0) {  // no keys at all: empty rows
-          // this half's output columns: [half * DVH, min((half + 1) * DVH, dv_out))
-          const int ncol = min(DVH, p.dv_out - half * DVH);
+          // this half's output columns: [c0, min(c0 + DVH, dv_out))
+          const int c0 = w.vh * DV + half * DVH;
+          const int ncol = min(DVH, p.dv_out - c0);
           if (row_ok && ncol > 0) {
             uint32_t z[DVH / 2];
 #pragma unroll
             for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
             if constexpr (F8) {
               // e5m2 output: one byte per element
-              uint8_t* orow8 = reinterpret_cast<uint8_t*>(p.o) + (w.out0 + qi) * p.dv_out + half * DVH;
+              uint8_t* orow8 = reinterpret_cast<uint8_t*>(p.o) + (w.out0 + qi) * p.dv_out + c0;
               store_row_bf16(reinterpret_cast<uint16_t*>(orow8), z, ncol / 4);
             } else {
-              uint16_t* orow = p.o + (w.out0 + qi) * p.dv_out + half * DVH;
-              uint16_t* torow = JVP ? p.to + (w.out0 + qi) * p.dv_out + half * DVH : nullptr;
+              uint16_t* orow = p.o + (w.out0 + qi) * p.dv_out + c0;
+              uint16_t* torow = JVP ? p.to + (w.out0 + qi) * p.dv_out + c0 : nullptr;
               store_row_bf16(orow, z, ncol / 2);
               if (JVP) store_row_bf16(torow, z, ncol / 2);
             }
           }
-          if (row_ok && half == 0) p.lse[w.out0 + qi] = -INFINITY;
+          if (row_ok && half == 0 && w.vh == 0) p.lse[w.out0 + qi] = -INFINITY;
           continue;
         }
         const float* brow = nullptr;
@@ -1749,7 +1777,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!ok) break;
 
         // ------------------------------------------------------------ epilogue
-        const Epi cur{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g, un};
+        const Epi cur{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g, un, w.vh};
         ++un;
         if constexpr (P::NOB == 2) {
           // runs after the next unit's first tile
@@ -1776,8 +1804,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             uint32_t z[DV / 2];
 #pragma unroll
             for (int i = 0; i < DV / 2; ++i) z[i] = 0u;
-            store_row_bf16(p.o + o_row * p.dv_out, z, p.dv_out / 2);
-            if (JVP) store_row_bf16(p.to + o_row * p.dv_out, z, p.dv_out / 2);
+            // the whole row (every column slice), DV columns at a time
+            for (int c0 = 0; c0 < p.dv_out; c0 += DV) {
+              const int n = min(DV, p.dv_out - c0);
+              store_row_bf16(p.o + o_row * p.dv_out + c0, z, n / 2);
+              if (JVP) store_row_bf16(p.to + o_row * p.dv_out + c0, z, n / 2);
+            }
             p.lse[o_row] = -INFINITY;
           }
         }
@@ -1794,6 +1826,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 template <int DQK, int DV, bool JVP, int BMODE, bool F16, bool F8 = false>
 cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
   using P = Plan<DQK, DV, JVP, BMODE, F8>;
+  static_assert(P::FITS, "shared memory plan exceeds 227 KB");
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -20,6 +20,7 @@ Workload names follow what they are, not where they came from:
   causal      B2 H16 N4096 D128  causal, tangents N(0, 0.5^2)
   jagged      64 sequences, lengths U{1..1024}, H8 D64, packed [H, T, D]
   bias_mask   B2 H8 M=N=2048 Dqk128 Dv64, fp32 bias N(0,1), keys >= 1536 masked
+  causal_d256 B2 H16 N4096 Dqk=Dv=256 causal, tangents N(0, 0.5^2)
 """
 from __future__ import annotations
 
@@ -66,6 +67,10 @@ WORKLOADS = {
                        max_seq_len=1024, max_len_draw=1024, sm_scale=1.0 / 8),
     "bias_mask": Workload("bias_mask", B=2, H=8, M=2048, N=2048, Dqk=128, Dv=64, bias=True,
                           mask_keep=1536),
+    # head dim 256 with tangents (the widest head dim the kernels accept);
+    # the causal workload's shape and distributions otherwise
+    "causal_d256": Workload("causal_d256", B=2, H=16, M=4096, N=4096, Dqk=256, Dv=256, causal=True,
+                            tangent_std=0.5, sm_scale=1.0 / 16),
 }
 
 

@@ -137,84 +137,106 @@ def roofline(flops: float, nbytes: float, seconds: float, pk: dict, pk_kind: str
             "hbm_gbs": gbs}
 
 
+_SAMPLER_CHILD = r"""
+import ctypes, sys, time
+nv = ctypes.CDLL("libnvidia-ml.so.1")
+if nv.nvmlInit_v2() != 0:
+    sys.exit(0)
+h = ctypes.c_void_p()
+key, period = sys.argv[1], float(sys.argv[2])
+ok = False
+if key.startswith("GPU-"):
+    ok = nv.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(h)) == 0
+elif key.startswith("PCI:"):
+    ok = nv.nvmlDeviceGetHandleByPciBusId_v2(key[4:].encode(), ctypes.byref(h)) == 0
+if not ok:
+    ok = nv.nvmlDeviceGetHandleByIndex_v2(int(sys.argv[3]), ctypes.byref(h)) == 0
+if not ok:
+    sys.exit(0)
+fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+c, m, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+print("ready", flush=True)
+while True:
+    t = time.monotonic()
+    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) == 0:
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m))
+        fn(h, ctypes.byref(r))
+        sys.stdout.write("%.6f %d %d %d\n" % (t, c.value, m.value, r.value))
+        sys.stdout.flush()
+    time.sleep(period)
+"""
+
+
 class ClockSampler:
     """Samples the SM clock and the clock-event (throttle) reasons of one GPU
-    every millisecond through NVML (read-only queries), in a thread.
-    mark() tags the samples taken from then on as the timed region."""
+    every millisecond through NVML (read-only queries), in a child process
+    of its own, so that the sampling takes no time from the thread that
+    launches the timed kernels.  mark() records, on the system-wide
+    monotonic clock, the instant from which samples belong to a region."""
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, device_index: int, period_s: float = 0.001):
-        import ctypes
-        import threading
         self.period = period_s
-        self.samples = []  # (tag, sm_mhz, max_mhz, reasons)
-        self.tag = "warmup"
-        self.stop_evt = threading.Event()
-        self.thread = None
-        self.nvml = None
-        self.h = ctypes.c_void_p()
+        self.device_index = device_index
+        self.marks = [("warmup", time.monotonic())]
+        self.samples = []  # (time, sm_mhz, max_mhz, reasons)
+        self.proc = None
+        self.key = str(device_index)
         try:
-            nv = ctypes.CDLL("libnvidia-ml.so.1")
-            if nv.nvmlInit_v2() != 0:
-                raise RuntimeError("nvmlInit failed")
-            ok = False
             props = torch.cuda.get_device_properties(device_index)
             uid = getattr(props, "uuid", None)
             if uid is not None:
-                key = str(uid)
-                key = key if key.startswith("GPU-") else "GPU-" + key
-                ok = nv.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(self.h)) == 0
-            if not ok and hasattr(props, "pci_bus_id"):
-                bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
-                                             getattr(props, "pci_device_id", 0))
-                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0
-            if not ok:
-                ok = nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.h)) == 0
-            if ok:
-                self.nvml = nv
+                self.key = str(uid) if str(uid).startswith("GPU-") else "GPU-" + str(uid)
+            elif hasattr(props, "pci_bus_id"):
+                self.key = "PCI:%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                                    getattr(props, "pci_device_id", 0))
         except Exception:
-            self.nvml = None
-
-    def _read(self):
-        import ctypes
-        c, m, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
-        nv = self.nvml
-        if nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) != 0:
-            return None
-        nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(m))
-        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        fn(self.h, ctypes.byref(r))
-        return c.value, m.value, r.value
-
-    def _run(self):
-        while not self.stop_evt.is_set():
-            s = self._read()
-            if s is not None:
-                self.samples.append((self.tag,) + s)
-            time.sleep(self.period)
+            pass
 
     def mark(self, tag):
-        self.tag = tag
+        self.marks.append((tag, time.monotonic()))
 
     def __enter__(self):
-        import threading
-        if self.nvml is not None:
-            self.thread = threading.Thread(target=self._run, daemon=True)
-            self.thread.start()
+        import subprocess
+        try:
+            self.proc = subprocess.Popen([sys.executable, "-c", _SAMPLER_CHILD, self.key, str(self.period),
+                                          str(self.device_index)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            if self.proc.stdout.readline().strip() != "ready":
+                self.proc.wait(timeout=5)
+                self.proc = None
+        except Exception:
+            self.proc = None
+        self.marks = [("warmup", time.monotonic())]
         return self
 
     def __exit__(self, *a):
-        if self.thread is not None:
-            self.stop_evt.set()
-            self.thread.join(timeout=2)
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            f = line.split()
+            if len(f) == 4:
+                self.samples.append((float(f[0]), int(f[1]), int(f[2]), int(f[3])))
+
+    def _tag(self, t):
+        tag = self.marks[0][0]
+        for name, t0 in self.marks:
+            if t >= t0:
+                tag = name
+        return tag
 
     def summary(self):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "source": "unavailable" if self.nvml is None else "nvml"}
-        timed = [s for s in self.samples if s[0] == "timed"]
+                    "source": "unavailable" if self.proc is None else "nvml"}
+        timed = [s for s in self.samples if self._tag(s[0]) == "timed"]
         use = timed if timed else self.samples
         reasons = set()
         for _, _, _, r in use:
@@ -224,7 +246,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(s[1] for s in use), "sm_max_mhz": max(s[2] for s in use),
                 "reasons": sorted(reasons), "samples": len(use),
                 "window": "timed region" if timed else "warm-up + timed region",
-                "source": "nvml, every %d ms" % round(self.period * 1000)}
+                "source": "nvml in a child process, every %d ms" % round(self.period * 1000)}
 
 
 def dist_setup(impl):

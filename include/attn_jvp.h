@@ -53,9 +53,14 @@
  *     launch nothing.  A device-side failure (a pipeline wait that ran out
  *     of time) is recorded in a per-device error word and reported by the
  *     next attn_sync_check on that device.
- *   - Supported head dims: Dqk, Dv in {16, 32, 64, 128} (16 and 32 run
+ *   - Supported head dims (forward, with and without tangents): Dqk, Dv
+ *     each in {16, 32, 64, 128, 256}, independently (16 and 32 run
  *     zero-padded to 64 inside the kernel); otherwise ATTN_ERR_UNSUPPORTED.
- *     Rows of every tensor are D elements, contiguous.
+ *     With tangents, Dv = 256 runs as two work units per query tile, one
+ *     per 128-column half of O and tO (O and tO of 256 columns each would
+ *     fill the tensor memory), each recomputing the scores; Dqk = 256 with
+ *     tangents keeps one key stage in shared memory beside Q and tQ.  Rows
+ *     of every tensor are D elements, contiguous.
  *   - The library allocates, on first use, one small per-device scratch
  *     buffer (error word) and, for jagged calls, one 1 MB work-list buffer
  *     per (device, stream); it keeps them until the process exits.  A
@@ -74,7 +79,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, causal with M != N (dense) */
-  ATTN_ERR_UNSUPPORTED = 2,   /* head dim outside {16, 32, 64, 128} */
+  ATTN_ERR_UNSUPPORTED = 2,   /* head dim outside the entry point's set, option not supported */
   ATTN_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
   ATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (no GPU, launch error) */
   ATTN_ERR_TIMEOUT = 5        /* a device pipeline wait ran out of time; outputs undefined */

@@ -53,8 +53,8 @@ int main(void) {
   attn_shape d96 = shape(128, 128, 96, 64);
   expect("head dim 96", attn_fwd_jvp(&d96, p, p, p, p, p, p, NULL, NULL, 0, nan_scale, p, p, l, NULL),
          ATTN_ERR_UNSUPPORTED);
-  attn_shape d256 = shape(128, 128, 256, 256);
-  expect("JVP at head dim 256", attn_fwd_jvp(&d256, p, p, p, p, p, p, NULL, NULL, 0, nan_scale, p, p, l, NULL),
+  attn_shape d512 = shape(128, 128, 512, 256);
+  expect("head dim 512", attn_fwd_jvp(&d512, p, p, p, p, p, p, NULL, NULL, 0, nan_scale, p, p, l, NULL),
          ATTN_ERR_UNSUPPORTED);
   attn_shape empty = shape(0, 128, 64, 64);
   expect("empty problem", attn_fwd(&empty, NULL, p, p, NULL, NULL, 0, nan_scale, NULL, NULL, NULL), ATTN_OK);

@@ -63,12 +63,13 @@ def test_rejects_null_shape(L):
 
 
 def test_rejects_unsupported_head_dims(L):
+    # the forward takes Dqk, Dv in {16, 32, 64, 128, 256}, with and without
+    # tangents; other widths are refused before anything is launched
     assert _call(L, _shape(Dqk=8)) == 2
-    assert _call(L, _shape(Dv=256)) == 2
     assert _call(L, _shape(Dqk=96)) == 2
     assert _call(L, _shape(Dv=48)) == 2
-    assert _call(L, _shape(Dqk=256, Dv=256)) == 2   # 256 only without tangents
-    assert _call(L, _shape(Dqk=256, Dv=128)) == 2
+    assert _call(L, _shape(Dqk=512, Dv=64)) == 2
+    assert _call(L, _shape(Dqk=64, Dv=320)) == 2
 
 
 def test_rejects_causal_cross_attention(L):

@@ -295,26 +295,72 @@ def test_outputs_16_byte_but_not_32_byte_aligned(Dv):
                  *oracle_dense(inp), what=f"16-byte aligned outputs Dv={Dv}")
 
 
-# ------------------------------------------------------ head dim 256 (forward)
-@pytest.mark.parametrize("name,kw", [
-    ("dense", dict(B=2, H=2, M=300, N=333, Dqk=256, Dv=256)),
-    ("causal", dict(B=1, H=3, M=400, N=400, Dqk=256, Dv=256, causal=True)),
-    ("bias", dict(B=2, H=2, M=200, N=260, Dqk=256, Dv=256, bias=True, mask_keep=200)),
-])
+# ----------------------------------------------------------- head dim 256
+# Dqk and Dv each in {16, 32, 64, 128, 256}, as the pages' kernels accept
+# them.  With tangents, Dv = 256 runs as two column slices of 128 (each its
+# own work unit); Dqk = 256 keeps Q and tQ (128 KB) resident with one K
+# stage, and reads a bias per thread.
+D256_JVP = [
+    ("256x256", dict(B=2, H=2, M=300, N=333, Dqk=256, Dv=256)),
+    ("256x256_causal", dict(B=1, H=3, M=400, N=400, Dqk=256, Dv=256, causal=True)),
+    ("256x256_bias_mask", dict(B=2, H=2, M=200, N=260, Dqk=256, Dv=256, bias=True, mask_keep=200)),
+    ("256x64", dict(B=2, H=2, M=260, N=300, Dqk=256, Dv=64)),
+    ("256x128_causal", dict(B=1, H=2, M=333, N=333, Dqk=256, Dv=128, causal=True)),
+    ("256x32_bias", dict(B=1, H=2, M=200, N=150, Dqk=256, Dv=32, bias=True)),
+    ("64x256", dict(B=2, H=2, M=200, N=333, Dqk=64, Dv=256)),
+    ("128x256_causal", dict(B=1, H=2, M=300, N=300, Dqk=128, Dv=256, causal=True)),
+    ("16x256_bias_mask", dict(B=1, H=2, M=130, N=200, Dqk=16, Dv=256, bias=True, mask_keep=150)),
+    ("128x256_many_units", dict(B=2, H=8, M=1024, N=1024, Dqk=128, Dv=256, causal=True)),
+]
+
+
+@pytest.mark.parametrize("name,kw", D256_JVP, ids=[c[0] for c in D256_JVP])
+def test_head_dim_256_jvp(name, kw):
+    inp = make_inputs(Workload("d256", input_std=0.5, tangent_std=0.5, **kw), seed=41)
+    assert_close(*run_gpu(inp, nan_prefill=True), *oracle_dense(inp), what=f"JVP {name}")
+
+
+D256_FWD = [
+    ("256x256", dict(B=2, H=2, M=300, N=333, Dqk=256, Dv=256)),
+    ("256x256_causal", dict(B=1, H=3, M=400, N=400, Dqk=256, Dv=256, causal=True)),
+    ("256x256_bias_mask", dict(B=2, H=2, M=200, N=260, Dqk=256, Dv=256, bias=True, mask_keep=200)),
+    ("256x64_bias", dict(B=2, H=2, M=260, N=300, Dqk=256, Dv=64, bias=True)),
+    ("256x128", dict(B=1, H=2, M=333, N=200, Dqk=256, Dv=128)),
+    ("64x256_causal", dict(B=1, H=2, M=300, N=300, Dqk=64, Dv=256, causal=True)),
+    ("128x256_bias_mask", dict(B=2, H=2, M=150, N=270, Dqk=128, Dv=256, bias=True, mask_keep=180)),
+]
+
+
+@pytest.mark.parametrize("name,kw", D256_FWD, ids=[c[0] for c in D256_FWD])
 def test_head_dim_256_forward(name, kw):
     inp = make_inputs(Workload("d256", input_std=0.5, **kw), seed=41)
-    O, L = run_gpu(inp, jvp=False)
+    O, L = run_gpu(inp, jvp=False, nan_prefill=True)
     Or, _, Lr = oracle_dense(inp)
     assert_close(O, np.zeros_like(O), L, Or, np.zeros_like(Or), Lr, what=f"D256 {name}")
 
 
-def test_head_dim_256_fp16_forward():
-    inp = make_inputs(Workload("d256h", B=1, H=2, M=260, N=300, Dqk=256, Dv=256, input_std=0.5), seed=42)
+def test_head_dim_256_fp16():
+    inp = make_inputs(Workload("d256h", B=1, H=2, M=260, N=300, Dqk=256, Dv=256, input_std=0.5,
+                               tangent_std=0.5), seed=42)
     for n in ("q", "k", "v", "tq", "tk", "tv"):
         inp[n] = inp[n].to(torch.float16)
-    O, L = run_gpu(inp, jvp=False)
-    Or, _, Lr = oracle_dense(inp)
-    assert_close(O, np.zeros_like(O), L, Or, np.zeros_like(Or), Lr, what="D256 fp16")
+    Or, tOr, Lr = oracle_dense(inp)
+    assert_close(*run_gpu(inp, nan_prefill=True), Or, tOr, Lr, what="D256 fp16 JVP")
+    O, L = run_gpu(inp, jvp=False, nan_prefill=True)
+    assert_close(O, np.zeros_like(O), L, Or, np.zeros_like(Or), Lr, what="D256 fp16 forward")
+
+
+@pytest.mark.parametrize("Dqk,Dv", [(256, 256), (64, 256), (256, 64)])
+def test_head_dim_256_jagged(Dqk, Dv):
+    lens = [1, 63, 64, 65, 200, 0, 129, 300]
+    w = Workload("j256", B=len(lens), H=2, Dqk=Dqk, Dv=Dv, jagged=True, max_seq_len=260,
+                 max_len_draw=1, input_std=0.5, tangent_std=0.5, sm_scale=0.1)
+    inp = make_inputs(w, seed=43, lengths=lens)
+    O, tO, L = run_gpu(inp, nan_prefill=True)
+    Or, tOr, Lr = oracle.attention_fwd_jvp_jagged(
+        inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"], inp["offsets"], 260,
+        sm_scale=0.1)
+    assert_close(O, tO, L, Or, tOr, Lr, what=f"jagged {Dqk}x{Dv}")
 
 
 # ------------------------------------------------------------- fp16 storage
