@@ -414,6 +414,21 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
     kp.unit_list = list;
     kp.unit_count = lbuf;
   }
+  // Dense with a key mask that does not depend on the query row: the key
+  // length of each (b, h) up to its last attended key, computed on the
+  // device (the mask lives there), so that trailing key tiles that every
+  // row masks are not visited.  (The allocation-free entry point, which has
+  // no buffer for it, visits every key tile.)
+  if (!jagged && kp.mask != nullptr && kp.mask_stride[2] == 0 && fixed == nullptr && s->N > 0 &&
+      static_cast<int64_t>(s->B) * s->H <= (kListOffsetBytes + attn::kPlanListBytes) / static_cast<int>(sizeof(int))) {
+    int* lbuf = nullptr;
+    const attn_status ls = stream_list(cs, &lbuf);
+    if (ls != ATTN_OK) return ls;
+    if (attn::launch_plan_keylen(kp.mask, kp.mask_stride, s->B, s->H, s->N, lbuf, cs) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1);
+    kp.keylen = lbuf;
+  }
   cudaError_t e = cudaErrorInvalidValue;
   // bias through the shared-memory ring when a tensor map describes it,
   // else per-thread loads; a mask alone also takes the ring mode

@@ -94,6 +94,11 @@ struct KernelParams {
   // u / H, head u % H.  A count of -1 means the list was not written.
   const int2* unit_list;
   const int* unit_count;
+  // Dense, with a key mask that does not depend on the query row (optional):
+  // keylen[b * H + h] = 1 + the last key any row of (b, h) attends; the
+  // units visit only the key tiles below it (a planning kernel earlier on
+  // the stream writes it).
+  const int* keylen;
   float scale_log2;  // sm_scale * log2(e)
   float sm_scale;
   const int* offsets;
@@ -280,7 +285,7 @@ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u, const 
     w.row0 = 0;
     w.mt = mt;
     w.q_len = p.M;
-    w.kv_len = p.N;
+    w.kv_len = p.keylen != nullptr ? min(p.N, __ldg(p.keylen + bh)) : p.N;
     w.out0 = static_cast<long long>(bh) * p.M;
   } else {
     int mt, b, h;

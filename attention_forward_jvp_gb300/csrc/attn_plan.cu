@@ -52,7 +52,37 @@ __global__ void __launch_bounds__(kPlanThreads) plan_jagged_kernel(const int* of
   }
 }
 
+// Key length of each (b, h) under a key mask that does not depend on the
+// query row: one block per (b, h) finds the last key j < N whose mask byte
+// is nonzero and writes j + 1 (0 when none).  Keys at or past it are masked
+// for every row, so the attention kernel need not visit them.
+__global__ void __launch_bounds__(256) plan_keylen_kernel(const unsigned char* mask, long long s0,
+                                                          long long s1, long long s3, int H, int N,
+                                                          int* keylen) {
+  const int bh = blockIdx.x;
+  const int b = bh / H, h = bh % H;
+  const unsigned char* row = mask + b * s0 + h * s1;
+  int last = -1;
+  for (int j = threadIdx.x; j < N; j += blockDim.x)
+    if (row[j * s3] != 0) last = j;
+  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  __shared__ int wmax[8];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int m = -1;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) m = max(m, wmax[w]);
+    keylen[bh] = m + 1;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_plan_keylen(const unsigned char* mask, const long long* stride, int B, int H, int N,
+                               int* keylen, cudaStream_t stream) {
+  plan_keylen_kernel<<<B * H, 256, 0, stream>>>(mask, stride[0], stride[1], stride[3], H, N, keylen);
+  return cudaGetLastError();
+}
 
 bool plan_jagged_supported(int max_seq_len) { return max_seq_len >= 0 && max_seq_len <= kPlanMaxSeqLen; }
 

@@ -267,6 +267,27 @@ def test_key_mask_with_dead_key_tiles(causal):
     assert_close(*run_gpu(inp), *oracle_dense(inp), what=f"dead key tiles (causal={causal})")
 
 
+@pytest.mark.parametrize("causal,bias", [(False, True), (True, True), (False, False)])
+def test_key_mask_trims_the_key_range(causal, bias):
+    """A key mask that does not depend on the query row ([B, H, 1, N]): a
+    planning kernel finds each (b, h)'s last kept key and the units stop
+    there.  Last kept key inside a tile and at a tile boundary, a (b, h)
+    with no kept key at all (empty rows), a hole before the last key."""
+    B, H, N = 3, 2, 64 * 9 + 13
+    M = N if causal else 200
+    w = Workload("kp", B=B, H=H, M=M, N=N, Dqk=128, Dv=64, bias=bias, causal=causal)
+    inp = make_inputs(w, seed=61)
+    mask = torch.ones((B, H, 1, N), dtype=torch.uint8)
+    mask[0, :, :, 300:] = 0
+    mask[1, 0] = 0
+    mask[1, 1, :, 64 * 5:] = 0
+    mask[2, :, :, 7] = 0
+    inp["mask"] = mask
+    O, tO, L = run_gpu(inp, nan_prefill=True)
+    assert_close(O, tO, L, *oracle_dense(inp), what=f"trimmed keys causal={causal} bias={bias}")
+    assert np.isneginf(L[1, 0]).all() and (O[1, 0] == 0).all() and (tO[1, 0] == 0).all()
+
+
 def test_mask_without_bias():
     w = Workload("mo", B=2, H=2, M=190, N=300, Dqk=128, Dv=64)
     inp = make_inputs(w, seed=15)
