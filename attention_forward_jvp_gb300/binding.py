@@ -298,18 +298,20 @@ BWD_DELTA, BWD_DQ, BWD_DKDV, BWD_ALL = 1, 2, 4, 7
 
 def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float] = None,
              offsets: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
+             bias: Optional[torch.Tensor] = None, mask: Optional[torch.Tensor] = None,
              out=None, stages: int = BWD_ALL):
-    """Attention backward (no bias / mask).  Takes the forward's
-    inputs, its output ``o`` and log-sum-exp ``lse`` and the gradient ``do``
-    of O; returns (dq, dk, dv, delta), delta = rowsum(do o o) in float32.
-    Dense ``[B, H, M|N, D]`` or jagged ``[H, T, D]`` with int32 ``offsets``
-    and ``max_seq_len`` (tokens past a sequence's cap get zero gradients).
+    """Attention backward.  Takes the forward's inputs (with its ``bias`` /
+    ``mask``, dense only; the bias gets no gradient), its output ``o`` and
+    log-sum-exp ``lse`` and the gradient ``do`` of O; returns
+    (dq, dk, dv, delta), delta = rowsum(do o o) in float32.  Dense
+    ``[B, H, M|N, D]`` or jagged ``[H, T, D]`` with int32 ``offsets`` and
+    ``max_seq_len`` (tokens past a sequence's cap get zero gradients).
     ``stages`` (an OR of BWD_DELTA, BWD_DQ, BWD_DKDV) runs a subset of the
     launches; the others leave their outputs as given."""
     if q.device.type == "cpu":
         return _host_call(attn_bwd, (q, k, v, o, lse, do),
                           dict(causal=causal, sm_scale=sm_scale, offsets=offsets,
-                               max_seq_len=max_seq_len), n_out=4)
+                               max_seq_len=max_seq_len, bias=bias, mask=mask), n_out=4)
     dev = q.device
     dt = _elem_type(q)
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
@@ -317,7 +319,7 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float
     _need(lse, "lse", torch.float32, dev)
     if offsets is not None:
         _need(offsets, "offsets", torch.int32, dev)
-    sh, _, out_shape, _ = _describe(q, k, v, offsets, max_seq_len, None, None)
+    sh, bs, out_shape, keep = _describe(q, k, v, offsets, max_seq_len, bias, mask)
     if tuple(o.shape) != out_shape or tuple(do.shape) != out_shape or tuple(lse.shape) != out_shape[:-1]:
         raise ValueError("o and do must be shaped like the forward's output and lse like its log-sum-exp")
     if out is None:
@@ -333,13 +335,15 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, sm_scale: Optional[float
     if stages == BWD_ALL:
         fn = lib().attn_bwd_f16 if dt == torch.float16 else lib().attn_bwd
         st = fn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(offsets),
-                None, 1 if causal else 0, _scale(sm_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
-                ctypes.c_void_p(stream))
+                ctypes.byref(bs) if bs is not None else None, 1 if causal else 0, _scale(sm_scale),
+                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta), ctypes.c_void_p(stream))
     else:
         st = lib().attn_bwd_stages(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do),
-                                   _ptr(lse), _ptr(offsets), None, 1 if causal else 0, _scale(sm_scale),
+                                   _ptr(lse), _ptr(offsets), ctypes.byref(bs) if bs is not None else None,
+                                   1 if causal else 0, _scale(sm_scale),
                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
                                    1 if dt == torch.float16 else 0, int(stages), ctypes.c_void_p(stream))
+    del keep
     _check(st)
     return dq, dk, dv, delta
 

@@ -1,5 +1,7 @@
 // Attention backward for sm_103a: gradients dQ, dK, dV of a loss through
-// O = softmax(s Q K^T) V, given dO and the forward's log-sum-exp.
+// O = softmax(s Q K^T + bias) V (keys outside the valid set -- causal, key
+// mask -- at -inf), given dO and the forward's log-sum-exp.  The bias gets
+// no gradient.
 //
 // Method (the Triton fused-attention tutorial's backward, "_attn_bwd_dkdv"
 // and "_attn_bwd_dq"; "flash_attention.py" "_attn_bwd_dkdv_inner" /
@@ -56,6 +58,12 @@ struct BwdParams {
   uint16_t* out2;      // KV pass: dV
   int d_qk;            // row width of q, k, dq, dk (Dqk; 16 / 32 run padded to 64)
   int d_v;             // row width of v, o, do, dv
+  // dense only, both optional: fp32 additive bias and uint8 mask (nonzero =
+  // attend) over [B, H, M, N], element strides, 0 = broadcast
+  const float* bias;
+  long long bias_stride[4];
+  const unsigned char* mask;
+  long long mask_stride[4];
   int* err;
   unsigned long long timeout_ns;
 };
@@ -114,6 +122,7 @@ struct BwdUnit {
   int row0;         // tensor-map row of position 0 (jagged: the sequence's first token)
   long long orow0;  // output row of position 0 of this pass's rows
   long long qrow0;  // LSE / Delta index of query 0
+  int b, h;         // batch entry and head (dense)
 };
 
 // Unit u, costliest first: dense causal dQ units by descending query tile,
@@ -153,6 +162,8 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
   }
   w.rows = KV ? k_len : q_len;
   w.cols = KV ? q_len : k_len;
+  w.b = p.jagged ? 0 : w.z / p.H;
+  w.h = p.jagged ? w.z : w.z % p.H;
   const bool active = w.rt * kBM < w.rows;
   if (!KV) {
     int hi = k_len;
@@ -447,6 +458,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       if (!KV) neg_terms(ri, nl_r, nd_r);
       else neg_terms((w.t0) * 64 + half * 32 + lane, nl_c, nd_c);
       const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
+      const bool has_bias = p.bias != nullptr, has_mask = p.mask != nullptr;
+      // this thread's row of the bias / mask: a query row (dQ pass, keys
+      // along it) or a key column (KV pass, queries along it)
+      const float* bbase = nullptr;
+      const unsigned char* mbase = nullptr;
+      long long bstep = 0, mstep = 0;  // element step along the streamed dimension
+      if (has_bias) {
+        bbase = p.bias + w.b * p.bias_stride[0] + w.h * p.bias_stride[1] +
+                static_cast<long long>(ri) * p.bias_stride[KV ? 3 : 2];
+        bstep = p.bias_stride[KV ? 2 : 3];
+      }
+      if (has_mask) {
+        mbase = p.mask + w.b * p.mask_stride[0] + w.h * p.mask_stride[1] +
+                static_cast<long long>(ri) * p.mask_stride[KV ? 3 : 2];
+        mstep = p.mask_stride[KV ? 2 : 3];
+      }
       for (int j = 0; j < w.nt; ++j, ++g, ++tuse) {
         const uint32_t sb = g % P::NSB;
         const int col0 = (w.t0 + j) * 64 + half * 32;  // first column (key or query) of this thread
@@ -465,7 +492,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         int lo = 0, hi = 32;
         if (!KV) hi = (p.causal ? min(w.cols, ri + 1) : w.cols) - col0;
         else if (p.causal) lo = ri - col0;
-        const bool full = lo <= 0 && hi >= 32;
+        // keep bit c: column col0 + c in [lo, hi) and, with a mask, attended
+        uint32_t keep = 0xffffffffu;
+        if (lo > 0) keep = lo >= 32 ? 0u : keep << lo;
+        if (hi < 32) keep &= hi <= 0 ? 0u : (1u << hi) - 1u;
+        // bias values of this thread's 32 columns (log2 units; 0 past the
+        // valid columns), loaded before the scores are waited for
+        float bl[32];
+        if (has_bias) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) bl[c] = 0.f;
+          if (row_ok) {
+            const float* bp = bbase + static_cast<long long>(col0) * bstep;
+            if (bstep == 1 && (reinterpret_cast<uintptr_t>(bp) & 15u) == 0 && col0 + 32 <= w.cols) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const float4 t4 = __ldg(reinterpret_cast<const float4*>(bp) + c);
+                bl[4 * c] = t4.x * kLog2eF;
+                bl[4 * c + 1] = t4.y * kLog2eF;
+                bl[4 * c + 2] = t4.z * kLog2eF;
+                bl[4 * c + 3] = t4.w * kLog2eF;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (col0 + c < w.cols) bl[c] = __ldg(bp + c * bstep) * kLog2eF;
+            }
+          }
+        }
+        if (has_mask && row_ok) {
+          const unsigned char* mp = mbase + static_cast<long long>(col0) * mstep;
+          uint32_t mb = 0u;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (col0 + c < w.cols && __ldg(mp + c * mstep) != 0) mb |= 1u << c;
+          keep &= mb;
+        }
+        const bool full = keep == 0xffffffffu;
         // a sleeping wait: a spinning one would take issue slots from the
         // MMA issuer on the same sub-partition
         ok = __all_sync(0xffffffffu, wait_bar_sleep(bar(P::B_SF + sb), (g / P::NSB) & 1u, W));
@@ -493,14 +556,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             const float nla = e == 0 ? nl4.x : nl4.z, nlb = e == 0 ? nl4.y : nl4.w;
             const float nda = e == 0 ? nd4.x : nd4.z, ndb = e == 0 ? nd4.y : nd4.w;
             // x = S s log2(e) - LSE log2(e);  P = 2^x;  dS = P (dP - Delta)
-            const uint64_t x = f2_fma(f2_make(__uint_as_float(xr[cc]), __uint_as_float(xr[cc + 1])), sc2,
-                                      f2_make(nla, nlb));
+            uint64_t x = f2_fma(f2_make(__uint_as_float(xr[cc]), __uint_as_float(xr[cc + 1])), sc2,
+                                f2_make(nla, nlb));
+            if (has_bias) x = f2_add(x, f2_make(bl[cc], bl[cc + 1]));
             float x0, x1;
             f2_split(x, x0, x1);
             float p0 = ex2(x0), p1 = ex2(x1);
             if (!full) {
-              p0 = (cc >= lo && cc < hi) ? p0 : 0.f;
-              p1 = (cc + 1 >= lo && cc + 1 < hi) ? p1 : 0.f;
+              p0 = ((keep >> cc) & 1u) ? p0 : 0.f;
+              p1 = ((keep >> (cc + 1)) & 1u) ? p1 : 0.f;
             }
             const uint64_t d = f2_add(f2_make(__uint_as_float(yr[cc]), __uint_as_float(yr[cc + 1])),
                                       f2_make(nda, ndb));

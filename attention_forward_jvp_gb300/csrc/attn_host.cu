@@ -561,7 +561,8 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
   if (s->B < 0 || s->H < 0 || s->Dqk < 0 || s->Dv < 0) return ATTN_ERR_INVALID_ARG;
   if (!jagged && (s->M < 0 || s->N < 0)) return ATTN_ERR_INVALID_ARG;
   if (jagged && (s->T < 0 || s->T > 0x7fffffffLL || s->max_seq_len < 0)) return ATTN_ERR_INVALID_ARG;
-  if (bias != nullptr && (bias->bias != nullptr || bias->mask != nullptr)) return ATTN_ERR_UNSUPPORTED;
+  const bool has_bias = bias != nullptr && (bias->bias != nullptr || bias->mask != nullptr);
+  if (has_bias && jagged) return ATTN_ERR_UNSUPPORTED;  // bias / mask are dense-only
   auto dim_ok = [](int d) { return d == 16 || d == 32 || d == 64 || d == 128; };
   if (!dim_ok(s->Dqk) || !dim_ok(s->Dv)) return ATTN_ERR_UNSUPPORTED;
   if (!std::isnan(sm_scale) && !(sm_scale > 0.f && std::isfinite(sm_scale)))
@@ -583,6 +584,8 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     if (rows_q && !aligned16(p)) return ATTN_ERR_MISALIGNED;
   for (const void* p : {k, v, static_cast<const void*>(dk), static_cast<const void*>(dv)})
     if (rows_k && !aligned16(p)) return ATTN_ERR_MISALIGNED;
+  if (has_bias && bias->bias != nullptr && (reinterpret_cast<uintptr_t>(bias->bias) & 3u) != 0)
+    return ATTN_ERR_MISALIGNED;
 
   DeviceState* ds = nullptr;
   attn_status st = device_state(&ds);
@@ -644,6 +647,14 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     bp.out2 = static_cast<uint16_t*>(kv ? dv : nullptr);
     bp.d_qk = s->Dqk;
     bp.d_v = s->Dv;
+    if (has_bias) {
+      bp.bias = bias->bias;
+      bp.mask = bias->mask;
+      for (int i = 0; i < 4; ++i) {
+        bp.bias_stride[i] = bias->bias_stride[i];
+        bp.mask_stride[i] = bias->mask_stride[i];
+      }
+    }
     bp.err = ds->scratch;
     bp.timeout_ns = g_timeout_ns.load();
     // the streamed side has no rows: its maps are never used, only valid

@@ -197,9 +197,9 @@ attn_status attn_fwd_jvp_noalloc(const attn_shape* shape,
                                  int causal, float sm_scale,
                                  void* o, void* to, float* lse, void* stream);
 
-/* Backward of softmax attention: given the forward's inputs q, k, v, its
- * output o and log-sum-exp lse (as attn_fwd writes them) and the gradient
- * dout = dL/dO of a loss L, writes
+/* Backward of softmax attention: given the forward's inputs q, k, v (and
+ * its bias / mask), its output o and log-sum-exp lse (as attn_fwd writes
+ * them) and the gradient dout = dL/dO of a loss L, writes
  *
  *   Delta = rowsum(dout o O)             delta [B, H, M] fp32
  *   dV    = P^T dout                     dv    [B, H, N, Dv]
@@ -207,16 +207,17 @@ attn_status attn_fwd_jvp_noalloc(const attn_shape* shape,
  *   dQ    = sm_scale dS K                dq    [B, H, M, Dqk]
  *   dK    = sm_scale dS^T Q              dk    [B, H, N, Dqk]
  *
- * with P = exp(sm_scale Q K^T - LSE) over the valid set (0 elsewhere and
- * on rows with LSE = -inf).  Sources: the Triton fused-attention tutorial's
+ * with P = exp(sm_scale Q K^T + bias - LSE) over the valid set (0 elsewhere
+ * and on rows with LSE = -inf); the bias gets no gradient.  Sources: the Triton fused-attention tutorial's
  * backward (_attn_bwd_preprocess for Delta, _attn_bwd_dkdv and _attn_bwd_dq
  * recomputing P from the stored log-sum-exp); "flash_attention.py"
  * (triton_flashattn) _attn_bwd_dkdv_inner / _attn_bwd_dq_inner.
  *
- * This version: no bias or mask (bias must be NULL or hold two NULL
- * pointers) and Dqk, Dv in {16, 32, 64, 128} (16 and 32 zero-padded to 64
- * inside; unequal dims as in "flash_attention.py"); otherwise
- * ATTN_ERR_UNSUPPORTED.  Dense (offsets NULL; causal requires M == N) or
+ * bias: as in attn_fwd (the same pointers and strides the forward was
+ * given; dense only, ATTN_ERR_UNSUPPORTED with offsets; ATTN_ERR_MISALIGNED
+ * for a bias not 4-byte aligned).  Dqk, Dv in {16, 32, 64, 128} (16 and 32
+ * zero-padded to 64 inside; unequal dims as in "flash_attention.py");
+ * otherwise ATTN_ERR_UNSUPPORTED.  Dense (offsets NULL; causal requires M == N) or
  * jagged (offsets != NULL, the FBGEMM jagged backward's layout:
  * q, k, v, o, dout, dq, dk, dv [H, T, D], lse and delta [H, T]); a jagged
  * token past its sequence's min(length, max_seq_len) gets dq = dk = dv = 0,

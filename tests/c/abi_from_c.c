@@ -59,11 +59,15 @@ int main(void) {
   attn_shape empty = shape(0, 128, 64, 64);
   expect("empty problem", attn_fwd(&empty, NULL, p, p, NULL, NULL, 0, nan_scale, NULL, NULL, NULL), ATTN_OK);
 
-  /* a bias with the backward is not supported */
+  /* a bias with jagged inputs is not supported (dense only) */
   attn_bias b;
   memset(&b, 0, sizeof b);
   b.bias = (const float*)p;
-  expect("backward with a bias", attn_bwd(&s, p, p, p, p, p, l, NULL, &b, 0, nan_scale, p, p, p, l, NULL),
+  attn_shape jag = shape(0, 0, 64, 64);
+  jag.T = 64;
+  jag.max_seq_len = 64;
+  expect("jagged backward with a bias",
+         attn_bwd(&jag, p, p, p, p, p, l, (const int32_t*)p, &b, 0, nan_scale, p, p, p, l, NULL),
          ATTN_ERR_UNSUPPORTED);
   expect("backward stages outside the flags",
          attn_bwd_stages(&s, p, p, p, p, p, l, NULL, NULL, 0, nan_scale, p, p, p, l, 0, 8u, NULL),

@@ -144,7 +144,10 @@ def test_bwd_validation(L):
     assert _bwd(L, _shape(T=0, msl=64), offsets=off) == 0           # no tokens: no-op
     b = binding.AttnBias()
     b.mask = 0x10000
-    assert _bwd(L, _shape(), bias=ctypes.byref(b)) == 2  # mask / bias
+    # a bias / mask with jagged inputs (dense only, as in the forward)
+    assert _bwd(L, _shape(T=100, msl=64), offsets=off, bias=ctypes.byref(b)) == 2
+    b.bias = 0x10002  # a bias not 4-byte aligned
+    assert _bwd(L, _shape(), bias=ctypes.byref(b)) == 3
     assert _bwd(L, _shape(M=128, N=256), causal=1) == 1
     assert _bwd(L, _shape(), scale=-1.0) == 1
     assert _bwd(L, _shape(M=-3)) == 1

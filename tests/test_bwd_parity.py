@@ -38,6 +38,9 @@ def run_gpu_bwd(inp, f16=False):
     cast = (lambda t: t.float().half()) if f16 else (lambda t: t)
     q, k, v, do = (cast(inp[n]).cuda() for n in ("q", "k", "v", "do"))
     kw = dict(causal=inp["causal"], sm_scale=inp["sm_scale"])
+    for n in ("bias", "mask"):
+        if inp.get(n) is not None:
+            kw[n] = inp[n].cuda()
     o, lse = binding.attn_fwd(q, k, v, **kw)
     dq, dk, dv, delta = binding.attn_bwd(q, k, v, o, lse, do, **kw)
     assert binding.sync_check() == 0
@@ -47,7 +50,8 @@ def run_gpu_bwd(inp, f16=False):
 def oracle_bwd(inp, f16=False):
     cast = (lambda t: t.float().half()) if f16 else (lambda t: t)
     return oracle.attention_bwd(*(cast(inp[n]) for n in ("q", "k", "v", "do")),
-                                causal=inp["causal"], sm_scale=inp["sm_scale"])
+                                causal=inp["causal"], sm_scale=inp["sm_scale"],
+                                bias=inp.get("bias"), mask=inp.get("mask"))
 
 
 def assert_grads_close(got, ref, what=""):
@@ -191,3 +195,49 @@ def test_bwd_jagged(causal, D):
         if L > 256:
             for g in got[:3]:
                 assert np.all(g[:, offs[b] + 256:offs[b + 1]] == 0)
+
+
+# ------------------------------------------------------ bias / mask backward
+# The same bias and mask go to the forward and the backward (the pages'
+# bias backward, "flash_attention.py" _attn_bwd_dkdv_inner /
+# _attn_bwd_dq_inner, without the bias gradient).
+def _bias_mask(B, H, M, N, kind, seed):
+    g = torch.Generator().manual_seed(seed)
+    bias = mask = None
+    if "bias" in kind:
+        bias = torch.randn((B, H, M, N), generator=g)
+    if "rowmask" in kind:
+        mask = (torch.rand((B, 1, M, N), generator=g) < 0.7).to(torch.uint8)
+        mask[0, 0, 3, :] = 0  # a fully masked row: LSE = -inf, no gradient through it
+    if "keymask" in kind:
+        mask = torch.ones((B, 1, 1, N), dtype=torch.uint8)
+        mask[..., N - N // 4:] = 0
+        mask[-1, ..., 5] = 0
+    if "headbias" in kind:
+        bias = torch.randn((1, H, 1, N), generator=g)  # broadcast over batch and rows
+    return bias, mask
+
+
+BIAS_CASES = [
+    ("bias", dict(M=256, N=320, Dqk=64, Dv=64), "bias"),
+    ("bias_rowmask", dict(M=200, N=333, Dqk=128, Dv=64), "bias+rowmask"),
+    ("causal_bias_keymask", dict(M=384, N=384, Dqk=128, Dv=128, causal=True), "bias+keymask"),
+    ("keymask_only", dict(M=260, N=300, Dqk=64, Dv=128), "keymask"),
+    ("headbias_broadcast", dict(M=190, N=257, Dqk=32, Dv=64), "headbias"),
+]
+
+
+@pytest.mark.parametrize("name,shape,kind", BIAS_CASES, ids=[c[0] for c in BIAS_CASES])
+def test_bwd_with_bias_and_mask(name, shape, kind):
+    w = _w(B=2, **shape)
+    inp = make_bwd_inputs(w, seed=71)
+    inp["bias"], inp["mask"] = _bias_mask(2, w.H, w.M, w.N, kind, seed=72)
+    assert_grads_close(run_gpu_bwd(inp), oracle_bwd(inp), what=name)
+
+
+def test_bwd_with_bias_fp16():
+    w = _w(B=1, M=200, N=264, Dqk=64, Dv=64)
+    inp = make_bwd_inputs(w, seed=73)
+    inp["bias"], inp["mask"] = _bias_mask(1, w.H, w.M, w.N, "bias+rowmask", seed=74)
+    assert_grads_close(run_gpu_bwd(inp, f16=True), oracle_bwd(inp, f16=True), what="fp16 bias")
+
