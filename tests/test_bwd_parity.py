@@ -133,19 +133,25 @@ def test_bwd_unsupported_configs():
     assert e.value.status == 2  # Dv = 256
 
 
-def test_bwd_full_size_sampled_heads():
-    # the benchmark's shape (B2 H16 N4096 D128 causal); two heads checked
-    # whole against the oracle, and at every head the identity
-    # sum_j dK_j = 0 (adding one vector to every key leaves each row's
-    # softmax unchanged)
-    w = WORKLOADS["causal"]
+@pytest.mark.parametrize("name", ["causal", "noncausal"])
+def test_bwd_full_size_whole_output(name):
+    # the benchmark's backward shapes (B2 H16 N4096 D128 causal, B4 H16 N1024
+    # D64 non-causal), outputs prefilled with NaN so that a unit the
+    # persistent schedule skipped would show; every head whole against the
+    # oracle, and at every head the identity sum_j dK_j = 0 (adding one
+    # vector to every key leaves each row's softmax unchanged)
+    w = WORKLOADS[name]
     inp = make_bwd_inputs(w, seed=0)
-    dq, dk, dv, delta = run_gpu_bwd(inp)
-    s = inp["sm_scale"]
-    for b, h in ((0, 0), (1, 15)):
-        r = oracle.head_bwd(*(inp[n][b, h].double().numpy() for n in ("q", "k", "v", "do")), s,
-                            causal=True)
-        assert_grads_close((dq[b, h], dk[b, h], dv[b, h], delta[b, h]), r, what=f"head {b},{h}")
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    kw = dict(causal=inp["causal"], sm_scale=inp["sm_scale"])
+    o, lse = binding.attn_fwd(q, k, v, **kw)
+    out = tuple(torch.full_like(t, float("nan")) for t in (q, k, v, lse))
+    binding.attn_bwd(q, k, v, o, lse, do, out=out, **kw)
+    assert binding.sync_check() == 0
+    dq, dk, dv, delta = (t.float().cpu().numpy() for t in out)
+    for t in (dq, dk, dv, delta):
+        assert not np.isnan(t).any(), f"{name}: unwritten gradient rows"
+    assert_grads_close((dq, dk, dv, delta), oracle_bwd(inp), what=name)
     col = np.abs(dk.astype(np.float64).sum(axis=2))
     scale = np.abs(dk).max()
     assert col.max() <= 2e-2 * max(1.0, scale) * 8, f"sum_j dK_j = {col.max():.3e}"
