@@ -188,6 +188,12 @@ struct Plan {
                             : (FIXED + NK * K_STAGE + 3 * V_STAGE <= RING) ? 3
                             : (FIXED + NK * K_STAGE + 2 * V_STAGE <= RING) ? 2
                                                                            : 1;
+  // One K stage only (Dqk = 256 with tangents): it is kept as CH chunk
+  // stages of 64 columns ([K | tK] of one chunk each), released one by one
+  // as the score MMAs that read them finish, so that the next tile's chunks
+  // load while the rest of this tile's score chain runs.
+  static constexpr bool KCH = JVP && NK == 1 && CH > 1;
+  static constexpr int NKB = KCH ? CH : NK;  // K full / empty barrier pairs
   static constexpr int OFF_Q = 0;       // buffer b at OFF_Q + b * QSET
   static constexpr int OFF_TQ = Q_TILE;  // buffer b at OFF_TQ + b * QSET
   static constexpr int OFF_K = FIXED;
@@ -212,8 +218,8 @@ struct Plan {
   // tensor memory holds them.
   static constexpr int NOB = (NQB == 2 && COL_O + 2 * OBUF <= 512) ? 2 : 1;
   static_assert(!PP || (NQB == 2 && NOB == 2), "ping-pong softmax: two Q and two O buffers");
-  static constexpr int B_QF = 0, B_QE = B_QF + NQB, B_KF = B_QE + NQB, B_KE = B_KF + NK,
-                       B_VF = B_KE + NK, B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2,
+  static constexpr int B_QF = 0, B_QE = B_QF + NQB, B_KF = B_QE + NQB, B_KE = B_KF + NKB,
+                       B_VF = B_KE + NKB, B_VE = B_VF + NV, B_SF = B_VE + NV, B_PF = B_SF + 2,
                        B_DRAIN = B_PF + 2, B_PAIR = B_DRAIN + 1, B_BF = B_PAIR + 4,
                        B_BE = B_BF + NB, B_OE = B_BE + NB, NBAR = B_OE + NOB;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
@@ -533,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bar(P::B_QE + i), 1);
     }
     for (int i = 0; i < P::NOB; ++i) mbar_init(bar(P::B_OE + i), 8);  // one arrival per softmax warp
-    for (int i = 0; i < P::NK; ++i) {
+    for (int i = 0; i < P::NKB; ++i) {
       mbar_init(bar(P::B_KF + i), 1);
       mbar_init(bar(P::B_KE + i), 1);
     }
@@ -593,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t qfill = 0, kfill = 0;
+      int kpart = 0;  // chunk stages issued for tile kfill (chunked K only)
       const bool first_q_loaded = p.skip_first_load == 0;
       bool skip = !first_q_loaded;
       bool ok = true;
@@ -620,6 +627,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ++qfill;
         for (int j = 0; j < w.nt; ++j) {
           const int r = w.row0 + j * kBN;
+          if constexpr (P::KCH) {
+            // chunk stages: chunk c of this tile once the score MMAs of the
+            // previous tile that read chunk c are done
+            kpart = 0;
+#pragma unroll 1
+            for (int c = 0; c < P::CH && ok; ++c) {
+              ok = wait_bar(bar(P::B_KE + c), (kfill & 1u) ^ 1u, W);
+              if (!ok) break;
+              mbar_arrive_expect_tx(bar(P::B_KF + c), P::K_GROUP);
+              const uint32_t kdst = sbase + P::OFF_K + c * P::K_GROUP;
+              tma_load_3d(kdst, &p.tm_k, bar(P::B_KF + c), c * 64, r, w.z);
+              if constexpr (JVP) tma_load_3d(kdst + P::K_SUB, &p.tm_tk, bar(P::B_KF + c), c * 64, r, w.z);
+              kpart = c + 1;
+            }
+            if (!ok) break;
+            kpart = 0;
+          } else {
           const uint32_t ks = kfill % P::NK;
           ok = wait_bar(bar(P::B_KE + ks), ((kfill / P::NK) & 1u) ^ 1u, W);
           if (!ok) break;
@@ -632,13 +656,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               tma_load_3d(kdst + c * P::K_GROUP + P::K_SUB, &p.tm_tk, bar(P::B_KF + ks), c * 64, r,
                           w.z);
           }
+          }
           ++kfill;
         }
       }
       // Teardown: every issued copy must have landed before the CTA exits.
-      for (uint32_t s = 0; s < P::NK && s < kfill; ++s) {
-        const uint32_t nf = (kfill - s + P::NK - 1) / P::NK;
-        drain_bar(bar(P::B_KF + s), (nf - 1) & 1u, p.timeout_ns);
+      if constexpr (P::KCH) {
+        // chunks of an interrupted tile (the first kpart) were filled for
+        // tile kfill; the others last for tile kfill - 1
+        for (int c = 0; c < P::CH; ++c) {
+          if (c < kpart) drain_bar(bar(P::B_KF + c), kfill & 1u, p.timeout_ns);
+          else if (kfill > 0) drain_bar(bar(P::B_KF + c), (kfill - 1) & 1u, p.timeout_ns);
+        }
+      } else {
+        for (uint32_t s = 0; s < P::NK && s < kfill; ++s) {
+          const uint32_t nf = (kfill - s + P::NK - 1) / P::NK;
+          drain_bar(bar(P::B_KF + s), (nf - 1) & 1u, p.timeout_ns);
+        }
       }
       // (a skipped first load leaves its buffer's barrier incomplete)
       for (uint32_t s = 0; s < static_cast<uint32_t>(P::NQB) && s < qfill; ++s) {
@@ -739,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ok = __all_sync(0xffffffffu, wait_bar_sleep(bar(P::B_SF + (g & 1u)), (g >> 1) & 1u, W));
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive(bar(P::B_KE + g % P::NK));
+          if constexpr (!P::KCH) mbar_arrive(bar(P::B_KE + g % P::NK));
           if (j == w.nt - 1) mbar_arrive(bar(P::B_QE + qu % P::NQB));
           mbar_arrive(bar(P::B_PF + (g & 1u)));
         }
@@ -776,7 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // copy never holds back the rest of the current batch.
     uint32_t k_seen = 0xffffffffu, v_seen = 0xffffffffu;
     auto poll_k = [&](uint32_t t) {
-      if (__all_sync(0xffffffffu, mbar_try_wait(bar(P::B_KF + t % P::NK), (t / P::NK) & 1u))) k_seen = t;
+      if constexpr (!P::KCH)
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar(P::B_KF + t % P::NK), (t / P::NK) & 1u))) k_seen = t;
     };
     auto poll_v = [&](uint32_t t) {
       if (__all_sync(0xffffffffu, mbar_try_wait(bar(P::B_VF + t % P::NV), (t / P::NV) & 1u))) v_seen = t;
@@ -804,9 +839,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // [S | Q tK^T] = Q [K ; tK]^T, tS += tQ K^T for tile t; `mid` runs after
     // the first half of the first chain.
     auto issue_s = [&](uint32_t t, uint32_t qb, auto&& mid) -> bool {
-      if (!wait_k(t)) return false;
       const uint32_t lq = lo_q + qb * (P::QSET >> 4);
       const uint32_t dS = tmem + (t & 1u) * P::SBUF;
+      if constexpr (P::KCH) {
+        // per 64-column chunk c: its four [S | Q tK^T] K steps, then its
+        // four tQ K^T steps (accumulating onto the Q tK^T columns the first
+        // step initialised), then a commit that frees chunk stage c
+#pragma unroll 1
+        for (int c = 0; c < P::CH; ++c) {
+          if (!wait_all(bar(P::B_KF + c), t & 1u)) return false;
+          const uint32_t lk = lo_k + ((c * P::K_GROUP) >> 4);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const uint32_t oq = (c * P::Q_SUB + k4 * 32) >> 4;
+            if (leader)
+              mma_ss(dS, sdesc_join(lq + oq, kHi), sdesc_join(lk + ((k4 * 32) >> 4), kHi), idesc_s,
+                     (c > 0 || k4 > 0) ? 1u : 0u);
+            __syncwarp();
+          }
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const uint32_t oq = (P::OFF_TQ - P::OFF_Q + c * P::Q_SUB + k4 * 32) >> 4;
+            if (leader) mma_ss(dS + kBN, sdesc_join(lq + oq, kHi), sdesc_join(lk + ((k4 * 32) >> 4), kHi), idesc_t, 1u);
+            __syncwarp();
+          }
+          if (leader) tc_commit(bar(P::B_KE + c));
+          __syncwarp();
+          if (c == P::CH / 2 - 1) mid();
+        }
+        if (leader) tc_commit(bar(P::B_SF + (t & 1u)));
+        __syncwarp();
+        return true;
+      }
+      if (!wait_k(t)) return false;
       const uint32_t lk = lo_k + (t % P::NK) * (P::K_STAGE >> 4);
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {

@@ -507,8 +507,14 @@ def test_default_scale_is_inverse_sqrt_dqk():
 
 
 # ----------------------------------------------------- failure detection
-def test_timed_out_wait_is_reported_and_context_survives():
-    inp = make_inputs(WORKLOADS["tiny"])
+@pytest.mark.parametrize("shape", ["tiny", "d256"])
+def test_timed_out_wait_is_reported_and_context_survives(shape):
+    # d256: head dim 256 with tangents, whose K copies use chunk stages
+    if shape == "tiny":
+        inp = make_inputs(WORKLOADS["tiny"])
+    else:
+        inp = make_inputs(Workload("t256", B=1, H=2, M=300, N=400, Dqk=256, Dv=256, input_std=0.5,
+                                   tangent_std=0.5), seed=44)
     q, k, v, tq, tk, tv = (dev(inp[n]) for n in ("q", "k", "v", "tq", "tk", "tv"))
     binding.set_wait_timeout_ns(100_000_000)
     binding.debug_skip_first_load(True)
