@@ -178,7 +178,9 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
   return w;
 }
 
-template <int DQK, int DV, bool KV, bool F16>
+// BM: the launch has a bias and / or a mask (their loads and terms are
+// compiled only into those instantiations).
+template <int DQK, int DV, bool KV, bool F16, bool BM>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using P = BwdPlan<DQK, DV, KV>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       if (!KV) neg_terms(ri, nl_r, nd_r);
       else neg_terms((w.t0) * 64 + half * 32 + lane, nl_c, nd_c);
       const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
-      const bool has_bias = p.bias != nullptr, has_mask = p.mask != nullptr;
+      const bool has_bias = BM && p.bias != nullptr, has_mask = BM && p.mask != nullptr;
       // this thread's row of the bias / mask: a query row (dQ pass, keys
       // along it) or a key column (KV pass, queries along it)
       const float* bbase = nullptr;
@@ -498,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         if (hi < 32) keep &= hi <= 0 ? 0u : (1u << hi) - 1u;
         // bias values of this thread's 32 columns (log2 units; 0 past the
         // valid columns), loaded before the scores are waited for
-        float bl[32];
+        float bl[BM ? 32 : 1];
+        if constexpr (BM) {
         if (has_bias) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) bl[c] = 0.f;
@@ -519,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 if (col0 + c < w.cols) bl[c] = __ldg(bp + c * bstep) * kLog2eF;
             }
           }
+        }
         }
         if (has_mask && row_ok) {
           const unsigned char* mp = mbase + static_cast<long long>(col0) * mstep;
@@ -558,7 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             // x = S s log2(e) - LSE log2(e);  P = 2^x;  dS = P (dP - Delta)
             uint64_t x = f2_fma(f2_make(__uint_as_float(xr[cc]), __uint_as_float(xr[cc + 1])), sc2,
                                 f2_make(nla, nlb));
-            if (has_bias) x = f2_add(x, f2_make(bl[cc], bl[cc + 1]));
+            if constexpr (BM) {
+              if (has_bias) x = f2_add(x, f2_make(bl[cc], bl[cc + 1]));
+            }
             float x0, x1;
             f2_split(x, x0, x1);
             float p0 = ex2(x0), p1 = ex2(x1);
@@ -640,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, P::TMEM_COLS);
 }
 
-template <int DQK, int DV, bool KV, bool F16>
+template <int DQK, int DV, bool KV, bool F16, bool BM>
 cudaError_t launch_attn_bwd(const BwdParams& bp, int grid, cudaStream_t stream) {
   using P = BwdPlan<DQK, DV, KV>;
   static bool attr_done[64] = {};
@@ -649,15 +655,15 @@ cudaError_t launch_attn_bwd(const BwdParams& bp, int grid, cudaStream_t stream) 
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_done[dev]) {
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<DQK, DV, KV, F16>);
+    e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<DQK, DV, KV, F16, BM>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_bwd_kernel<DQK, DV, KV, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_bwd_kernel<DQK, DV, KV, F16, BM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              P::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  attn_bwd_kernel<DQK, DV, KV, F16><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(bp);
+  attn_bwd_kernel<DQK, DV, KV, F16, BM><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(bp);
   return cudaGetLastError();
 }
 

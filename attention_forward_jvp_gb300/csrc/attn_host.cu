@@ -50,22 +50,38 @@ ATTN_FWD_DECL_ALL(128, 256, false)
 ATTN_FWD_DECL_ALL(256, 256, false)
 extern template cudaError_t launch_attn<64, 64, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<128, 128, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, 64, false, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, 64, false, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, 64, true, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, 64, true, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, 128, false, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, 128, false, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, 128, true, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<64, 128, true, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, 64, false, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, 64, false, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, 64, true, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, 64, true, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, 128, false, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, 128, false, true>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, 128, true, false>(const BwdParams&, int, cudaStream_t);
-extern template cudaError_t launch_attn_bwd<128, 128, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, false, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, false, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, false, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, false, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, true, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, true, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, true, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 64, true, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, false, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, false, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, false, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, false, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, true, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, true, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, true, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<64, 128, true, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, false, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, false, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, false, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, false, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, true, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, true, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, true, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 64, true, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, false, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, false, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, false, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, false, true, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, true, false, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, true, false, true>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, true, true, false>(const BwdParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn_bwd<128, 128, true, true, true>(const BwdParams&, int, cudaStream_t);
 }
 
 namespace {
@@ -535,20 +551,27 @@ __global__ void attn_bwd_zero_tail_kernel(const int* offsets, int H, long long T
 
 // One pass of the dQ kernel (kv = false) or of the dK / dV kernel; key
 // bit 1 for Dqk = 128, bit 0 for Dv = 128 (else 64).
-template <bool KV, bool F16>
+template <bool KV, bool F16, bool BM>
 cudaError_t dispatch_bwd_dims(int key, const attn::BwdParams& bp, int grid, cudaStream_t cs) {
   switch (key) {
-    case 0: return attn::launch_attn_bwd<64, 64, KV, F16>(bp, grid, cs);
-    case 1: return attn::launch_attn_bwd<64, 128, KV, F16>(bp, grid, cs);
-    case 2: return attn::launch_attn_bwd<128, 64, KV, F16>(bp, grid, cs);
-    case 3: return attn::launch_attn_bwd<128, 128, KV, F16>(bp, grid, cs);
+    case 0: return attn::launch_attn_bwd<64, 64, KV, F16, BM>(bp, grid, cs);
+    case 1: return attn::launch_attn_bwd<64, 128, KV, F16, BM>(bp, grid, cs);
+    case 2: return attn::launch_attn_bwd<128, 64, KV, F16, BM>(bp, grid, cs);
+    case 3: return attn::launch_attn_bwd<128, 128, KV, F16, BM>(bp, grid, cs);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t dispatch_bwd(int key, bool kv, bool f16, const attn::BwdParams& bp, int grid, cudaStream_t cs) {
-  if (f16) return kv ? dispatch_bwd_dims<true, true>(key, bp, grid, cs) : dispatch_bwd_dims<false, true>(key, bp, grid, cs);
-  return kv ? dispatch_bwd_dims<true, false>(key, bp, grid, cs) : dispatch_bwd_dims<false, false>(key, bp, grid, cs);
+template <bool BM>
+cudaError_t dispatch_bwd_bm(int key, bool kv, bool f16, const attn::BwdParams& bp, int grid, cudaStream_t cs) {
+  if (f16)
+    return kv ? dispatch_bwd_dims<true, true, BM>(key, bp, grid, cs) : dispatch_bwd_dims<false, true, BM>(key, bp, grid, cs);
+  return kv ? dispatch_bwd_dims<true, false, BM>(key, bp, grid, cs) : dispatch_bwd_dims<false, false, BM>(key, bp, grid, cs);
+}
+
+// bm: the launch has a bias and / or a mask
+cudaError_t dispatch_bwd(int key, bool kv, bool f16, bool bm, const attn::BwdParams& bp, int grid, cudaStream_t cs) {
+  return bm ? dispatch_bwd_bm<true>(key, kv, f16, bp, grid, cs) : dispatch_bwd_bm<false>(key, kv, f16, bp, grid, cs);
 }
 
 attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const void* v, const void* o,
@@ -675,7 +698,7 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     bp.num_units = static_cast<int>(units);
     const int grid = static_cast<int>(units < ds->num_sms ? units : ds->num_sms);
-    if (dispatch_bwd(key, kv, f16, bp, grid, cs) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dispatch_bwd(key, kv, f16, has_bias, bp, grid, cs) != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1);
   }
   return ATTN_OK;
