@@ -383,7 +383,7 @@ def attn_fwd_f8(q, k, vt, causal: bool = False, sm_scale: Optional[float] = None
 _STREAMS = {}
 
 
-def _chunk_streams(dev, n=3):
+def _chunk_streams(dev, n=4):
     """Streams of the chunked host path (per device, created once)."""
     key = dev.index
     if key not in _STREAMS:
@@ -393,9 +393,11 @@ def _chunk_streams(dev, n=3):
 
 def _slab_chunks(fn, tensors, kw) -> int:
     """How many chunks of whole (batch, head) slabs the host path of a dense
-    forward call is cut into: 4 when there are at least 8 slabs, every
-    tensor is contiguous and every chunk boundary keeps the 16-byte
-    alignment of the lse rows (M a multiple of 4); else 1."""
+    forward call is cut into: with at least 8 slabs, every tensor contiguous
+    and every chunk boundary keeping the 16-byte alignment of the lse rows
+    (M a multiple of 4), 4 when the inputs are 128 MB or more and 2 below
+    (each chunk costs host time to issue; on a GB300 the copies of a step
+    this small finish sooner in two chunks); else 1."""
     if fn not in (attn_fwd_jvp, attn_fwd):
         return 1
     if any(kw.get(k) is not None for k in ("offsets", "bias", "mask")):
@@ -406,7 +408,8 @@ def _slab_chunks(fn, tensors, kw) -> int:
         return 1
     if q.shape[0] * q.shape[1] < 8 or q.shape[2] % 4 != 0:
         return 1
-    return 4
+    nbytes = sum(t.numel() * t.element_size() for t in tensors)
+    return 4 if nbytes >= (128 << 20) else 2
 
 
 def _host_call(fn, tensors, kw, n_out):
@@ -414,9 +417,11 @@ def _host_call(fn, tensors, kw, n_out):
 
     A dense forward without bias or mask is cut into chunks of whole
     (batch, head) slabs, each an independent problem computed by its own
-    call; a chunk's input copies, kernel and output copies run in order on
-    one of three streams, so the copies of one chunk overlap the kernel of
-    another.  The results are those of one call over the whole batch."""
+    call of the C entry point (the whole problem is validated once, then
+    each chunk passes its slab pointers); a chunk's input copies, kernel and
+    output copies run in order on a stream of its own, so the copies of one
+    chunk overlap the kernel of another.  The results are those of one call
+    over the whole batch."""
     dev = torch.device("cuda", torch.cuda.current_device())
     n = _slab_chunks(fn, tensors, kw)
     if n == 1:
@@ -443,6 +448,22 @@ def _host_call(fn, tensors, kw, n_out):
     def slab(t, a, b):  # slabs [a, b) of a [B, H, ...] tensor, as [1, b - a, ...]
         return t.view(S, *t.shape[2:])[a:b].view(1, b - a, *t.shape[2:])
 
+    # the whole problem through the binding's checks once (shapes, dtypes,
+    # devices), with no launch: the chunks below skip them
+    jvp = fn is attn_fwd_jvp
+    f16 = _elem_type(q) == torch.float16
+    for name, t in zip(("q", "k", "v", "tq", "tk", "tv"), d_in):
+        _need(t, name, q.dtype, dev)
+    if jvp and (tensors[3].shape != q.shape or tensors[4].shape != tensors[1].shape
+                or tensors[5].shape != v.shape):
+        raise ValueError("tangents must have the primals' shapes")
+    sh, _, _, _ = _describe(d_in[0], d_in[1], d_in[2], None, None, None, None)
+    L = lib()
+    cfn = (L.attn_fwd_jvp_f16 if f16 else L.attn_fwd_jvp) if jvp else (L.attn_fwd_f16 if f16 else L.attn_fwd)
+    scale = _scale(kw.get("sm_scale"))
+    causal = 1 if kw.get("causal") else 0
+    per_in = [t.numel() // S * t.element_size() for t in d_in]      # bytes per slab
+    per_out = [t.numel() // S * t.element_size() for t in d_out]
     cur = torch.cuda.current_stream(dev)
     streams = _chunk_streams(dev)
     for st in streams:
@@ -450,13 +471,17 @@ def _host_call(fn, tensors, kw, n_out):
     try:
         for c in range(n):
             a, b = S * c // n, S * (c + 1) // n
-            with torch.cuda.stream(streams[c % len(streams)]):
-                ins = []
+            st = streams[c % len(streams)]
+            with torch.cuda.stream(st):
                 for h, d in zip(tensors, d_in):
-                    dc = slab(d, a, b)
-                    dc.copy_(slab(h, a, b), non_blocking=True)
-                    ins.append(dc)
-                fn(*ins, out=tuple(slab(o, a, b) for o in d_out), **kw)
+                    slab(d, a, b).copy_(slab(h, a, b), non_blocking=True)
+                csh = AttnShape()
+                csh.B, csh.H, csh.M, csh.N, csh.Dqk, csh.Dv = 1, b - a, sh.M, sh.N, sh.Dqk, sh.Dv
+                pin = [ctypes.c_void_p(d.data_ptr() + a * pb) for d, pb in zip(d_in, per_in)]
+                pout = [ctypes.c_void_p(o.data_ptr() + a * pb) for o, pb in zip(d_out, per_out)]
+                # (q, k, v[, tq, tk, tv], offsets, bias, causal, scale, o[, to], lse, stream)
+                _check(cfn(ctypes.byref(csh), *pin, None, None, causal, scale, *pout,
+                           ctypes.c_void_p(st.cuda_stream)))
                 for ho, o in zip(h_out, d_out):
                     slab(ho, a, b).copy_(slab(o, a, b), non_blocking=True)
     finally:

@@ -54,13 +54,16 @@ def test_backward_sources_do_not_change_the_forward_hash(tmp_path, monkeypatch):
 def test_host_path_chunking_decision():
     """Which host calls the binding cuts into (batch, head) slab chunks: a
     dense forward without bias, mask or offsets, contiguous, at least 8
-    slabs and M a multiple of 4 (lse rows of a chunk stay 16-byte aligned)."""
+    slabs and M a multiple of 4 (lse rows of a chunk stay 16-byte aligned);
+    four chunks from 128 MB of inputs, else two."""
     import torch
     from attention_forward_jvp_gb300 import binding
     t = torch.zeros(2, 8, 200, 64, dtype=torch.bfloat16)
     six, three = (t,) * 6, (t,) * 3
-    assert binding._slab_chunks(binding.attn_fwd_jvp, six, {}) == 4
-    assert binding._slab_chunks(binding.attn_fwd, three, {"bias": None, "mask": None}) == 4
+    assert binding._slab_chunks(binding.attn_fwd_jvp, six, {}) == 2
+    assert binding._slab_chunks(binding.attn_fwd, three, {"bias": None, "mask": None}) == 2
+    big = torch.empty(2, 16, 4096, 128, dtype=torch.bfloat16)   # 32 MB each, 192 MB for six
+    assert binding._slab_chunks(binding.attn_fwd_jvp, (big,) * 6, {}) == 4
     assert binding._slab_chunks(binding.attn_fwd, three, {"bias": t}) == 1
     assert binding._slab_chunks(binding.attn_fwd, three, {"mask": t}) == 1
     assert binding._slab_chunks(binding.attn_fwd, three, {"offsets": t}) == 1
