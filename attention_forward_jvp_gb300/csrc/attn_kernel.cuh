@@ -95,9 +95,11 @@ struct KernelParams {
   const int2* unit_list;
   const int* unit_count;
   // Dense, with a key mask that does not depend on the query row (optional):
-  // keylen[b * H + h] = 1 + the last key any row of (b, h) attends; the
-  // units visit only the key tiles below it (a planning kernel earlier on
-  // the stream writes it).
+  // bits 0-30 of keylen[b * H + h] = 1 + the last key any row of (b, h)
+  // attends, bit 31 set when every key below it is attended (the mask is
+  // then a key prefix, and the key length alone masks the rest); the units
+  // visit only the key tiles below it (a planning kernel earlier on the
+  // stream writes it).
   const int* keylen;
   float scale_log2;  // sm_scale * log2(e)
   float sm_scale;
@@ -255,6 +257,7 @@ struct Unit {
   int b, h;
   long long out0;   // row index of query 0 in the [.., rows] output view
   int vh;           // output column slice: columns [vh * DV, vh * DV + DV)
+  bool mask_on;     // the key mask has to be read (false: a key prefix, in kv_len)
   bool active;
 };
 
@@ -269,6 +272,7 @@ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u, const 
   // the column slices of one query tile are adjacent units (they share Q, K
   // and V tiles through L2)
   w.vh = 0;
+  w.mask_on = true;
   if constexpr (SLICES) {
     if (p.n_vh > 1) {
       w.vh = u % p.n_vh;
@@ -291,7 +295,12 @@ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u, const 
     w.row0 = 0;
     w.mt = mt;
     w.q_len = p.M;
-    w.kv_len = p.keylen != nullptr ? min(p.N, __ldg(p.keylen + bh)) : p.N;
+    w.kv_len = p.N;
+    if (p.keylen != nullptr) {
+      const int kl = __ldg(p.keylen + bh);
+      w.kv_len = min(p.N, kl & 0x7fffffff);
+      w.mask_on = kl >= 0;
+    }
     w.out0 = static_cast<long long>(bh) * p.M;
   } else {
     int mt, b, h;
@@ -1494,7 +1503,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (has_bias)
           brow = p.bias + w.b * p.bias_stride[0] + w.h * p.bias_stride[1] +
                  static_cast<long long>(qi) * p.bias_stride[2];
-        if (has_mask)
+        // a mask that is a key prefix of this (b, h) is already in kv_len
+        const bool umask = has_mask && w.mask_on;
+        if (umask)
           mrow = p.mask + w.b * p.mask_stride[0] + w.h * p.mask_stride[1] +
                  static_cast<long long>(qi) * p.mask_stride[2];
 
@@ -1543,7 +1554,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               }
             }
           }
-          if (has_mask) {
+          if (umask) {
             load_mask32(mrow, key0, w.kv_len, p.mask_stride[3], row_ok, mv);
             if (RING) load_mask32(mrow, j * kBN + (half ^ 1) * kHalf, w.kv_len, p.mask_stride[3], row_ok, mvo);
           }
@@ -1601,7 +1612,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const int keyo = j * kBN + (half ^ 1) * kHalf;
             uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
             uint32_t kmo = keep_bits(keyo, w.kv_len, qi, p.causal);
-            if (has_mask) {
+            if (umask) {
               // Most tiles of a key-padding or block mask are wholly kept or
               // wholly masked: only mixed mask bytes need the bit gather.
               uint32_t any_set = 0u, any_zero = 0u;
@@ -1704,7 +1715,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               mx = fmaxf(rowmax32(x), rowmax32(xo));
             } else {
               uint32_t km = keep_bits(key0, w.kv_len, qi, p.causal);
-              if (has_mask) km &= mask_bits32(mv);
+              if (umask) km &= mask_bits32(mv);
 #pragma unroll
               for (int c = 0; c < kHalf; ++c) {
                 float v = x[c] * p.scale_log2;

@@ -54,25 +54,40 @@ __global__ void __launch_bounds__(kPlanThreads) plan_jagged_kernel(const int* of
 
 // Key length of each (b, h) under a key mask that does not depend on the
 // query row: one block per (b, h) finds the last key j < N whose mask byte
-// is nonzero and writes j + 1 (0 when none).  Keys at or past it are masked
-// for every row, so the attention kernel need not visit them.
+// is nonzero and the first key whose byte is zero, and writes j + 1 (0 when
+// none), with bit 31 set when no key below j + 1 is masked (the mask is a
+// key prefix).  Keys at or past j + 1 are masked for every row, so the
+// attention kernel need not visit them; under a prefix it need not read
+// the mask at all.
 __global__ void __launch_bounds__(256) plan_keylen_kernel(const unsigned char* mask, long long s0,
                                                           long long s1, long long s3, int H, int N,
                                                           int* keylen) {
   const int bh = blockIdx.x;
   const int b = bh / H, h = bh % H;
   const unsigned char* row = mask + b * s0 + h * s1;
-  int last = -1;
-  for (int j = threadIdx.x; j < N; j += blockDim.x)
+  int last = -1, first_zero = N;
+  for (int j = threadIdx.x; j < N; j += blockDim.x) {
     if (row[j * s3] != 0) last = j;
-  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-  __shared__ int wmax[8];
-  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = last;
+    else first_zero = min(first_zero, j);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    first_zero = min(first_zero, __shfl_xor_sync(0xffffffffu, first_zero, o));
+  }
+  __shared__ int wmax[8], wmin[8];
+  if ((threadIdx.x & 31) == 0) {
+    wmax[threadIdx.x >> 5] = last;
+    wmin[threadIdx.x >> 5] = first_zero;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int m = -1;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) m = max(m, wmax[w]);
-    keylen[bh] = m + 1;
+    int m = -1, z = N;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+      m = max(m, wmax[w]);
+      z = min(z, wmin[w]);
+    }
+    const bool prefix = z > m;  // keys 0 .. m all attended
+    keylen[bh] = (m + 1) | (prefix ? static_cast<int>(0x80000000u) : 0);
   }
 }
 

@@ -18,9 +18,10 @@ cudaError_t launch_plan_jagged(const int* offsets, int B, int max_seq_len, int c
                                int* count, int capacity, cudaStream_t stream);
 
 // Writes keylen[b * H + h] = 1 + the last key j < N with mask[b, h, ., j]
-// nonzero (0 when none), for a [B, H, 1, N] view of a key mask that does not
-// depend on the query row (element strides stride[0], stride[1], stride[3]).
-// One block per (b, h), asynchronous on `stream`.
+// nonzero (0 when none), bit 31 set when every key below it is nonzero, for
+// a [B, H, 1, N] view of a key mask that does not depend on the query row
+// (element strides stride[0], stride[1], stride[3]).  One block per (b, h),
+// asynchronous on `stream`.
 cudaError_t launch_plan_keylen(const unsigned char* mask, const long long* stride, int B, int H, int N,
                                int* keylen, cudaStream_t stream);
 
