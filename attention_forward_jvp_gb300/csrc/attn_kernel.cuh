@@ -1562,6 +1562,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (g >> 1) & 1u, W));
           if (!ok) break;
           tc_fence_after();
+          if constexpr (RING) {
+            if (has_bias) {
+              // this tile's bias stage, waited for before the score loads so
+              // that the wait overlaps them (the stage is waited on even when
+              // unused, so that its next fill cannot start before this one
+              // has landed)
+              constexpr int NBR = P::NB > 0 ? P::NB : 1;
+              ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_BF + g % NBR), (g / NBR) & 1u, W));
+              if (!ok) break;
+            }
+          }
           // Each warp also reads the partner half's 32 score columns and takes
           // the row maximum over all 64 itself, so the two warps of a quadrant
           // never wait for each other: unmasked tiles (`fast`) and masked tiles
@@ -1633,12 +1644,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             // selects) or none kept (no arithmetic; P = H = 0)
             const bool all_keep = __all_sync(0xffffffffu, (km & kmo) == 0xffffffffu);
             dead = __all_sync(0xffffffffu, (km | kmo) == 0u);
-            if (has_bias) {
-              // the stage is waited on even when unused, so that its next
-              // fill cannot start before this one has landed
-              ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_BF + g % NBR), (g / NBR) & 1u, W));
-              if (!ok) break;
-            }
             const uint8_t* bbase = smem + P::OFF_BIAS + (g % NBR) * P::BIAS_STAGE + row * 128;
             float xo[kHalf];
             if (dead) {
