@@ -4,6 +4,8 @@
 // share (longest-processing-time-first).  One block, counting sort by cost.
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
 #include "attn_plan.h"
 
 namespace attn {
@@ -66,9 +68,33 @@ __global__ void __launch_bounds__(256) plan_keylen_kernel(const unsigned char* m
   const int b = bh / H, h = bh % H;
   const unsigned char* row = mask + b * s0 + h * s1;
   int last = -1, first_zero = N;
-  for (int j = threadIdx.x; j < N; j += blockDim.x) {
-    if (row[j * s3] != 0) last = j;
-    else first_zero = min(first_zero, j);
+  if (s3 == 1 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+    // 16 keys per load: a key row of up to 4096 bytes in one pass
+    for (int j0 = threadIdx.x * 16; j0 < N; j0 += blockDim.x * 16) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (j0 + 16 <= N) {
+        v = __ldg(reinterpret_cast<const uint4*>(row + j0));
+      } else {
+        unsigned char t[16] = {};
+        for (int c = 0; j0 + c < N; ++c) t[c] = row[j0 + c];
+        v = make_uint4(t[0] | t[1] << 8 | t[2] << 16 | static_cast<uint32_t>(t[3]) << 24,
+                       t[4] | t[5] << 8 | t[6] << 16 | static_cast<uint32_t>(t[7]) << 24,
+                       t[8] | t[9] << 8 | t[10] << 16 | static_cast<uint32_t>(t[11]) << 24,
+                       t[12] | t[13] << 8 | t[14] << 16 | static_cast<uint32_t>(t[15]) << 24);
+      }
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        if (j0 + c >= N) break;
+        if ((w[c >> 2] >> ((c & 3) * 8)) & 0xffu) last = j0 + c;
+        else first_zero = min(first_zero, j0 + c);
+      }
+    }
+  } else {
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+      if (row[j * s3] != 0) last = j;
+      else first_zero = min(first_zero, j);
+    }
   }
   for (int o = 16; o > 0; o >>= 1) {
     last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
