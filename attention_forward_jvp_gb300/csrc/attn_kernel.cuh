@@ -1305,30 +1305,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         return true;
       };
+      // One walk over units and this warp's tiles, flattened so that the
+      // merge has a single call site (its code is large; one inlined copy
+      // keeps the loop's instruction footprint small): each step takes the
+      // next unit when the last one is done, then this warp's next tile of
+      // it, then the previous unit's merge if one is pending (after the
+      // first tile of the next unit, or at once when this parity has no
+      // tile in it or no unit is left).
       Epi ppend{};
       bool has_ppend = false;
-      for (int rnd = 0; ok; ++rnd) {
-        const int u = unit_of_round(rnd);
-        if (u >= num_units) break;
-        const Unit w = decode_unit<kSlices>(p, u, list);
-        if (!w.active) continue;
-        const int qi = w.mt * kBM + row;
-        const bool row_ok = qi < w.q_len;
-        if (w.nt == 0) {  // no keys at all: empty rows (this warp: columns [par DVH, ...))
-          const int ncol = min(DVH, p.dv_out - par * DVH);
-          if (row_ok && ncol > 0) {
-            uint32_t z[DVH / 2];
+      Unit w{};
+      int rnd = 0, j = 0, qi = 0;
+      bool have = false, fresh = true;
+      float m_run = -INFINITY;
+      uint64_t l2 = 0, lt2 = 0, r2 = 0;
+      for (;;) {
+        if (fresh) {
+          // the next unit with keys; units without keys get empty rows
+          fresh = false;
+          have = false;
+          for (;;) {
+            const int u = unit_of_round(rnd);
+            if (u >= num_units) break;
+            ++rnd;
+            w = decode_unit<kSlices>(p, u, list);
+            if (!w.active) continue;
+            qi = w.mt * kBM + row;
+            const bool row_ok = qi < w.q_len;
+            if (w.nt == 0) {  // no keys at all: empty rows (this warp: columns [par DVH, ...))
+              const int ncol = min(DVH, p.dv_out - par * DVH);
+              if (row_ok && ncol > 0) {
+                uint32_t z[DVH / 2];
 #pragma unroll
-            for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
-            store_row_bf16(p.o + (w.out0 + qi) * p.dv_out + par * DVH, z, ncol / 2);
-            if (JVP) store_row_bf16(p.to + (w.out0 + qi) * p.dv_out + par * DVH, z, ncol / 2);
+                for (int i = 0; i < DVH / 2; ++i) z[i] = 0u;
+                store_row_bf16(p.o + (w.out0 + qi) * p.dv_out + par * DVH, z, ncol / 2);
+                if (JVP) store_row_bf16(p.to + (w.out0 + qi) * p.dv_out + par * DVH, z, ncol / 2);
+              }
+              if (row_ok && par == 0) p.lse[w.out0 + qi] = -INFINITY;
+              continue;
+            }
+            have = true;
+            j = (par ^ static_cast<int>(g)) & 1;
+            m_run = -INFINITY;
+            l2 = lt2 = r2 = 0;
+            break;
           }
-          if (row_ok && par == 0) p.lse[w.out0 + qi] = -INFINITY;
-          continue;
         }
-        float m_run = -INFINITY;
-        uint64_t l2 = 0, lt2 = 0, r2 = 0;
-        for (int j = (par ^ static_cast<int>(g)) & 1; j < w.nt; j += 2) {
+        if (have && j < w.nt) {
           const uint32_t gt = g + static_cast<uint32_t>(j);
           const uint32_t sb = gt & 1u;
           ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (gt >> 1) & 1u, W));
@@ -1445,24 +1468,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(P::B_PF + sb));
-          if (has_ppend) {
-            has_ppend = false;
-            ok = pp_merge(ppend);
-            if (!ok) break;
-          }
+          j += 2;
         }
-        if (!ok) break;
-        if (has_ppend) {  // this parity had no tile in this unit
+        if (has_ppend) {
           has_ppend = false;
           ok = pp_merge(ppend);
           if (!ok) break;
         }
-        ppend = Epi{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g + static_cast<uint32_t>(w.nt), un, 0};
-        has_ppend = true;
-        g += static_cast<uint32_t>(w.nt);
-        ++un;
+        if (!have) break;
+        if (j >= w.nt) {
+          ppend = Epi{w.mt, w.q_len, w.out0, m_run, l2, lt2, r2, g + static_cast<uint32_t>(w.nt), un, 0};
+          has_ppend = true;
+          g += static_cast<uint32_t>(w.nt);
+          ++un;
+          fresh = true;
+        }
       }
-      if (ok && has_ppend) ok = pp_merge(ppend);
     } else {
       uint32_t un = 0;         // units with keys seen so far
       Epi pend{};              // with two O buffers: the unit whose epilogue is due
