@@ -987,22 +987,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (w.nt == 0) continue;
         ok = wait_all(bar(P::B_QF), quse & 1u);
         if (!ok) break;
-        for (int j = 0; j < w.nt; ++j, ++g) {
-          ok = issue_s(g, 0, [&]() {
-            if (j > 0) poll_v(g - 1);
-            if (j == w.nt - 1) poll_v(g);
-            else if (j == 0) poll_k(g + 1);
-          });
-          if (!ok) break;
+        // step j: S(t0 + j) (j < nt), then PV(t0 + j - 1) (j > 0): one call
+        // site per batch kind keeps the issue loop's code small
+        for (int j = 0; j <= w.nt; ++j) {
+          if (j < w.nt) {
+            ok = issue_s(g, 0, [&]() {
+              if (j > 0) poll_v(g - 1);
+              if (j == w.nt - 1) poll_v(g);
+              else if (j == 0) poll_k(g + 1);
+            });
+            if (!ok) break;
+            ++g;
+          }
           if (j > 0) {
-            ok = issue_pv(g - 1, j - 1, quse, [&]() {
-              if (j + 1 < w.nt) poll_k(g + 1);
+            ok = issue_pv(g - 1 - (j < w.nt ? 1u : 0u), j - 1, quse, [&]() {
+              if (j + 1 < w.nt) poll_k(g);
             });
             if (!ok) break;
           }
         }
         if (!ok) break;
-        ok = issue_pv(g - 1, w.nt - 1, quse, []() {});
         ++quse;
       }
     } else {
