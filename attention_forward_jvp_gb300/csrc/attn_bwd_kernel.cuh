@@ -326,22 +326,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             tc_fence_after();
             const uint32_t lt = lo_t + ts * (P::T_STAGE >> 4);
             const uint32_t dX = tmem + sb * P::SBUF;
-#pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
-              const uint32_t ob = ((kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
-              if (leader) mma_ss(dX, sdesc_join(lo_r1 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
-              __syncwarp();
-            }
-#pragma unroll
-            for (int kk = 0; kk < DV / 16; ++kk) {
-              const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
-              const uint32_t ob = (P::T1_TILE + (kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
-              if (leader)
-                mma_ss(dX + P::TN, sdesc_join(lo_r2 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
-              __syncwarp();
-            }
+            // both chains from the elected lane in one pass (the rest of the
+            // warp waits at the commit's warp sync)
             if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < DQK / 16; ++kk) {
+                const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
+                const uint32_t ob = ((kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
+                mma_ss(dX, sdesc_join(lo_r1 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
+              }
+#pragma unroll
+              for (int kk = 0; kk < DV / 16; ++kk) {
+                const uint32_t oa = ((kk >> 2) * P::R_SUB + (kk & 3) * 32) >> 4;
+                const uint32_t ob = (P::T1_TILE + (kk >> 2) * P::T_SUB + (kk & 3) * 32) >> 4;
+                mma_ss(dX + P::TN, sdesc_join(lo_r2 + oa, kHi), sdesc_join(lt + ob, kHi), idesc_s, kk > 0 ? 1u : 0u);
+              }
               tc_commit(bar(P::B_SF + sb));
               // the unit's last score chain: the row operands are free once
               // it is done (the output chains never read them)
@@ -372,29 +371,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             // P^T (KV pass) at +0 and dS at +16 (KV) / +0 (dQ pass), 8
             // packed columns per 16 streamed rows
             const uint32_t aY = tmem + sb * P::SBUF + P::TN;
-            if (KV) {
-              // dV += P^T dO
-#pragma unroll
-              for (int kk = 0; kk < P::TN / 16; ++kk) {
-                const uint64_t db = sdesc_join(lm + ((P::T1_TILE + kk * 2048) >> 4), kHi);
-                if (leader)
-                  mma_ts(tmem + P::COL_A, aY + 32 * (kk >> 1) + 8 * (kk & 1), db, idesc_v,
-                         (first && kk == 0) ? 0u : 1u);
-                __syncwarp();
-              }
-            }
             // dQ += dS K   /   dK += dS^T Q
             const uint32_t acc = tmem + P::COL_A + (KV ? DV : 0);
             const uint32_t ds_off = KV ? 16u : 0u;
+            if (leader) {
+              if (KV) {
+                // dV += P^T dO
 #pragma unroll
-            for (int kk = 0; kk < P::TN / 16; ++kk) {
-              const uint64_t db = sdesc_join(lm + ((kk * 2048) >> 4), kHi);
-              if (leader)
+                for (int kk = 0; kk < P::TN / 16; ++kk) {
+                  const uint64_t db = sdesc_join(lm + ((P::T1_TILE + kk * 2048) >> 4), kHi);
+                  mma_ts(tmem + P::COL_A, aY + 32 * (kk >> 1) + 8 * (kk & 1), db, idesc_v,
+                         (first && kk == 0) ? 0u : 1u);
+                }
+              }
+#pragma unroll
+              for (int kk = 0; kk < P::TN / 16; ++kk) {
+                const uint64_t db = sdesc_join(lm + ((kk * 2048) >> 4), kHi);
                 mma_ts(acc, aY + 32 * (kk >> 1) + ds_off + 8 * (kk & 1), db, idesc_k,
                        (first && kk == 0) ? 0u : 1u);
-              __syncwarp();
-            }
-            if (leader) {
+              }
               tc_commit(bar(P::B_TE + ts));  // stage free (the tile's score chains finished first)
               tc_commit(bar(P::B_OD + sb));  // score buffer free
             }
