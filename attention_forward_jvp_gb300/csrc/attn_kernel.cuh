@@ -528,10 +528,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Launched as a programmatic dependent, this kernel may start while the
+  // kernel before it on the stream (a planning kernel, or the previous
+  // call) is still running: the prologue below touches only shared and
+  // tensor memory and the kernel parameters, and every thread waits for
+  // the kernels before it to complete before the first global access.
+  griddep_launch_dependents();
   // 128-byte swizzled operands need 1024-byte aligned tiles; the dynamic
   // shared window starts aligned, and a launch where it does not reports
   // an error instead of computing.
   if ((smem_u32(smem) & 1023u) != 0) {
+    griddep_wait();
     if (threadIdx.x == 0) atomicCAS(p.err, 0, ERR_SMEM_ALIGN);
     return;
   }
@@ -585,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), P::TMEM_COLS);
     tmem_relinquish();
   }
+  griddep_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1956,8 +1964,19 @@ cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8><<<grid, kThreads, P::SMEM_LAUNCH, stream>>>(kp);
-  return cudaGetLastError();
+  // a programmatic dependent of the kernel before it on the stream (the
+  // kernel waits for it before its first global access)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = P::SMEM_LAUNCH;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8>, kp);
 }
 
 }  // namespace attn

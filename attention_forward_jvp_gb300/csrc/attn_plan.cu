@@ -24,6 +24,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_jagged_kernel(const int* of
                                                                    int2* list, int* count,
                                                                    int capacity) {
   extern __shared__ int bins[];  // one counter per cost 0 .. nbins-1
+  // the attention kernel after this one may start its prologue now (it
+  // waits for this kernel to complete before it reads the list)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int nbins = (max_seq_len + kPlanBN - 1) / kPlanBN + 1;
   for (int i = threadIdx.x; i < nbins; i += blockDim.x) bins[i] = 0;
   __syncthreads();
@@ -64,6 +67,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_jagged_kernel(const int* of
 __global__ void __launch_bounds__(256) plan_keylen_kernel(const unsigned char* mask, long long s0,
                                                           long long s1, long long s3, int H, int N,
                                                           int* keylen) {
+  // the attention kernel after this one may start its prologue now (it
+  // waits for this kernel to complete before it reads the key lengths)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int bh = blockIdx.x;
   const int b = bh / H, h = bh % H;
   const unsigned char* row = mask + b * s0 + h * s1;
