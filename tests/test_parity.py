@@ -75,12 +75,14 @@ def oracle_dense(inp):
 
 
 # ------------------------------------------------------------ full configs
-@pytest.mark.parametrize("name", ["tiny", "noncausal", "causal", "jagged", "bias_mask"])
+@pytest.mark.parametrize("name", ["tiny", "noncausal", "causal", "jagged", "bias_mask", "causal_d256"])
 def test_full_size_whole_output(name):
-    """Each of the five workloads at full size, in the launch configuration the benchmark
-    times (persistent grid, snake unit order, jagged cost-ordered work list),
-    into NaN-prefilled outputs; every element of O, tO and LSE against the
-    float64 oracle over all heads (jagged: all sequences)."""
+    """Each benchmark workload at full size (the five configurations and
+    the head-dim-256 line), in the launch configuration the benchmark times
+    (persistent grid, snake unit order, jagged cost-ordered work list, head
+    groups at Dqk = 256), into NaN-prefilled outputs; every element of O, tO
+    and LSE against the float64 oracle over all heads (jagged: all
+    sequences)."""
     w = WORKLOADS[name]
     inp = make_inputs(w)
     O, tO, L = run_gpu(inp, nan_prefill=True)
@@ -332,6 +334,8 @@ D256_JVP = [
     ("128x256_causal", dict(B=1, H=2, M=300, N=300, Dqk=128, Dv=256, causal=True)),
     ("16x256_bias_mask", dict(B=1, H=2, M=130, N=200, Dqk=16, Dv=256, bias=True, mask_keep=150)),
     ("128x256_many_units", dict(B=2, H=8, M=1024, N=1024, Dqk=128, Dv=256, causal=True)),
+    # eight (b, h): the causal Dqk = 256 units walk the heads in four groups
+    ("256x256_causal_head_groups", dict(B=2, H=4, M=333, N=333, Dqk=256, Dv=256, causal=True)),
 ]
 
 
