@@ -135,6 +135,35 @@ def test_many_units_per_cta_with_odd_tile_counts(case):
         assert_close(O, tO, L, *ref, what=f"{case} run {rep}")
 
 
+def test_inputs_written_by_the_kernels_just_before():
+    """The forward kernel is launched as a programmatic dependent of the
+    kernel before it on the stream, so its prologue may run while that
+    kernel is still writing.  Here every input is produced on the device
+    by kernels launched immediately before the call (no synchronisation),
+    the last of them rewriting Q in place; the outputs start as NaN and
+    every element is compared with the oracle."""
+    B, H, N, D = 1, 6, 700, 64
+    g = torch.Generator(device="cuda").manual_seed(81)
+    dev_in = [torch.randn((B, H, N, D), generator=g, device="cuda", dtype=torch.float32) for _ in range(6)]
+    q_src = dev_in[0].to(torch.bfloat16)
+    inp = {"causal": True, "sm_scale": 0.125, "offsets": None, "max_seq_len": None, "bias": None, "mask": None}
+    names = ("q", "k", "v", "tq", "tk", "tv")
+    torch.cuda.synchronize()
+    # launched back to back on the current stream, the attention call last
+    bf = [t.to(torch.bfloat16) for t in dev_in]
+    q = torch.zeros_like(q_src)
+    q.copy_(q_src)
+    o = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    to = torch.full_like(o, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    out = binding.attn_fwd_jvp(q, *bf[1:], causal=True, sm_scale=0.125, out=(o, to, lse))
+    assert binding.sync_check() == 0
+    for n, t in zip(names, [q] + bf[1:]):
+        inp[n] = t.cpu()
+    O, tO, L = (x.float().cpu().numpy() for x in out)
+    assert_close(O, tO, L, *oracle_dense(inp), what="inputs written just before the call")
+
+
 # ------------------------------------------------------------- edge shapes
 EDGE = [
     # B, H, M, N, Dqk, Dv, causal
