@@ -164,6 +164,64 @@ def test_inputs_written_by_the_kernels_just_before():
     assert_close(O, tO, L, *oracle_dense(inp), what="inputs written just before the call")
 
 
+def _random_case(rng):
+    """One seeded draw over the supported space: head dims for Q / K and V
+    independently in {16, 32, 64, 128, 256}, dense (causal, cross-attention
+    lengths, bias and / or key mask) or jagged (lengths around tile edges,
+    causal or not), bf16 or fp16 storage."""
+    dims = [16, 32, 64, 128, 256]
+    dqk, dv = int(rng.choice(dims)), int(rng.choice(dims))
+    jagged = rng.random() < 0.3
+    causal = rng.random() < 0.4
+    scale = float(rng.choice([0.125, 0.2, 1.0 / math.sqrt(dqk)]))
+    if jagged:
+        nb = int(rng.integers(1, 7))
+        msl = int(rng.choice([64, 100, 200, 300]))
+        lens = [int(x) for x in rng.integers(0, msl + 70, nb)]
+        w = Workload("rj", B=nb, H=int(rng.integers(1, 4)), Dqk=dqk, Dv=dv, jagged=True, max_seq_len=msl,
+                     max_len_draw=1, causal=causal, sm_scale=scale)
+        return w, lens, None
+    M = int(rng.integers(1, 520))
+    N = M if causal else int(rng.integers(1, 520))
+    bias = rng.random() < 0.35
+    w = Workload("rd", B=int(rng.integers(1, 3)), H=int(rng.integers(1, 4)), M=M, N=N, Dqk=dqk, Dv=dv,
+                 causal=causal, bias=bias, sm_scale=scale)
+    mask_kind = int(rng.integers(0, 3)) if rng.random() < 0.35 else None
+    return w, None, mask_kind
+
+
+@pytest.mark.parametrize("seed", list(range(24)))
+def test_random_shapes_whole_output(seed):
+    """Seeded random draws over head dims, lengths, causal, bias / mask,
+    jagged and fp16 (see _random_case); NaN-prefilled outputs, every
+    element against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    w, lens, mask_kind = _random_case(rng)
+    inp = make_inputs(w, seed=2000 + seed, lengths=lens)
+    if mask_kind is not None:
+        g = torch.Generator().manual_seed(3000 + seed)
+        if mask_kind == 0:    # key padding per batch, [B, 1, 1, N]
+            m = torch.zeros((w.B, 1, 1, w.N), dtype=torch.uint8)
+            for b in range(w.B):
+                m[b, ..., : int(torch.randint(0, w.N + 1, (1,), generator=g))] = 1
+        elif mask_kind == 1:  # per (b, h) key mask with holes, [B, H, 1, N]
+            m = (torch.rand((w.B, w.H, 1, w.N), generator=g) < 0.7).to(torch.uint8)
+        else:                 # full [B, H, M, N] mask
+            m = (torch.rand((w.B, w.H, w.M, w.N), generator=g) < 0.6).to(torch.uint8)
+        inp["mask"] = m
+    if rng.random() < 0.3:
+        inp = _to_f16(inp)
+    O, tO, L = run_gpu(inp, nan_prefill=True)
+    assert not np.isnan(O).any() and not np.isnan(tO).any() and not np.isnan(L).any(), "unwritten output"
+    if w.jagged:
+        ref = oracle.attention_fwd_jvp_jagged(inp["q"], inp["k"], inp["v"], inp["tq"], inp["tk"], inp["tv"],
+                                              inp["offsets"], w.max_seq_len, causal=w.causal,
+                                              sm_scale=inp["sm_scale"])
+    else:
+        ref = oracle_dense(inp)
+    assert_close(O, tO, L, *ref, what=f"seed {seed}: {w}")
+
+
 # ------------------------------------------------------------- edge shapes
 EDGE = [
     # B, H, M, N, Dqk, Dv, causal
