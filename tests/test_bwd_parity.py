@@ -247,3 +247,59 @@ def test_bwd_with_bias_fp16():
     inp["bias"], inp["mask"] = _bias_mask(1, w.H, w.M, w.N, "bias+rowmask", seed=74)
     assert_grads_close(run_gpu_bwd(inp, f16=True), oracle_bwd(inp, f16=True), what="fp16 bias")
 
+
+
+def _random_bwd_case(rng):
+    """One seeded draw over the backward's supported set: head dims for Q / K
+    and V independently in {16, 32, 64, 128}; dense (causal, cross-attention
+    lengths, bias and / or key mask) or jagged (lengths around tile edges
+    and past the cap); bf16 or fp16."""
+    dims = [16, 32, 64, 128]
+    dqk, dv = int(rng.choice(dims)), int(rng.choice(dims))
+    causal = rng.random() < 0.4
+    if rng.random() < 0.3:
+        nb = int(rng.integers(1, 6))
+        msl = int(rng.choice([64, 130, 256]))
+        lens = [int(x) for x in rng.integers(0, msl + 60, nb)]
+        return Workload("rbj", B=nb, H=int(rng.integers(1, 3)), Dqk=dqk, Dv=dv, jagged=True, max_seq_len=msl,
+                        max_len_draw=1, causal=causal), lens, False, None
+    M = int(rng.integers(1, 400))
+    N = M if causal else int(rng.integers(1, 400))
+    w = Workload("rbd", B=int(rng.integers(1, 3)), H=int(rng.integers(1, 3)), M=M, N=N, Dqk=dqk, Dv=dv,
+                 causal=causal)
+    return w, None, rng.random() < 0.3, (int(rng.integers(0, 2)) if rng.random() < 0.3 else None)
+
+
+@pytest.mark.parametrize("seed", list(range(16)))
+def test_bwd_random_shapes(seed):
+    """Seeded random draws (see _random_bwd_case): the library's forward
+    then backward, every gradient against the float64 oracle."""
+    rng = np.random.default_rng(500 + seed)
+    w, lens, bias, mask_kind = _random_bwd_case(rng)
+    f16 = rng.random() < 0.3
+    inp = make_bwd_inputs(w, seed=600 + seed, lengths=lens)
+    if w.jagged:
+        cast = (lambda t: t.float().half()) if f16 else (lambda t: t)
+        q, k, v, do = (cast(inp[n]).cuda() for n in ("q", "k", "v", "do"))
+        kw = dict(causal=w.causal, sm_scale=inp["sm_scale"], offsets=inp["offsets"].cuda(),
+                  max_seq_len=w.max_seq_len)
+        o, lse = binding.attn_fwd(q, k, v, **kw)
+        dq, dk, dv, delta = binding.attn_bwd(q, k, v, o, lse, do, **kw)
+        assert binding.sync_check() == 0
+        got = tuple(t.float().cpu().numpy() for t in (dq, dk, dv, delta))
+        ref = oracle.attention_bwd_jagged(*(cast(inp[n]) for n in ("q", "k", "v", "do")), inp["offsets"],
+                                          w.max_seq_len, causal=w.causal, sm_scale=inp["sm_scale"])
+    else:
+        g = torch.Generator().manual_seed(700 + seed)
+        if bias:
+            inp["bias"] = torch.randn((w.B, w.H, w.M, w.N), generator=g)
+        if mask_kind == 0:
+            m = torch.zeros((w.B, 1, 1, w.N), dtype=torch.uint8)
+            for b in range(w.B):
+                m[b, ..., : int(torch.randint(0, w.N + 1, (1,), generator=g))] = 1
+            inp["mask"] = m
+        elif mask_kind == 1:
+            inp["mask"] = (torch.rand((w.B, w.H, w.M, w.N), generator=g) < 0.6).to(torch.uint8)
+        got = run_gpu_bwd(inp, f16=f16)
+        ref = oracle_bwd(inp, f16=f16)
+    assert_grads_close(got, ref, what=f"seed {seed}: {w} bias={bias} mask={mask_kind} f16={f16}")

@@ -158,3 +158,21 @@ def test_fp8_guard_bands(N):
         assert torch.all(o.view(torch.uint8) == 0) and torch.all(torch.isneginf(lse))
     else:
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("seed", list(range(8)))
+def test_fp8_random_shapes(seed):
+    """Seeded random draws over the e5m2 forward's supported set (D = 64 or
+    128, key length a multiple of 16, causal with M = N), against the
+    oracle's e5m2 step order and bound."""
+    rng = np.random.default_rng(800 + seed)
+    D = int(rng.choice([64, 128]))
+    causal = rng.random() < 0.5
+    N = 16 * int(rng.integers(1, 48))
+    M = N if causal else int(rng.integers(1, 700))
+    B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+    q, k, v = make_f8(B, H, M, N, D, seed=900 + seed)
+    s = float(rng.choice([D ** -0.5, 0.2]))
+    O, L = run_f8(q, k, v, causal, s)
+    Or, Lr = oracle.attention_fwd_e5m2(q, k, v, causal=causal, sm_scale=s)
+    assert_f8_close(O, L, Or, Lr, *bound_terms(q, k, v, causal, s), f"seed {seed}: B{B} H{H} M{M} N{N} D{D} causal={causal}")
