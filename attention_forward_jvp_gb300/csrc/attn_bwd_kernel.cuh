@@ -50,6 +50,11 @@ struct BwdParams {
   int max_seq_len;     // jagged: cap on a sequence's length
   int n_rt;       // row tiles of 128 per (b, h) (jagged: per max_seq_len)
   int num_units;  // B * H * n_rt
+  // Jagged work list (optional): unit_count[0] (sequence, row tile) pairs,
+  // costliest first, at unit_list (x = sequence, y = tile); unit u is pair
+  // u / H, head u % H.  A count of -1 means the list was not written.
+  const int2* unit_list;
+  const int* unit_count;
   float scale_log2;  // sm_scale * log2(e)
   float sm_scale;
   const float* lse;    // [B, H, M] (jagged [H, T]), natural log
@@ -127,8 +132,9 @@ struct BwdUnit {
 
 // Unit u, costliest first: dense causal dQ units by descending query tile,
 // causal KV units by ascending key tile (more query tiles above the
-// diagonal); jagged units by descending row tile (a high tile only exists
-// in a long sequence) except causal KV, ascending.  A jagged unit past its
+// diagonal); jagged units from the work list when one was written (ordered
+// by cost), else by descending row tile (a high tile only exists in a long
+// sequence) except causal KV, ascending.  A jagged unit past its
 // sequence's length has no rows and nt = 0.
 template <bool KV>
 __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
@@ -149,9 +155,18 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int u) {
     w.qrow0 = static_cast<long long>(w.z) * p.M;
     w.orow0 = static_cast<long long>(w.z) * (KV ? p.N : p.M);
   } else {
-    const int tile = u / BH, r = u % BH;
-    w.rt = (KV && p.causal) ? tile : p.n_rt - 1 - tile;
-    const int b = r / p.H, h = r % p.H;
+    int b, h;
+    if (p.unit_list != nullptr && __ldg(p.unit_count) >= 0) {
+      const int2 e = p.unit_list[u / p.H];
+      b = e.x;
+      w.rt = e.y;
+      h = u % p.H;
+    } else {
+      const int tile = u / BH, r = u % BH;
+      w.rt = (KV && p.causal) ? tile : p.n_rt - 1 - tile;
+      b = r / p.H;
+      h = r % p.H;
+    }
     const int begin = __ldg(p.offsets + b), end = __ldg(p.offsets + b + 1);
     const int len = max(0, min(end - begin, p.max_seq_len));
     q_len = k_len = len;
@@ -229,6 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.err, p.timeout_ns};
   auto unit_at = [&](int rnd) { return unit_of_round(rnd); };
+  // The units this launch walks: a jagged work list when one was written
+  // (by the planning kernel earlier on the stream), else the slot order;
+  // read from the parameters at each unit, so the dense kernels' loops
+  // carry nothing for it.
+  auto units_end = [&]() -> int {
+    if (p.unit_list != nullptr) {
+      const int c = __ldg(p.unit_count);
+      if (c >= 0) return c * p.H;
+    }
+    return p.num_units;
+  };
 
   if (warp < 4) {
     setmaxnreg_dec<kLowRegs>();
@@ -239,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         bool ok = true;
         for (int rnd = 0; ok; ++rnd) {
           const int u = unit_at(rnd);
-          if (u >= p.num_units) break;
+          if (u >= units_end()) break;
           const BwdUnit w = bwd_unit<KV>(p, u);
           if (w.nt == 0) continue;
           ok = wait_bar(bar(P::B_RE), (rfill & 1u) ^ 1u, W);
@@ -311,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         uint32_t ruse = 0;
         for (int rnd = 0; ok; ++rnd) {
           const int u = unit_at(rnd);
-          if (u >= p.num_units) break;
+          if (u >= units_end()) break;
           const BwdUnit w = bwd_unit<KV>(p, u);
           if (w.nt == 0) continue;
           ok = wait_all(bar(P::B_RF), ruse & 1u);
@@ -357,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       } else {
         for (int rnd = 0; ok; ++rnd) {
           const int u = unit_at(rnd);
-          if (u >= p.num_units) break;
+          if (u >= units_end()) break;
           const BwdUnit w = bwd_unit<KV>(p, u);
           if (w.nt == 0) continue;
           for (int j = 0; j < w.nt; ++j, ++g) {
@@ -417,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_at(rnd);
-      if (u >= p.num_units) break;
+      if (u >= units_end()) break;
       const BwdUnit w = bwd_unit<KV>(p, u);
       const int ri = w.rt * kBM + row;  // this thread's row (query for dQ, key for KV)
       const bool row_ok = ri < w.rows;

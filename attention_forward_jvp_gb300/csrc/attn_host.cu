@@ -697,6 +697,22 @@ attn_status run_bwd(const attn_shape* s, const void* q, const void* k, const voi
     const int64_t units = BH * bp.n_rt;
     if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     bp.num_units = static_cast<int>(units);
+    // Jagged: order this pass's (sequence, row tile) pairs by cost on the
+    // device (the offsets live there) so the kernel can balance them; the
+    // dK / dV pass counts query tiles per key tile.  (The second pass's
+    // planning kernel runs after the first pass's kernel has read the list.)
+    if (jagged && attn::plan_jagged_supported(s->max_seq_len)) {
+      int* lbuf = nullptr;
+      const attn_status ls = stream_list(cs, &lbuf);
+      if (ls != ATTN_OK) return ls;
+      int2* list = reinterpret_cast<int2*>(reinterpret_cast<char*>(lbuf) + kListOffsetBytes);
+      if (attn::launch_plan_jagged(offsets, s->B, s->max_seq_len, causal ? 1 : 0, list, lbuf, kListCapacity,
+                                   cs, kv ? 1 : 0) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      g_launches.fetch_add(1);
+      bp.unit_list = list;
+      bp.unit_count = lbuf;
+    }
     const int grid = static_cast<int>(units < ds->num_sms ? units : ds->num_sms);
     if (dispatch_bwd(key, kv, f16, has_bias, bp, grid, cs) != cudaSuccess) return ATTN_ERR_CUDA;
     g_launches.fetch_add(1);

@@ -1,7 +1,8 @@
-// Work list for jagged launches: every (sequence, query tile) pair that has
-// rows, ordered by decreasing cost (key tiles it visits), so that the
-// attention kernel's snake walk over the list gives each SM a near-equal
-// share (longest-processing-time-first).  One block, counting sort by cost.
+// Work list for jagged launches: every (sequence, row tile) pair that has
+// rows, ordered by decreasing cost (the 64-wide tiles it streams), so that
+// the attention kernels' snake walk over the list gives each SM a
+// near-equal share (longest-processing-time-first).  One block, counting
+// sort by cost.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -14,7 +15,12 @@ namespace {
 
 constexpr int kPlanThreads = 512;
 
-__device__ __forceinline__ int pair_cost(int len, int mt, int causal) {
+__device__ __forceinline__ int pair_cost(int len, int mt, int causal, int kv) {
+  if (kv) {
+    // the queries of a key tile: from its first row on under the causal mask
+    const int all = (len + kPlanBN - 1) / kPlanBN;
+    return causal ? all - mt * (kPlanBM / kPlanBN) : all;
+  }
   const int hi = causal ? min(len, (mt + 1) * kPlanBM) : len;
   return (hi + kPlanBN - 1) / kPlanBN;
 }
@@ -22,7 +28,7 @@ __device__ __forceinline__ int pair_cost(int len, int mt, int causal) {
 __global__ void __launch_bounds__(kPlanThreads) plan_jagged_kernel(const int* offsets, int B,
                                                                    int max_seq_len, int causal,
                                                                    int2* list, int* count,
-                                                                   int capacity) {
+                                                                   int capacity, int kv) {
   extern __shared__ int bins[];  // one counter per cost 0 .. nbins-1
   // the attention kernel after this one may start its prologue now (it
   // waits for this kernel to complete before it reads the list)
@@ -32,7 +38,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_jagged_kernel(const int* of
   __syncthreads();
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const int len = min(offsets[b + 1] - offsets[b], max_seq_len);
-    for (int mt = 0; mt * kPlanBM < len; ++mt) atomicAdd(&bins[pair_cost(len, mt, causal)], 1);
+    for (int mt = 0; mt * kPlanBM < len; ++mt) atomicAdd(&bins[pair_cost(len, mt, causal, kv)], 1);
   }
   __syncthreads();
   __shared__ int total;
@@ -51,7 +57,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_jagged_kernel(const int* of
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const int len = min(offsets[b + 1] - offsets[b], max_seq_len);
     for (int mt = 0; mt * kPlanBM < len; ++mt) {
-      const int pos = atomicAdd(&bins[pair_cost(len, mt, causal)], 1);
+      const int pos = atomicAdd(&bins[pair_cost(len, mt, causal, kv)], 1);
       list[pos] = make_int2(b, mt);
     }
   }
@@ -134,11 +140,11 @@ cudaError_t launch_plan_keylen(const unsigned char* mask, const long long* strid
 bool plan_jagged_supported(int max_seq_len) { return max_seq_len >= 0 && max_seq_len <= kPlanMaxSeqLen; }
 
 cudaError_t launch_plan_jagged(const int* offsets, int B, int max_seq_len, int causal, int2* list,
-                               int* count, int capacity, cudaStream_t stream) {
+                               int* count, int capacity, cudaStream_t stream, int kv) {
   const int nbins = (max_seq_len + kPlanBN - 1) / kPlanBN + 1;
   const size_t smem = static_cast<size_t>(nbins) * sizeof(int);
   plan_jagged_kernel<<<1, kPlanThreads, smem, stream>>>(offsets, B, max_seq_len, causal, list,
-                                                        count, capacity);
+                                                        count, capacity, kv);
   return cudaGetLastError();
 }
 

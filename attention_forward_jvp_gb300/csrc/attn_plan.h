@@ -11,11 +11,15 @@ constexpr int kPlanListBytes = 1 << 20;  // list capacity in the per-device scra
 
 bool plan_jagged_supported(int max_seq_len);
 
-// Writes count[0] = number of (sequence, query tile) pairs with rows (or -1
+// Writes count[0] = number of (sequence, row tile) pairs with rows (or -1
 // when more than `capacity`) and list[0 .. count) = those pairs as
-// (sequence, tile), costliest first.  Asynchronous on `stream`.
+// (sequence, tile), costliest first.  The cost of a pair is the number of
+// 64-wide tiles its row tile streams: keys for a query tile (kv = 0, the
+// forward and the backward's dQ pass), queries for a key tile (kv = 1, the
+// backward's dK / dV pass: under the causal mask, those from the tile's
+// first row to the sequence end).  Asynchronous on `stream`.
 cudaError_t launch_plan_jagged(const int* offsets, int B, int max_seq_len, int causal, int2* list,
-                               int* count, int capacity, cudaStream_t stream);
+                               int* count, int capacity, cudaStream_t stream, int kv = 0);
 
 // Writes keylen[b * H + h] = 1 + the last key j < N with mask[b, h, ., j]
 // nonzero (0 when none), bit 31 set when every key below it is nonzero, for
