@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // causal units at Dqk = 256 walk the heads in four groups: each query
   // tile's score work re-reads K / V (two column slices with tangents), and
   // keeping a quarter of the heads' K / V in L2 outweighs the coarser
-  // balance (measured: 930 -> 865 us on B2 H16 N4096; at Dqk = 128, where
+  // balance (measured: 930 -> 857 us on B2 H16 N4096; at Dqk = 128, where
   // the reads are far from the HBM roof, grouping was slower)
   constexpr int kHeadGroups = DQK >= 256 ? 4 : 1;
   constexpr bool BM = BMODE != kNoBias;
