@@ -182,7 +182,15 @@ struct Plan {
   static constexpr int RING = BUDGET - NB * BIAS_STAGE;
   // (one K stage only when two do not fit: Dqk = 256 with tangents, whose
   // Q and tQ take 128 KB)
-  static constexpr int NK = (FIXED + 4 * K_STAGE + 4 * V_STAGE <= RING)   ? 4
+  // With one Q buffer and K / V stages of the same size (Dqk = Dv = 128
+  // with tangents, no bias), three K stages and two V stages fit, and so do
+  // two and three: the second measured faster (causal B2 H16 N4096:
+  // 257.7 -> 250.7 us), so there the V ring gets the third stage.
+  static constexpr bool V3 = !F8 && BMODE == kNoBias && NQB == 1 && K_STAGE == V_STAGE &&
+                             FIXED + 2 * K_STAGE + 3 * V_STAGE <= RING &&
+                             FIXED + 3 * K_STAGE + 3 * V_STAGE > RING;
+  static constexpr int NK = V3 ? 2
+                            : (FIXED + 4 * K_STAGE + 4 * V_STAGE <= RING) ? 4
                             : (FIXED + 3 * K_STAGE + 2 * V_STAGE <= RING) ? 3
                             : (FIXED + 2 * K_STAGE + V_STAGE <= RING)     ? 2
                                                                           : 1;
