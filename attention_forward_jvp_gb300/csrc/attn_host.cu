@@ -49,6 +49,10 @@ ATTN_FWD_DECL_ALL(64, 256, false)
 ATTN_FWD_DECL_ALL(128, 256, false)
 ATTN_FWD_DECL_ALL(256, 256, false)
 extern template cudaError_t launch_attn<64, 64, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kNoBias, false, false, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kNoBias, false, false, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, true, kNoBias, true, false, true>(const KernelParams&, int, cudaStream_t);
+extern template cudaError_t launch_attn<64, 64, false, kNoBias, true, false, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn<128, 128, false, kNoBias, false, true>(const KernelParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn_bwd<64, 64, false, false, false>(const BwdParams&, int, cudaStream_t);
 extern template cudaError_t launch_attn_bwd<64, 64, false, false, true>(const BwdParams&, int, cudaStream_t);
@@ -129,6 +133,17 @@ cudaError_t dispatch_mode(int kq, int kv, int mode, const attn::KernelParams& kp
     case attn::kBiasGlobal: return dispatch_dims<JVP, attn::kBiasGlobal, F16>(kq, kv, kp, grid, cs);
   }
   return cudaErrorInvalidValue;
+}
+
+// The lean ping-pong kernel: head dims <= 64, no bias or mask, dense,
+// non-causal, N a positive multiple of the 64-key tile.
+cudaError_t dispatch_lean(bool jvp, bool f16, const attn::KernelParams& kp, int grid, cudaStream_t cs) {
+  using namespace attn;
+  if (f16)
+    return jvp ? launch_attn<64, 64, true, kNoBias, true, false, true>(kp, grid, cs)
+               : launch_attn<64, 64, false, kNoBias, true, false, true>(kp, grid, cs);
+  return jvp ? launch_attn<64, 64, true, kNoBias, false, false, true>(kp, grid, cs)
+             : launch_attn<64, 64, false, kNoBias, false, false, true>(kp, grid, cs);
 }
 
 cudaError_t dispatch_attn(int kq, int kv, bool jvp, int mode, bool f16, const attn::KernelParams& kp, int grid,
@@ -451,7 +466,9 @@ attn_status run(const attn_shape* s, const void* q, const void* k, const void* v
   const int mode = (kp.bias == nullptr && kp.mask == nullptr) ? attn::kNoBias
                    : (kp.bias != nullptr && kp.bias_tma == 0) ? attn::kBiasGlobal
                                                                : attn::kBiasRing;
-  e = dispatch_attn(kq, kv, jvp, mode, f16, kp, grid, cs);
+  const bool lean = !jagged && !causal && mode == attn::kNoBias && kq == 64 && kv == 64 && n_vh == 1 &&
+                    s->N > 0 && s->N % attn::kBN == 0 && kp.keylen == nullptr && kp.unit_list == nullptr;
+  e = lean ? dispatch_lean(jvp, f16, kp, grid, cs) : dispatch_attn(kq, kv, jvp, mode, f16, kp, grid, cs);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   g_launches.fetch_add(1);
   return ATTN_OK;

@@ -10,4 +10,7 @@ template cudaError_t launch_attn<64, 64, true, kBiasGlobal, false>(const KernelP
 template cudaError_t launch_attn<64, 64, false, kNoBias, false>(const KernelParams&, int, cudaStream_t);
 template cudaError_t launch_attn<64, 64, false, kBiasRing, false>(const KernelParams&, int, cudaStream_t);
 template cudaError_t launch_attn<64, 64, false, kBiasGlobal, false>(const KernelParams&, int, cudaStream_t);
+// the lean ping-pong variants (dense, non-causal, whole key tiles)
+template cudaError_t launch_attn<64, 64, true, kNoBias, false, false, true>(const KernelParams&, int, cudaStream_t);
+template cudaError_t launch_attn<64, 64, false, kNoBias, false, false, true>(const KernelParams&, int, cudaStream_t);
 }  // namespace attn

@@ -10,4 +10,7 @@ template cudaError_t launch_attn<64, 64, true, kBiasGlobal, true>(const KernelPa
 template cudaError_t launch_attn<64, 64, false, kNoBias, true>(const KernelParams&, int, cudaStream_t);
 template cudaError_t launch_attn<64, 64, false, kBiasRing, true>(const KernelParams&, int, cudaStream_t);
 template cudaError_t launch_attn<64, 64, false, kBiasGlobal, true>(const KernelParams&, int, cudaStream_t);
+// the lean ping-pong variants (dense, non-causal, whole key tiles)
+template cudaError_t launch_attn<64, 64, true, kNoBias, true, false, true>(const KernelParams&, int, cudaStream_t);
+template cudaError_t launch_attn<64, 64, false, kNoBias, true, false, true>(const KernelParams&, int, cudaStream_t);
 }  // namespace attn

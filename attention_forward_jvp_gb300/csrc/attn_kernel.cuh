@@ -274,10 +274,28 @@ struct Unit {
 // a jagged work list is already ordered by cost.  SLICES: the kernel may
 // run output column slices (tangents with a 128-wide kernel DV); other
 // kernels carry no slice arithmetic.  NG > 1: causal dense units take the
-// heads in NG groups, one group after the other.
-template <bool SLICES, int NG>
+// heads in NG groups, one group after the other.  LEAN: dense, non-causal,
+// no key mask, every key tile whole (N a positive multiple of the key
+// tile): unit u is query tile u % n_mt of (b, h) = u / n_mt.
+template <bool SLICES, int NG, bool LEAN = false>
 __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u, const int2* list) {
   Unit w;
+  if constexpr (LEAN) {
+    const int bh = u / p.n_mt;
+    w.vh = 0;
+    w.mask_on = false;
+    w.b = bh / p.H;
+    w.h = bh % p.H;
+    w.z = bh;
+    w.row0 = 0;
+    w.mt = u % p.n_mt;
+    w.q_len = p.M;
+    w.kv_len = p.N;
+    w.out0 = static_cast<long long>(bh) * p.M;
+    w.active = true;
+    w.nt = p.N / kBN;
+    return w;
+  }
   // the column slices of one query tile are adjacent units (they share Q, K
   // and V tiles through L2)
   w.vh = 0;
@@ -538,9 +556,13 @@ __device__ __forceinline__ float rowmax32(const float* x) {
 // BMODE: kNoBias, kBiasRing or kBiasGlobal (see Plan).  Each mode compiles
 // only its own bias / mask code, which keeps the per-tile loop small.
 // F16: fp16 inputs, MMA operands and outputs instead of bf16.
-template <int DQK, int DV, bool JVP, int BMODE, bool F16, bool F8 = false>
+template <int DQK, int DV, bool JVP, int BMODE, bool F16, bool F8 = false, bool LEAN = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KernelParams p) {
   using P = Plan<DQK, DV, JVP, BMODE, F8>;
+  // LEAN: the ping-pong kernel compiled for dense non-causal problems whose
+  // key tiles are all whole (no masking, no jagged or causal unit decode,
+  // no empty rows): the kernel's speed depends on its code size
+  static_assert(!LEAN || P::PP, "the lean variant is a ping-pong kernel");
   // output column slices (tangents at Dv = 256 run the 128-wide kernels)
   constexpr bool kSlices = JVP && DV == 128;
   // causal units at Dqk = 256 walk the heads in four groups: each query
@@ -629,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // (by the planning kernel earlier on the stream), else the slot order.
   const int2* list = nullptr;
   int num_units = p.num_units;
-  if (p.unit_list != nullptr) {
+  if (!LEAN && p.unit_list != nullptr) {
     const int c = __ldg(p.unit_count);
     if (c >= 0) {
       list = p.unit_list;
@@ -650,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit<kSlices, kHeadGroups>(p, u, list);
+        const Unit w = decode_unit<kSlices, kHeadGroups, LEAN>(p, u, list);
         if (w.nt == 0) continue;
         const uint32_t qb = qfill % P::NQB;
         ok = wait_bar(bar(P::B_QE + qb), ((qfill / P::NQB) & 1u) ^ 1u, W);
@@ -738,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit<kSlices, kHeadGroups>(p, u, list);
+        const Unit w = decode_unit<kSlices, kHeadGroups, LEAN>(p, u, list);
         for (int j = 0; j < w.nt; ++j) {
           const int r = w.row0 + j * kBN;
           if constexpr (P::NB > 0) {
@@ -811,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_of_round(rnd);
       if (u >= num_units) break;
-      const Unit w = decode_unit<kSlices, kHeadGroups>(p, u, list);
+      const Unit w = decode_unit<kSlices, kHeadGroups, LEAN>(p, u, list);
       if (w.nt == 0) continue;
       for (int j = 0; j < w.nt; ++j, ++g) {
         ok = __all_sync(0xffffffffu, wait_bar_sleep(bar(P::B_SF + (g & 1u)), (g >> 1) & 1u, W));
@@ -1018,7 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit<kSlices, kHeadGroups>(p, u, list);
+        const Unit w = decode_unit<kSlices, kHeadGroups, LEAN>(p, u, list);
         if (w.nt == 0) continue;
         ok = wait_all(bar(P::B_QF), quse & 1u);
         if (!ok) break;
@@ -1055,7 +1077,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit<kSlices, kHeadGroups>(p, u, list);
+        const Unit w = decode_unit<kSlices, kHeadGroups, LEAN>(p, u, list);
         if (w.nt == 0) continue;
         const uint32_t qb = quse % P::NQB;
         ok = wait_all(bar(P::B_QF + qb), (quse / P::NQB) & 1u);
@@ -1367,11 +1389,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const int u = unit_of_round(rnd);
             if (u >= num_units) break;
             ++rnd;
-            w = decode_unit<kSlices, kHeadGroups>(p, u, list);
+            w = decode_unit<kSlices, kHeadGroups, LEAN>(p, u, list);
             if (!w.active) continue;
             qi = w.mt * kBM + row;
             const bool row_ok = qi < w.q_len;
-            if (w.nt == 0) {  // no keys at all: empty rows (this warp: columns [par DVH, ...))
+            if (!LEAN && w.nt == 0) {  // no keys at all: empty rows (this warp: columns [par DVH, ...))
               const int ncol = min(DVH, p.dv_out - par * DVH);
               if (row_ok && ncol > 0) {
                 uint32_t z[DVH / 2];
@@ -1396,8 +1418,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ok = __all_sync(0xffffffffu, wait_bar(bar(P::B_SF + sb), (gt >> 1) & 1u, W));
           if (!ok) break;
           tc_fence_after();
-          const bool diag = p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
-          const bool fast = !diag && (j * kBN + kBN <= w.kv_len);
+          const bool diag = !LEAN && p.causal && (j * kBN + kBN - 1 > w.mt * kBM);
+          const bool fast = LEAN || (!diag && (j * kBN + kBN <= w.kv_len));
           uint32_t s0[kHalf], s1[kHalf];
           tmem_ld_32x32b_x32(tl + sb * P::SBUF, s0);
           tmem_ld_32x32b_x32(tl + sb * P::SBUF + kHalf, s1);
@@ -1532,7 +1554,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_of_round(rnd);
         if (u >= num_units) break;
-        const Unit w = decode_unit<kSlices, kHeadGroups>(p, u, list);
+        const Unit w = decode_unit<kSlices, kHeadGroups, LEAN>(p, u, list);
         if (!w.active) continue;
         const int qi = w.mt * kBM + row;
         const bool row_ok = qi < w.q_len;
@@ -1969,7 +1991,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, P::TMEM_COLS);
 }
 
-template <int DQK, int DV, bool JVP, int BMODE, bool F16, bool F8 = false>
+template <int DQK, int DV, bool JVP, int BMODE, bool F16, bool F8 = false, bool LEAN = false>
 cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
   using P = Plan<DQK, DV, JVP, BMODE, F8>;
   static_assert(P::FITS, "shared memory plan exceeds 227 KB");
@@ -1982,11 +2004,11 @@ cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
     // computed for; a build that compiled to another count is refused
     // (setmaxnreg.inc would otherwise wait for registers that never free).
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8>);
+    e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8, LEAN>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8, LEAN>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -2003,7 +2025,7 @@ cudaError_t launch_attn(const KernelParams& kp, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8>, kp);
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<DQK, DV, JVP, BMODE, F16, F8, LEAN>, kp);
 }
 
 }  // namespace attn

@@ -497,6 +497,24 @@ def test_fp16_storage(name, kw):
     assert_close(O, tO, L, *oracle_dense(inp), what=f"fp16 {name}")
 
 
+@pytest.mark.parametrize("f16", [False, True])
+def test_whole_key_tiles_dense_noncausal(f16):
+    """Dense non-causal problems with head dims <= 64, no bias or mask and N
+    a multiple of 64 run a lean instantiation of the ping-pong kernel (no
+    masking, jagged or causal decode): forward + JVP against the oracle,
+    NaN-prefilled, with a query tail and small head dims; the forward only
+    bit-identical to its primal outputs."""
+    for kw, seed in ((dict(B=2, H=3, M=200, N=320, Dqk=64, Dv=64), 81),
+                     (dict(B=1, H=2, M=130, N=64, Dqk=32, Dv=16), 82)):
+        inp = make_inputs(Workload("lean", sm_scale=0.125, **kw), seed=seed)
+        if f16:
+            inp = _to_f16(inp)
+        O, tO, L = run_gpu(inp, nan_prefill=True)
+        assert_close(O, tO, L, *oracle_dense(inp), what=f"lean {kw} f16={f16}")
+        O2, L2 = run_gpu(inp, jvp=False, nan_prefill=True)
+        assert np.array_equal(O, O2) and np.array_equal(L, L2)
+
+
 def test_fp16_jagged_and_forward_only():
     lens = [3, 64, 130, 257, 1]
     w = Workload("jf16", B=len(lens), H=2, Dqk=64, Dv=64, jagged=True, max_seq_len=300,
